@@ -1,0 +1,483 @@
+"""Benchmark of the ParisKV decode step on GB300.
+
+One step = one decode step of one layer of the Llama-3.1-8B-shaped workload:
+paris_append_decode (new token per KV head, flush every 128 steps),
+paris_retrieve (32 query heads over a 131072-token context) and
+paris_sparse_attend.  Layer contexts are rotated so the working set is far
+larger than L2.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "keys scanned/s & µs per decode step (frac. of HBM peak); recall@k vs exact top-k"
+UNIT = "keys/s"
+
+WORKLOADS = {
+    # Llama-3.1-8B-shaped decode layer: batch 1, 32 q / 8 KV heads, d = 128,
+    # 131072-token bf16 context, sink 16, local 512, update buffer 128,
+    # B = 16 (m = 8), rho = 4, candidates 5%, k = 1024.
+    "llama8b-128k": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16, local=512,
+                         update_buf=128, topk=1024, cand_bp=500, context=131072, layers=8),
+    # the small case the oracle finishes in seconds
+    "tiny-4k": dict(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=128, n_sub=16, rho=4, sink=0, local=0,
+                    update_buf=128, topk=64, cand_bp=1000, context=4096, layers=64),
+}
+DESCRIPTION = {
+    "llama8b-128k": "Llama-3.1-8B-shaped decode layer, 131072-token context",
+    "tiny-4k": "one KV head, 4096 float32 keys",
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_record(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", "kernels_retrieve.cu"), "rb").read() + \
+        open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", "kernels_attend.cu"), "rb").read()
+    sha = hashlib.sha1(src).hexdigest()[:12]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[1] == sha:
+            return float(parts[2])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    from long_context_kv_gb300 import build as B
+    from long_context_kv_gb300 import paris as P
+    from long_context_kv_gb300 import synth
+
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    B.build()
+    P.load()
+    w = WORKLOADS[args.workload]
+    nl = args.layers or w["layers"]
+    ctxlen, d = w["context"], w["head_dim"]
+    b, hkv, hq, S = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["sink"]
+    per_layer_steps = (args.warmup + 3 * args.steps + nl - 1) // nl + 2
+    max_ctx = ctxlen + per_layer_steps + 8
+    fdt = torch.bfloat16 if args.workload != "tiny-4k" else torch.float32
+    seed0 = 20260202 + 1 + 1000 * rank
+    gen = torch.Generator(device="cuda")
+    layers = []
+    keep_keys = None
+    t_setup = time.time()
+    for li in range(nl):
+        seed = seed0 + li
+        cfg = P.make_config(batch=b, n_kv_heads=hkv, n_q_heads=hq, head_dim=d, n_sub=w["n_sub"], rho=w["rho"],
+                            sink=S, local=w["local"], update_buf=w["update_buf"], topk=w["topk"],
+                            cand_bp=w["cand_bp"], max_ctx=max_ctx, retrieval_on_host=0)
+        ctx = P.Context(cfg, synth.srht_signs(seed, d))
+        scale = torch.from_numpy(synth.channel_scale(seed, hkv, d)).cuda()
+        gen.manual_seed(seed)
+        K = (torch.randn((b, hkv, ctxlen, d), generator=gen, device="cuda") * scale[None, :, None, :]).to(fdt)
+        V = torch.randn((b, hkv, ctxlen, d), generator=gen, device="cuda").to(fdt)
+        ctx.paris_encode_prefill(K, V, ctxlen)
+        st = ctx.paris_get_state()
+        N0 = st["N"]
+        # per decode step of this layer: new token and the query (a Retrieval-zone key + N(0, 0.5^2))
+        kn = (torch.randn((per_layer_steps, b, hkv, d), generator=gen, device="cuda") * scale[None, None]).to(fdt)
+        vn = torch.randn((per_layer_steps, b, hkv, d), generator=gen, device="cuda").to(fdt)
+        pos = torch.randint(S, S + N0, (per_layer_steps, b, hq), generator=gen, device="cuda")
+        kvh_of = torch.arange(hq, device="cuda") // (hq // hkv)
+        picked = K[torch.arange(b, device="cuda")[None, :, None], kvh_of[None, None, :], pos].float()
+        qs = (picked + 0.5 * torch.randn(picked.shape, generator=gen, device="cuda")).to(fdt).contiguous()
+        if li == 0:
+            keep_keys = K  # layer 0 keys, for recall
+        del K, V, picked
+        idx = torch.empty((b, hq, w["topk"]), dtype=torch.int32, device="cuda")
+        sc = torch.empty((b, hq, w["topk"]), dtype=torch.float32, device="cuda")
+        out = torch.empty((b, hq, d), dtype=torch.bfloat16, device="cuda")
+        layers.append(dict(ctx=ctx, kn=kn, vn=vn, qs=qs, idx=idx, sc=sc, out=out, step=0, N0=N0))
+    torch.cuda.synchronize()
+    log(f"[rank {rank}] setup {time.time() - t_setup:.1f}s, {nl} layer contexts, "
+        f"{torch.cuda.memory_allocated() / 2**30:.1f} GiB allocated by torch")
+
+    def step(i):
+        L = layers[i % nl]
+        j = L["step"]
+        L["step"] = j + 1
+        ctx = L["ctx"]
+        ctx.paris_append_decode(L["kn"][j], L["vn"][j])
+        ctx.paris_retrieve(L["qs"][j], L["idx"], L["sc"])
+        ctx.paris_sparse_attend(L["qs"][j], L["idx"], L["out"])
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+
+    def max_over_ranks(x):
+        if not dist:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        return float(t.item())
+
+    i = 0
+    for _ in range(args.warmup):
+        step(i)
+        i += 1
+    keys_per_step = []
+    counts0 = [L["ctx"].paris_launch_counts() for L in layers]
+    barrier()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            L = layers[i % nl]
+            keys_per_step.append(L["ctx"].paris_get_state()["N"] * b * hkv)
+            step(i)
+            i += 1
+        e1.record(stream)
+        barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    counts1 = [L["ctx"].paris_launch_counts() for L in layers]
+    launches = sum(counts1[li][k] - counts0[li][k] for li in range(nl) for k in counts1[li])
+    keys_total = sum(keys_per_step) * world
+    value = keys_total / (ms / 1e3)
+
+    # profiled pass: the same steps with per-kernel events on the launch stream
+    for L in layers:
+        L["ctx"].paris_profile_begin(64 * args.steps)
+    barrier()
+    for _ in range(args.steps):
+        step(i)
+        i += 1
+    prof = {}
+    for L in layers:
+        for k, (t, n) in L["ctx"].paris_profile_end().items():
+            a = prof.setdefault(k, [0.0, 0])
+            a[0] += t
+            a[1] += n
+    kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
+    retrieve_kernels = ("qprep", "vote", "select_rerank", "topk")
+    us_retrieve = sum(1e3 * prof[k][0] for k in retrieve_kernels) / args.steps
+    us_attend = sum(1e3 * prof[k][0] for k in ("attn_partial", "attn_combine")) / args.steps
+    us_append = sum(1e3 * prof[k][0] for k in ("append", "build_index")) / args.steps
+
+    # roofline of the dominant kernel (algorithmic bytes per launch)
+    Nmean = sum(keys_per_step) / len(keys_per_step) / (b * hkv)
+    C = max((w["cand_bp"] * int(Nmean) + 9999) // 10000, min(w["topk"], int(Nmean)))
+    keff = min(w["topk"], C)
+    nwin = S + w["local"] + w["update_buf"] // 2
+    alg = {
+        "select_rerank": b * hq * C * (128 + 8),
+        "attn_partial": b * hq * keff * 4 * d + b * hkv * nwin * 4 * d,
+        "topk": b * hq * (C * 8 + keff * 8),
+    }
+    dom = max(kernels, key=lambda k: kernels[k]["us_per_launch"] * kernels[k]["launches"])
+    peak, peak_src = hbm_peak()
+    roof = None
+    if dom in alg:
+        ach = alg[dom] / (kernels[dom]["us_per_launch"] * 1e-6) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom),
+                "algorithmic_bytes": alg[dom]}
+    retr_bytes = alg["select_rerank"] + b * hq * 64 * (Nmean / 256) * 2 * w["rho"] * w["n_sub"] / 4
+    retrieve_frac = retr_bytes / (us_retrieve * 1e-6) / 1e9 / peak
+
+    # end to end through the public API with host buffers
+    L0 = layers[0]
+    h_q = torch.empty(L0["qs"][0].shape, dtype=fdt, pin_memory=True)
+    h_k = torch.empty(L0["kn"][0].shape, dtype=fdt, pin_memory=True)
+    h_v = torch.empty_like(h_k, pin_memory=True)
+    h_idx = torch.empty(L0["idx"].shape, dtype=torch.int32, pin_memory=True)
+    h_sc = torch.empty(L0["sc"].shape, dtype=torch.float32, pin_memory=True)
+    h_out = torch.empty(L0["out"].shape, dtype=torch.bfloat16, pin_memory=True)
+    h_q.copy_(L0["qs"][0])
+    h_k.copy_(L0["kn"][0])
+    h_v.copy_(L0["vn"][0])
+    d_q, d_k, d_v = torch.empty_like(L0["qs"][0]), torch.empty_like(L0["kn"][0]), torch.empty_like(L0["vn"][0])
+    barrier()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    keys_e2e = 0
+    e2.record(stream)
+    for _ in range(args.steps):
+        L = layers[i % nl]
+        keys_e2e += L["ctx"].paris_get_state()["N"] * b * hkv
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        L["ctx"].paris_append_decode(d_k, d_v)
+        L["ctx"].paris_retrieve(d_q, L["idx"], L["sc"])
+        L["ctx"].paris_sparse_attend(d_q, L["idx"], L["out"])
+        h_idx.copy_(L["idx"], non_blocking=True)
+        h_sc.copy_(L["sc"], non_blocking=True)
+        h_out.copy_(L["out"], non_blocking=True)
+        i += 1
+    e3.record(stream)
+    barrier()
+    ms_e2e = max_over_ranks(e2.elapsed_time(e3))
+    h2d = (h_q.numel() * h_q.element_size() + 2 * h_k.numel() * h_k.element_size())
+    d2h = h_idx.numel() * 4 + h_sc.numel() * 4 + h_out.numel() * 2
+
+    # recall@k on layer 0 against the exact float64 top-k of <k, q>
+    recall = None
+    if keep_keys is not None and rank == 0:
+        ctx = L0["ctx"]
+        st = ctx.paris_get_state()
+        N0 = L0["N0"]
+        gen.manual_seed(777)
+        rs = []
+        for t in range(4):
+            pos = torch.randint(S, S + N0, (b, hq), generator=gen, device="cuda")
+            kvh_of = torch.arange(hq, device="cuda") // (hq // hkv)
+            picked = keep_keys[torch.arange(b, device="cuda")[:, None], kvh_of[None, :], pos].float()
+            q = (picked + 0.5 * torch.randn(picked.shape, generator=gen, device="cuda")).to(fdt).contiguous()
+            k_eff = ctx.paris_retrieve(q, L0["idx"], L0["sc"])
+            torch.cuda.synchronize()
+            for s_ in range(b):
+                for h in range(hq):
+                    Kz = keep_keys[s_, h // (hq // hkv), S:S + min(N0, st["N"])].double()
+                    ex = torch.topk(Kz @ q[s_, h].double(), k_eff).indices + S
+                    got = L0["idx"][s_, h, :k_eff].long()
+                    rs.append(torch.isin(got, ex).float().mean().item())
+        recall = sum(rs) / len(rs)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DESCRIPTION[args.workload], "batch": b, "n_q_heads": hq, "n_kv_heads": hkv,
+                   "head_dim": d, "context": ctxlen, "sink": S, "local": w["local"], "update_buf": w["update_buf"],
+                   "n_sub": w["n_sub"], "rho": w["rho"], "cand_pct": w["cand_bp"] / 100, "topk": w["topk"],
+                   "kv_dtype": "bf16" if fdt == torch.bfloat16 else "f32", "layers_rotated": nl,
+                   "l2": f"inputs larger than L2: {nl} layer contexts rotated, each revisited after "
+                         f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"},
+        "us_per_decode_step": 1e3 * ms / args.steps,
+        "us_retrieve": us_retrieve, "us_attend": us_attend, "us_append": us_append,
+        "retrieve_hbm_frac": round(retrieve_frac, 4),
+        "recall_at_k": recall,
+        "kernels": kernels,
+        "roofline": roof,
+        "e2e": {"value": keys_e2e * world / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    return res
+
+
+def cpu_baseline(args):
+    """Time the oracle on the host cores in a fresh single-threaded process."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", args.workload,
+           "--steps", str(args.cpu_steps), "--warmup", str(args.warmup if args.impl == "reference" else 0)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        log(r.stderr[-2000:])
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample(args):
+    """Decode steps of one KV head (its G query heads) of the workload, run
+    by the oracle as it stands; keys scanned = N per step."""
+    import numpy as np
+
+    from long_context_kv_gb300 import synth
+    from oracle import pariskv as o
+
+    w = WORKLOADS[args.workload]
+    d, S, L, U = w["head_dim"], w["sink"], w["local"], w["update_buf"]
+    G = w["n_q_heads"] // w["n_kv_heads"]
+    T = w["context"]
+    seed = 20260202 + 1
+    scale = synth.channel_scale(seed, 1, d)
+    K = synth.keys(seed, 1, 1, 0, T, d, scale)[0, 0]
+    V = synth.values(seed, 1, 1, 0, T, d)[0, 0]
+    bf = args.workload != "tiny-4k"
+    if bf:
+        import torch
+        K = torch.from_numpy(K).to(torch.bfloat16).float().numpy()
+        V = torch.from_numpy(V).to(torch.bfloat16).float().numpy()
+    signs = synth.srht_signs(seed, d)
+    lev, thr = o.rsq_levels_f32(8)
+    z = o.Zones(S, L, U)
+    z.prefill(T)
+    enc = o.encode_contract(K[S:], signs, 16, lev, thr)  # prefill (untimed)
+    rng = np.random.default_rng(seed)
+    steps = max(1, args.steps)
+    t0 = time.perf_counter()
+    keys = 0
+    for s in range(args.warmup + steps):
+        if s == args.warmup:
+            t0 = time.perf_counter()
+            keys = 0
+        kn = (rng.standard_normal(d).astype(np.float32) * scale[0])
+        vn = rng.standard_normal(d).astype(np.float32)
+        K = np.vstack([K, kn[None]])
+        V = np.vstack([V, vn[None]])
+        e1 = o.encode_contract(kn[None], signs, 16, lev, thr)
+        for key in enc:
+            enc[key] = np.concatenate([enc[key], e1[key]])
+        z.append()
+        N = z.N
+        sub = {k: v[:N] for k, v in enc.items()}
+        for h in range(G):
+            q = K[S + rng.integers(0, N)] + 0.5 * rng.standard_normal(d).astype(np.float32)
+            r = o.retrieve_contract(sub, q.astype(np.float32), signs, 16, w["rho"], w["cand_bp"], w["topk"], lev)
+            rows = np.concatenate([z.sink(), z.local(), z.buffer(), S + r["top_idx"]])
+            o.attention(q, K[rows], V[rows])
+        keys += N
+    dt = time.perf_counter() - t0
+    print(json.dumps({"value": keys / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
+                      "sample": f"{steps} decode steps of 1 KV head ({G} query heads) of the "
+                                f"{DESCRIPTION[args.workload]}, single thread"}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b-128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--cpu-steps", type=int, default=60)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_sample:
+        oracle_sample(args)
+        return
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        args.cpu_steps = max(1, args.steps)
+        cb = cpu_baseline(args)
+        if cb is None:
+            print(json.dumps({"impl": "reference", "unavailable": "oracle run failed"}))
+            return
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": DESCRIPTION[args.workload]},
+            "cpu_baseline": {"value": cb["value"], "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(args)  # before any CUDA work in this process
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        res["cpu_baseline"] = cb
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

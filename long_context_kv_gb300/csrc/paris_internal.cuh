@@ -1,0 +1,121 @@
+// Internal declarations shared by the translation units of the ParisKV CUDA
+// library.  Nothing here is part of the C ABI (include/paris.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace paris {
+
+// Geometry the kernels are written for: d = 128 split into B = 16 subspaces
+// of m = 8 coordinates, so a bucket id is one byte and the 4-bit codes of a
+// subspace fill one 32-bit word.
+constexpr int kDim = 128;
+constexpr int kSub = 16;
+constexpr int kM = 8;
+constexpr int kCentroids = 1 << kM;
+constexpr int kRecBytes = 128;         // 64 B packed codes + 16 x float w
+constexpr int kChunk = 16384;          // keys per inverted-index chunk
+constexpr int kOffStride = 264;        // 257 bucket offsets, padded
+constexpr int kAttnSplit = 128;        // attention rows per partial block
+constexpr int kPartStride = kDim + 4;  // m, l, pad, pad, o[128]
+constexpr int kMaxBins = 256;          // vote values 0..255
+
+// RSQ-IP magnitude levels and midpoints, rounded to float32 once, and
+// float32(sqrt(d)).
+struct RsqParams {
+  float lev[8];
+  float thr[7];
+  float sqrtd;
+};
+
+// Diagonal D of the SRHT as a bit mask: bit c set means D_c = -1.
+struct SignMask {
+  uint32_t w[4];
+};
+
+// Device view of one context's key-side tables (per sequence and KV head).
+struct Tables {
+  uint8_t* ids;      // [batch][Hkv][Rcap][16]
+  uint8_t* rec;      // [batch][Hkv][Rcap][128]
+  uint16_t* ent;     // [batch][Hkv][nchunk][16][kChunk]
+  uint32_t* off;     // [batch][Hkv][nchunk][16][kOffStride]
+  int64_t rcap;      // Retrieval-zone capacity (rows)
+  int nchunk;        // chunks per (sequence, KV head)
+};
+
+struct KvStore {
+  __nv_bfloat16* win_k;  // [batch][Hkv][win][d]: sink slots then the Local/Buffer ring
+  __nv_bfloat16* win_v;
+  __nv_bfloat16* st_k;   // [batch][Hkv][rcap][d] by position - S (device address; may be mapped host memory)
+  __nv_bfloat16* st_v;
+  int win;               // S + L + U
+  int64_t rcap;
+};
+
+struct Shape {
+  int batch, hkv, hq, g;
+  int sink, local, ubuf;
+};
+
+// ---- cache side: prefill placement, encoding, index build, append ----------
+cudaError_t launch_place_kv(const void* K, const void* V, int dtype, int64_t T, int64_t N,
+                            const Shape& s, const KvStore& kv, cudaStream_t st);
+cudaError_t launch_encode(const void* K, int dtype, int64_t T, int64_t pos0, int64_t pos1,
+                          const Shape& s, const Tables& t, const SignMask& sm, const RsqParams& rp,
+                          cudaStream_t st);
+cudaError_t launch_build_index(int64_t N, int chunk0, int chunk1, const Shape& s, const Tables& t,
+                               cudaStream_t st);
+cudaError_t launch_append(const void* k, const void* v, int dtype, int64_t pos, const Shape& s,
+                          const KvStore& kv, const Tables& t, const SignMask& sm,
+                          const RsqParams& rp, cudaStream_t st);
+
+// ---- retrieval ----------------------------------------------------------
+struct RetrieveArgs {
+  Shape s;
+  Tables t;
+  SignMask sm;
+  RsqParams rp;
+  int rho, flat, nbins;
+  int64_t N, C, k, k_eff;
+  int nchunk_active;
+  // scratch
+  float* qt;          // [batch*Hq][d]
+  float* qnorm;       // [batch*Hq]
+  uint32_t* hot;      // [batch*Hq][16*rho]
+  uint8_t* votes;     // [batch*Hq][nchunk*kChunk]
+  uint32_t* hist;     // [batch*Hq][nchunk][kMaxBins]
+  int32_t* cand_idx;  // [batch*Hq][cmax]
+  float* cand_est;
+  int64_t cmax;
+  // outputs
+  int32_t* topk_idx;  // [batch*Hq][k]
+  float* topk_score;  // may be null
+};
+cudaError_t launch_qprep(const void* q, int dtype, const RetrieveArgs& a, cudaStream_t st);
+cudaError_t launch_vote(const RetrieveArgs& a, cudaStream_t st);
+cudaError_t launch_select_rerank(const RetrieveArgs& a, cudaStream_t st);
+cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st);
+cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_t st);
+
+// ---- sparse attention ---------------------------------------------------
+struct AttendArgs {
+  Shape s;
+  KvStore kv;
+  int64_t T, N, n_local_buf;  // n_local_buf = tokens in Local + Buffer
+  int64_t k, k_eff;
+  const int32_t* topk_idx;
+  float* part;                // [batch*Hq][nsplit_max][kPartStride]
+  int nsplit_max;
+  uint32_t* status;
+  __nv_bfloat16* out;
+};
+int attend_splits(const AttendArgs& a);
+cudaError_t launch_attn_partial(const void* q, int dtype, const AttendArgs& a, int nsplit, cudaStream_t st);
+cudaError_t launch_attn_combine(const AttendArgs& a, int nsplit, cudaStream_t st);
+
+// Status word bits.
+constexpr uint32_t kStatusBadIndex = 1u;
+
+}  // namespace paris
