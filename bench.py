@@ -148,7 +148,7 @@ def run_ours(args, rank, world):
     nl = args.layers or w["layers"]
     ctxlen, d = w["context"], w["head_dim"]
     b, hkv, hq, S = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["sink"]
-    per_layer_steps = (args.warmup + 3 * args.steps + nl - 1) // nl + 2
+    per_layer_steps = (args.warmup + 4 * args.steps + nl - 1) // nl + 2
     max_ctx = ctxlen + per_layer_steps + 8
     fdt = torch.bfloat16 if args.workload != "tiny-4k" else torch.float32
     seed0 = 20260202 + 1 + 1000 * rank
@@ -216,39 +216,72 @@ def run_ours(args, rank, world):
     for _ in range(args.warmup):
         step(i)
         i += 1
-    keys_per_step = []
-    counts0 = [L["ctx"].paris_launch_counts() for L in layers]
-    barrier()
     stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev) as clk:
-        e0.record(stream)
+
+    def timed(fn):
+        barrier()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(torch.cuda.current_stream())
+        fn()
+        z.record(torch.cuda.current_stream())
+        barrier()
+        return max_over_ranks(a.elapsed_time(z))
+
+    # eager: every step launched from Python through the ABI
+    def eager_steps():
+        nonlocal i
         for _ in range(args.steps):
-            L = layers[i % nl]
-            keys_per_step.append(L["ctx"].paris_get_state()["N"] * b * hkv)
             step(i)
             i += 1
-        e1.record(stream)
-        barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1))
-    counts1 = [L["ctx"].paris_launch_counts() for L in layers]
-    launches = sum(counts1[li][k] - counts0[li][k] for li in range(nl) for k in counts1[li])
+    ms_eager = timed(eager_steps)
+
+    # graph: the same K decode steps captured once (positions, flushes and
+    # all) and replayed; replays repeat identical, idempotent work, so the
+    # replay time is the device time of those K steps without host gaps
+    def capture(profile=False):
+        nonlocal i
+        keys = []
+        cs = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        if profile:
+            for L in layers:
+                L["ctx"].paris_profile_begin(64 * args.steps)
+        c0 = [L["ctx"].paris_launch_counts() for L in layers]
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(args.steps):
+                keys.append(layers[i % nl]["ctx"].paris_get_state()["N"] * b * hkv)
+                step(i)
+                i += 1
+        c1 = [L["ctx"].paris_launch_counts() for L in layers]
+        n = sum(c1[li][k] - c0[li][k] for li in range(nl) for k in c1[li])
+        return g, keys, n
+
+    g_main, keys_per_step, launches = capture()
+    g_main.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        t_end = time.time() + 1.0
+        while time.time() < t_end:  # load before the timed replay so the clock samples see it
+            g_main.replay()
+            torch.cuda.synchronize()
+        ms = timed(g_main.replay)
+        for _ in range(3):
+            g_main.replay()
+        torch.cuda.synchronize()
     keys_total = sum(keys_per_step) * world
     value = keys_total / (ms / 1e3)
 
-    # profiled pass: the same steps with per-kernel events on the launch stream
-    for L in layers:
-        L["ctx"].paris_profile_begin(64 * args.steps)
-    barrier()
-    for _ in range(args.steps):
-        step(i)
-        i += 1
+    # per-kernel device time: a second capture with events around every kernel
+    g_prof, _, _ = capture(profile=True)
+    g_prof.replay()
+    torch.cuda.synchronize()
     prof = {}
     for L in layers:
         for k, (t, n) in L["ctx"].paris_profile_end().items():
             a = prof.setdefault(k, [0.0, 0])
             a[0] += t
             a[1] += n
+    del g_prof
     kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
     retrieve_kernels = ("qprep", "vote", "select_rerank", "topk")
     us_retrieve = sum(1e3 * prof[k][0] for k in retrieve_kernels) / args.steps
@@ -345,6 +378,7 @@ def run_ours(args, rank, world):
                    "l2": f"inputs larger than L2: {nl} layer contexts rotated, each revisited after "
                          f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"},
         "us_per_decode_step": 1e3 * ms / args.steps,
+        "us_per_decode_step_eager": 1e3 * ms_eager / args.steps,
         "us_retrieve": us_retrieve, "us_attend": us_attend, "us_append": us_append,
         "retrieve_hbm_frac": round(retrieve_frac, 4),
         "recall_at_k": recall,
