@@ -84,7 +84,9 @@ cudaError_t launch(paris_ctx* c, int slot, cudaStream_t st, F&& call) {
     cudaError_t e = cudaEventCreate(&e0);
     if (e == cudaSuccess) e = cudaEventCreate(&e1);
     if (e != cudaSuccess) return e;
-    e = cudaEventRecord(e0, st);
+    // external records: inside a stream capture they become event-record
+    // nodes of the graph, so the pair still times the kernel on replay
+    e = cudaEventRecordWithFlags(e0, st, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = call();
@@ -92,7 +94,7 @@ cudaError_t launch(paris_ctx* c, int slot, cudaStream_t st, F&& call) {
     c->prof_ev.push_back(e0);
     c->prof_ev.push_back(e1);
     c->prof_slot.push_back(slot);
-    if (e == cudaSuccess) e = cudaEventRecord(e1, st);
+    if (e == cudaSuccess) e = cudaEventRecordWithFlags(e1, st, cudaEventRecordExternal);
   }
   return e;
 }
