@@ -191,10 +191,7 @@ def run_ours(args, rank, world):
         L = layers[i % nl]
         j = L["step"]
         L["step"] = j + 1
-        ctx = L["ctx"]
-        ctx.paris_append_decode(L["kn"][j], L["vn"][j])
-        ctx.paris_retrieve(L["qs"][j], L["idx"], L["sc"])
-        ctx.paris_sparse_attend(L["qs"][j], L["idx"], L["out"])
+        L["ctx"].paris_decode_step(L["kn"][j], L["vn"][j], L["qs"][j], L["idx"], L["sc"], L["out"])
 
     dist = world > 1
     if dist:
@@ -283,9 +280,8 @@ def run_ours(args, rank, world):
             a[1] += n
     del g_prof
     kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
-    retrieve_kernels = ("qprep", "vote", "select_rerank", "topk")
-    us_retrieve = sum(1e3 * prof[k][0] for k in retrieve_kernels) / args.steps
-    us_attend = sum(1e3 * prof[k][0] for k in ("attn_partial", "attn_combine")) / args.steps
+    us_retrieve = sum(1e3 * prof[k][0] for k in ("vote", "select", "fill")) / args.steps
+    us_attend = 1e3 * prof["attend"][0] / args.steps
     us_append = sum(1e3 * prof[k][0] for k in ("append", "build_index")) / args.steps
 
     # roofline of the dominant kernel (algorithmic bytes per launch)
@@ -294,9 +290,12 @@ def run_ours(args, rank, world):
     keff = min(w["topk"], C)
     nwin = S + w["local"] + w["update_buf"] // 2
     alg = {
-        "select_rerank": b * hq * C * (128 + 8),
-        "attn_partial": b * hq * keff * 4 * d + b * hkv * nwin * 4 * d,
-        "topk": b * hq * (C * 8 + keff * 8),
+        # votes read back (1 B per key and query head), candidate records
+        # (64 B codes + 64 B w) gathered, candidate index + estimate written,
+        # top-k index + estimate written
+        "select": b * hq * (int(Nmean) + C * (128 + 8) + keff * 8),
+        # retrieved K and V rows, plus the window rows once per KV head
+        "attend": b * hq * keff * 4 * d + b * hkv * nwin * 4 * d,
     }
     dom = max(kernels, key=lambda k: kernels[k]["us_per_launch"] * kernels[k]["launches"])
     peak, peak_src = hbm_peak()
@@ -306,7 +305,7 @@ def run_ours(args, rank, world):
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom),
                 "algorithmic_bytes": alg[dom]}
-    retr_bytes = alg["select_rerank"] + b * hq * 64 * (Nmean / 256) * 2 * w["rho"] * w["n_sub"] / 4
+    retr_bytes = alg["select"] + b * hq * (w["rho"] * w["n_sub"]) * (Nmean / 256) * 2
     retrieve_frac = retr_bytes / (us_retrieve * 1e-6) / 1e9 / peak
 
     # end to end through the public API with host buffers
@@ -331,9 +330,7 @@ def run_ours(args, rank, world):
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
-        L["ctx"].paris_append_decode(d_k, d_v)
-        L["ctx"].paris_retrieve(d_q, L["idx"], L["sc"])
-        L["ctx"].paris_sparse_attend(d_q, L["idx"], L["out"])
+        L["ctx"].paris_decode_step(d_k, d_v, d_q, L["idx"], L["sc"], L["out"])
         h_idx.copy_(L["idx"], non_blocking=True)
         h_sc.copy_(L["sc"], non_blocking=True)
         h_out.copy_(L["out"], non_blocking=True)

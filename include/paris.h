@@ -148,6 +148,16 @@ paris_status paris_retrieve(paris_ctx* ctx, const void* q, paris_dtype dtype, in
 paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtype,
                                  const int32_t* topk_idx, void* out_bf16, void* stream);
 
+/* One decode step: exactly paris_append_decode(k, v), then
+ * paris_retrieve(q, ...), then paris_sparse_attend(q, topk_idx, out), with the
+ * same arguments and results, in three kernels instead of five: the append
+ * rides in the vote kernel unless it fills the Update Buffer (then the flush
+ * and index rebuild run first).  k, v: device, kv_dtype, [batch][Hkv][d];
+ * q: device, q_dtype, [batch][Hq][d]; outputs as in the two calls.          */
+paris_status paris_decode_step(paris_ctx* ctx, const void* k, const void* v, paris_dtype kv_dtype, const void* q,
+                               paris_dtype q_dtype, int32_t* topk_idx, float* topk_score, void* out_bf16,
+                               int64_t* k_eff, void* stream);
+
 /* Copy the zone bookkeeping to *out (host).  No device work.               */
 paris_status paris_get_state(const paris_ctx* ctx, paris_state* out);
 
@@ -183,18 +193,16 @@ const char* paris_last_error(const paris_ctx* ctx);
 
 /* Kernels of the library, for per-kernel accounting. */
 typedef enum {
-  PARIS_KERNEL_PLACE_KV = 0,   /* prefill: K/V into Sink, store and Local ring   */
-  PARIS_KERNEL_ENCODE = 1,     /* prefill: SRHT, bucket ids, codes, w            */
-  PARIS_KERNEL_BUILD_INDEX = 2,/* per-chunk inverted bucket index                */
-  PARIS_KERNEL_APPEND = 3,     /* decode append (store + encode one token)       */
-  PARIS_KERNEL_QPREP = 4,      /* query rotation, ||q||, top-rho centroids       */
-  PARIS_KERNEL_VOTE = 5,       /* collision votes + histograms                   */
-  PARIS_KERNEL_SELECT_RERANK = 6, /* candidate selection + RSQ-IP estimates      */
-  PARIS_KERNEL_TOPK = 7,       /* top-k of the estimates                         */
-  PARIS_KERNEL_ATTN_PARTIAL = 8, /* split sparse attention                       */
-  PARIS_KERNEL_ATTN_COMBINE = 9, /* merge of the splits                          */
-  PARIS_KERNEL_FILL = 10,      /* empty-result fill                              */
-  PARIS_KERNEL_COUNT = 11
+  PARIS_KERNEL_PLACE_KV = 0,    /* prefill: K/V into Sink, store and Local ring          */
+  PARIS_KERNEL_ENCODE = 1,      /* prefill: SRHT, bucket ids, codes, w                   */
+  PARIS_KERNEL_BUILD_INDEX = 2, /* per-chunk inverted bucket index                       */
+  PARIS_KERNEL_APPEND = 3,      /* standalone decode append (store + encode one token)   */
+  PARIS_KERNEL_VOTE = 4,        /* query rotation, top-rho centroids, collision votes,
+                                   candidate plan (and a fused append in decode steps)  */
+  PARIS_KERNEL_SELECT = 5,      /* candidate selection, RSQ-IP estimates, top-k          */
+  PARIS_KERNEL_ATTEND = 6,      /* sparse attention and the merge of its splits          */
+  PARIS_KERNEL_FILL = 7,        /* empty-result fill                                     */
+  PARIS_KERNEL_COUNT = 8
 } paris_kernel;
 
 /* Cumulative kernel launches of this context since paris_create, per

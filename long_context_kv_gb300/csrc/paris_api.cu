@@ -40,6 +40,10 @@ struct paris_ctx {
   float* cand_est;
   float* part;
   uint32_t* status;
+  int32_t* plan;
+  int plan_stride;
+  uint32_t* counters;  // [3][batch*Hq]: vote, select, attend
+  uint32_t* minmax;    // [batch*Hq][2]
   std::string err;
   // accounting
   int64_t launches[PARIS_KERNEL_COUNT];
@@ -145,7 +149,8 @@ void lloyd_max_levels(int m, double lev[8], double thr[7]) {
 
 void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
-                 c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status};
+                 c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status, c->plan,
+                 c->counters, c->minmax};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_store) {
@@ -171,6 +176,109 @@ paris_status dalloc(paris_ctx* c, T** p, size_t bytes, const char* what) {
 
 paris_status check_dtype(paris_ctx* c, int dtype) {
   if (dtype != PARIS_F32 && dtype != PARIS_BF16) return fail(c, PARIS_EINVAL, "dtype must be PARIS_F32 or PARIS_BF16");
+  return PARIS_OK;
+}
+
+}  // namespace
+
+namespace {
+
+RetrieveArgs retrieve_args(paris_ctx* c, int32_t* topk_idx, float* topk_score) {
+  RetrieveArgs a;
+  a.s = c->s;
+  a.t = c->t;
+  a.sm = c->sm;
+  a.rp = c->rp;
+  a.rho = c->cfg.rho;
+  a.flat = c->cfg.vote_weighting == PARIS_VOTE_FLAT;
+  a.nbins = c->nbins;
+  a.N = c->N;
+  a.C = candidate_count(c->N, c->cfg.cand_bp, c->cfg.topk);
+  a.k = c->cfg.topk;
+  a.k_eff = std::min<int64_t>(a.k, a.C);
+  a.nchunk_active = (int)((c->N + kChunk - 1) / kChunk);
+  a.qt = c->qt;
+  a.qnorm = c->qnorm;
+  a.hot = c->hot;
+  a.votes = c->votes;
+  a.hist = c->hist;
+  a.cand_idx = c->cand_idx;
+  a.cand_est = c->cand_est;
+  a.cmax = c->cmax;
+  a.plan = c->plan;
+  a.plan_stride = c->plan_stride;
+  const int64_t bq = (int64_t)c->s.batch * c->s.hq;
+  a.counter_vote = c->counters;
+  a.counter_select = c->counters + bq;
+  a.minmax = c->minmax;
+  a.topk_idx = topk_idx;
+  a.topk_score = topk_score;
+  return a;
+}
+
+AttendArgs attend_args(paris_ctx* c, const int32_t* topk_idx, void* out_bf16) {
+  AttendArgs a;
+  a.s = c->s;
+  a.kv = c->kv;
+  a.T = c->T;
+  a.N = c->N;
+  a.n_local_buf = c->n_local + c->n_buf;
+  a.k = c->cfg.topk;
+  a.k_eff = c->N > 0 ? std::min<int64_t>(a.k, candidate_count(c->N, c->cfg.cand_bp, c->cfg.topk)) : 0;
+  a.topk_idx = topk_idx;
+  a.part = c->part;
+  a.nsplit_max = c->nsplit_max;
+  a.status = c->status;
+  a.counter = c->counters + 2 * (int64_t)c->s.batch * c->s.hq;
+  a.out = static_cast<__nv_bfloat16*>(out_bf16);
+  return a;
+}
+
+// Advance the zone bookkeeping by one appended token; returns the number of
+// tokens the append moved into the Retrieval zone (their chunks need a new
+// index) and the Retrieval size before it.
+int64_t zones_append(paris_ctx* c, int64_t* n_old) {
+  const int64_t pos = c->T;
+  c->T += 1;
+  *n_old = c->N;
+  if (pos < c->s.sink) return 0;
+  c->n_buf += 1;
+  if (c->n_buf < c->s.ubuf) return 0;
+  c->n_local += c->n_buf;
+  c->n_buf = 0;
+  c->n_flushes += 1;
+  const int64_t evict = std::max<int64_t>(0, c->n_local - c->s.local);
+  c->N += evict;
+  c->n_local -= evict;
+  return evict;
+}
+
+// Would appending one token now move tokens into the Retrieval zone?
+bool append_flushes(const paris_ctx* c) {
+  if (c->T < c->s.sink) return false;
+  if (c->n_buf + 1 < c->s.ubuf) return false;
+  return c->n_local + c->n_buf + 1 > c->s.local;
+}
+
+paris_status retrieve_launch(paris_ctx* c, const void* q, paris_dtype dtype, int32_t* topk_idx, float* topk_score,
+                             int64_t* k_eff, const AppendFuse* fuse, cudaStream_t s) {
+  const int64_t nq = (int64_t)c->s.batch * c->s.hq;
+  if (c->N == 0) {
+    *k_eff = 0;
+    if (fuse) {
+      const AppendFuse f = *fuse;
+      PARIS_CUDA(c, launch(c, PARIS_KERNEL_APPEND, s, [&] {
+                   return launch_append(f.k, f.v, f.dtype, f.pos, c->s, c->kv, c->t, c->sm, c->rp, s);
+                 }));
+    }
+    PARIS_CUDA(c, launch(c, PARIS_KERNEL_FILL, s,
+                         [&] { return launch_fill_empty(topk_idx, topk_score, nq * c->cfg.topk, s); }));
+    return PARIS_OK;
+  }
+  const RetrieveArgs a = retrieve_args(c, topk_idx, topk_score);
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_VOTE, s, [&] { return launch_vote(q, dtype, a, fuse, s); }));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_SELECT, s, [&] { return launch_select(a, s); }));
+  *k_eff = a.k_eff;
   return PARIS_OK;
 }
 
@@ -210,6 +318,11 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   c->nbins = (f.vote_weighting == PARIS_VOTE_RANK ? f.rho * kSub : kSub) + 1;
   c->rcap = std::max<int64_t>(0, (int64_t)f.max_ctx - f.sink);
   c->nchunk = (int)std::max<int64_t>(1, (c->rcap + kChunk - 1) / kChunk);
+  if (c->nchunk > kMaxChunks) {
+    delete c;
+    return fail(nullptr, PARIS_EINVAL, "max_ctx - sink must be at most %d tokens", kMaxChunks * kChunk);
+  }
+  c->plan_stride = 1 + 2 * c->nchunk;
   c->cmax = std::max<int64_t>(1, candidate_count(c->rcap, f.cand_bp, f.topk));
   c->nsplit_max = (int)((f.sink + f.local + f.update_buf + f.topk + kAttnSplit - 1) / kAttnSplit) + 1;
   std::memset(&c->sm, 0, sizeof c->sm);
@@ -268,8 +381,20 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   TRY(dalloc(c, &c->cand_est, (size_t)bq * c->cmax * sizeof(float), "candidate estimates"));
   TRY(dalloc(c, &c->part, (size_t)bq * c->nsplit_max * kPartStride * sizeof(float), "attention partials"));
   TRY(dalloc(c, &c->status, sizeof(uint32_t), "status word"));
+  TRY(dalloc(c, &c->plan, (size_t)bq * c->plan_stride * sizeof(int32_t), "candidate plan"));
+  TRY(dalloc(c, &c->counters, (size_t)3 * bq * sizeof(uint32_t), "tile counters"));
+  TRY(dalloc(c, &c->minmax, (size_t)2 * bq * sizeof(uint32_t), "estimate range"));
   cudaError_t e = cudaMemset(c->status, 0, sizeof(uint32_t));
-  if (e != cudaSuccess) TRY(cuda_fail(c, e, "cudaMemset(status)"));
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)3 * bq * sizeof(uint32_t));
+  if (e == cudaSuccess) {
+    std::vector<uint32_t> mm((size_t)2 * bq);
+    for (size_t i = 0; i < mm.size(); i += 2) {
+      mm[i] = 0xffffffffu;
+      mm[i + 1] = 0u;
+    }
+    e = cudaMemcpy(c->minmax, mm.data(), mm.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) TRY(cuda_fail(c, e, "initialising the context"));
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "cudaDeviceSynchronize"));
 #undef TRY
@@ -324,19 +449,9 @@ paris_status paris_append_decode(paris_ctx* c, const void* k, const void* v, par
   const int64_t pos = c->T;
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_APPEND, s,
                        [&] { return launch_append(k, v, dtype, pos, c->s, c->kv, c->t, c->sm, c->rp, s); }));
-  c->T += 1;
-  if (pos < c->s.sink) return PARIS_OK;
-  c->n_buf += 1;
-  if (c->n_buf < c->s.ubuf) return PARIS_OK;
+  int64_t n_old;
   // flush: the buffer joins Local, Local's oldest tokens beyond L join Retrieval
-  c->n_local += c->n_buf;
-  c->n_buf = 0;
-  c->n_flushes += 1;
-  const int64_t evict = std::max<int64_t>(0, c->n_local - c->s.local);
-  if (evict == 0) return PARIS_OK;
-  const int64_t n_old = c->N;
-  c->N += evict;
-  c->n_local -= evict;
+  if (zones_append(c, &n_old) == 0) return PARIS_OK;
   const int64_t n_new = c->N;
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_BUILD_INDEX, s, [&] {
                return launch_build_index(n_new, (int)(n_old / kChunk), (int)((n_new + kChunk - 1) / kChunk), c->s, c->t, s);
@@ -350,43 +465,7 @@ paris_status paris_retrieve(paris_ctx* c, const void* q, paris_dtype dtype, int3
   paris_status st = check_dtype(c, dtype);
   if (st != PARIS_OK) return st;
   if (!q || !topk_idx || !k_eff) return fail(c, PARIS_EINVAL, "q, topk_idx and k_eff must not be NULL");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t nq = (int64_t)c->s.batch * c->s.hq;
-  if (c->N == 0) {
-    *k_eff = 0;
-    PARIS_CUDA(c, launch(c, PARIS_KERNEL_FILL, s,
-                         [&] { return launch_fill_empty(topk_idx, topk_score, nq * c->cfg.topk, s); }));
-    return PARIS_OK;
-  }
-  RetrieveArgs a;
-  a.s = c->s;
-  a.t = c->t;
-  a.sm = c->sm;
-  a.rp = c->rp;
-  a.rho = c->cfg.rho;
-  a.flat = c->cfg.vote_weighting == PARIS_VOTE_FLAT;
-  a.nbins = c->nbins;
-  a.N = c->N;
-  a.C = candidate_count(c->N, c->cfg.cand_bp, c->cfg.topk);
-  a.k = c->cfg.topk;
-  a.k_eff = std::min<int64_t>(a.k, a.C);
-  a.nchunk_active = (int)((c->N + kChunk - 1) / kChunk);
-  a.qt = c->qt;
-  a.qnorm = c->qnorm;
-  a.hot = c->hot;
-  a.votes = c->votes;
-  a.hist = c->hist;
-  a.cand_idx = c->cand_idx;
-  a.cand_est = c->cand_est;
-  a.cmax = c->cmax;
-  a.topk_idx = topk_idx;
-  a.topk_score = topk_score;
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_QPREP, s, [&] { return launch_qprep(q, dtype, a, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_VOTE, s, [&] { return launch_vote(a, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_SELECT_RERANK, s, [&] { return launch_select_rerank(a, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_TOPK, s, [&] { return launch_topk(a, s); }));
-  *k_eff = a.k_eff;
-  return PARIS_OK;
+  return retrieve_launch(c, q, dtype, topk_idx, topk_score, k_eff, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 paris_status paris_sparse_attend(paris_ctx* c, const void* q, paris_dtype dtype, const int32_t* topk_idx,
@@ -395,23 +474,41 @@ paris_status paris_sparse_attend(paris_ctx* c, const void* q, paris_dtype dtype,
   paris_status st = check_dtype(c, dtype);
   if (st != PARIS_OK) return st;
   if (!q || !out_bf16 || (!topk_idx && c->N > 0)) return fail(c, PARIS_EINVAL, "q, topk_idx and out must not be NULL");
-  AttendArgs a;
-  a.s = c->s;
-  a.kv = c->kv;
-  a.T = c->T;
-  a.N = c->N;
-  a.n_local_buf = c->n_local + c->n_buf;
-  a.k = c->cfg.topk;
-  a.k_eff = c->N > 0 ? std::min<int64_t>(a.k, candidate_count(c->N, c->cfg.cand_bp, c->cfg.topk)) : 0;
-  a.topk_idx = topk_idx;
-  a.part = c->part;
-  a.nsplit_max = c->nsplit_max;
-  a.status = c->status;
-  a.out = static_cast<__nv_bfloat16*>(out_bf16);
+  const AttendArgs a = attend_args(c, topk_idx, out_bf16);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int nsplit = attend_splits(a);
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTN_PARTIAL, s, [&] { return launch_attn_partial(q, dtype, a, nsplit, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTN_COMBINE, s, [&] { return launch_attn_combine(a, nsplit, s); }));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTEND, s, [&] { return launch_attend(q, dtype, a, s); }));
+  return PARIS_OK;
+}
+
+paris_status paris_decode_step(paris_ctx* c, const void* k, const void* v, paris_dtype kv_dtype, const void* q,
+                               paris_dtype q_dtype, int32_t* topk_idx, float* topk_score, void* out_bf16,
+                               int64_t* k_eff, void* stream) {
+  if (!c) return fail(nullptr, PARIS_EINVAL, "ctx is NULL");
+  paris_status st = check_dtype(c, kv_dtype);
+  if (st == PARIS_OK) st = check_dtype(c, q_dtype);
+  if (st != PARIS_OK) return st;
+  if (!k || !v || !q || !topk_idx || !out_bf16 || !k_eff)
+    return fail(c, PARIS_EINVAL, "k, v, q, topk_idx, out and k_eff must not be NULL");
+  if (c->T + 1 > c->cfg.max_ctx) return fail(c, PARIS_ECAPACITY, "cache is full (max_ctx = %d)", c->cfg.max_ctx);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (append_flushes(c)) {
+    st = paris_append_decode(c, k, v, kv_dtype, stream);
+    if (st != PARIS_OK) return st;
+    st = retrieve_launch(c, q, q_dtype, topk_idx, topk_score, k_eff, nullptr, s);
+  } else {
+    AppendFuse f;
+    f.k = k;
+    f.v = v;
+    f.dtype = kv_dtype;
+    f.pos = c->T;
+    f.kv = c->kv;
+    int64_t n_old;
+    zones_append(c, &n_old);
+    st = retrieve_launch(c, q, q_dtype, topk_idx, topk_score, k_eff, &f, s);
+  }
+  if (st != PARIS_OK) return st;
+  const AttendArgs a = attend_args(c, topk_idx, out_bf16);
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTEND, s, [&] { return launch_attend(q, q_dtype, a, s); }));
   return PARIS_OK;
 }
 

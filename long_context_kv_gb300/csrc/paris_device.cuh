@@ -96,4 +96,147 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* tmp, u
   return r;
 }
 
+// Encode one key held by a warp (lane l owns coordinates 4l..4l+3 of the
+// raw key).  Float32 order, every operation rounded once:
+//   z = fwht(D * k);  id_b bit j = [z_{b,j} < 0];
+//   n_b = sqrt(((0 + z_0 z_0) + z_1 z_1) + ... + z_7 z_7);
+//   x_j = z_j / n_b;  sign s_j = [z_j < 0];  t_j = #{thr < |x_j|};
+//   v_j = (-1)^s_j lev[t_j];  <v,x> = ((0 + v_0 x_0) + v_1 x_1) + ...;
+//   w_b = n_b / (sqrt(d) * <v,x>), and w_b = 0, codes 0 where n_b = 0.
+// Subspace b is lanes 2b (j = 0..3) and 2b+1 (j = 4..7); a sequential sum
+// over j starts in the even lane and continues in the odd lane.
+// Writes the 16 ids and the 128-byte record (16 code words, 16 w) of the key.
+__device__ __forceinline__ void encode_key_warp(float (&y)[4], int lane, const SignMask& sm,
+                                                const RsqParams& rp, uint8_t* ids_row,
+                                                uint8_t* rec_row) {
+  apply_signs(y, sm, lane);
+  fwht128_warp(y, lane);
+  const bool odd = (lane & 1) != 0;
+
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) bits |= (y[i] < 0.f ? 1u : 0u) << i;
+  const uint32_t obits = __shfl_xor_sync(kFull, bits, 1);
+  const uint32_t id = odd ? (obits | (bits << 4)) : (bits | (obits << 4));
+
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc = __fadd_rn(acc, __fmul_rn(y[i], y[i]));
+  float acc2 = __shfl_xor_sync(kFull, acc, 1);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc2 = __fadd_rn(acc2, __fmul_rn(y[i], y[i]));
+  const float nsq = __shfl_sync(kFull, acc2, lane | 1);
+  const float nb = __fsqrt_rn(nsq);
+  const bool live = nb > 0.f;
+
+  float x[4], v[4];
+  uint32_t half = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[i] = live ? __fdiv_rn(y[i], nb) : 0.f;
+    const float ax = fabsf(x[i]);
+    uint32_t t = 0;
+#pragma unroll
+    for (int r = 0; r < 7; ++r) t += (rp.thr[r] < ax) ? 1u : 0u;
+    const uint32_t s = (live && y[i] < 0.f) ? 1u : 0u;
+    const float l = rp.lev[t];
+    v[i] = s ? -l : l;
+    half |= ((s << 3) | t) << (4 * i);
+  }
+  float vx = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) vx = __fadd_rn(vx, __fmul_rn(v[i], x[i]));
+  float vx2 = __shfl_xor_sync(kFull, vx, 1);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) vx2 = __fadd_rn(vx2, __fmul_rn(v[i], x[i]));
+  const float w = live ? __fdiv_rn(nb, __fmul_rn(rp.sqrtd, vx2)) : 0.f;  // valid in odd lanes
+
+  // record word l: l < 16 the code word of subspace l, else w of subspace l - 16
+  const uint32_t h_lo = __shfl_sync(kFull, half, (2 * lane) & 31);
+  const uint32_t h_hi = __shfl_sync(kFull, half, (2 * lane + 1) & 31);
+  const float w_src = __shfl_sync(kFull, w, (2 * (lane - 16) + 1) & 31);
+  const uint32_t word = lane < 16 ? (h_lo | (h_hi << 16)) : __float_as_uint(w_src);
+  reinterpret_cast<uint32_t*>(rec_row)[lane] = word;
+
+  // ids word q (q < 4) holds the ids of subspaces 4q..4q+3, one byte each
+  uint32_t idw = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t o = __shfl_sync(kFull, id, (2 * (4 * (lane & 3) + i)) & 31);
+    idw |= (o & 0xffu) << (8 * i);
+  }
+  if (lane < 4) reinterpret_cast<uint32_t*>(ids_row)[lane] = idw;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Copy 8 consecutive elements (element offset e, multiple of 8) of a float32
+// or bf16 row to bf16 destinations.
+__device__ __forceinline__ uint4 load8_as_bf16(const void* p, int dtype, int64_t e) {
+  if (dtype == 1) return *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p) + e);
+  const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + e);
+  const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + e + 4);
+  return make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                    pack_bf16x2(b.z, b.w));
+}
+
+// Place K/V row `pos` of (sequence, KV head) `sh`: Sink slot if pos < S;
+// otherwise the store row pos - S, and the Local/Buffer ring slot when the
+// token is in Local or the Buffer (pos >= S + N).  16 threads per row.
+__device__ __forceinline__ void place_row(uint4 kk, uint4 vv, int64_t sh, int64_t pos, int64_t N,
+                                          int part, const Shape& s, const KvStore& kv) {
+  const int ring = s.local + s.ubuf;
+  if (pos < s.sink) {
+    const int64_t o = (sh * kv.win + pos) * kDim + 8 * part;
+    *reinterpret_cast<uint4*>(kv.win_k + o) = kk;
+    *reinterpret_cast<uint4*>(kv.win_v + o) = vv;
+    return;
+  }
+  const int64_t so = (sh * kv.rcap + (pos - s.sink)) * kDim + 8 * part;
+  *reinterpret_cast<uint4*>(kv.st_k + so) = kk;
+  *reinterpret_cast<uint4*>(kv.st_v + so) = vv;
+  if (pos >= s.sink + N) {
+    const int64_t slot = s.sink + (pos - s.sink) % ring;
+    const int64_t o = (sh * kv.win + slot) * kDim + 8 * part;
+    *reinterpret_cast<uint4*>(kv.win_k + o) = kk;
+    *reinterpret_cast<uint4*>(kv.win_v + o) = vv;
+  }
+}
+
+
+// Append one token of (sequence, KV head) `sh` (one warp): store its K/V as
+// bf16 (Sink slot, or store row + Local/Buffer ring slot) and, past the Sink,
+// encode its key at table row pos - S.
+__device__ __forceinline__ void append_token_warp(const void* k, const void* v, int dtype, int64_t pos,
+                                                  int64_t sh, int lane, const Shape& s, const KvStore& kv,
+                                                  const Tables& t, const SignMask& sm, const RsqParams& rp) {
+  if (lane < 16) {
+    const uint4 kk = load8_as_bf16(k, dtype, sh * kDim + 8 * lane);
+    const uint4 vv = load8_as_bf16(v, dtype, sh * kDim + 8 * lane);
+    // a new token is never in the Retrieval zone: with N = 0 every position
+    // past the Sink also lands in its Local/Buffer ring slot
+    place_row(kk, vv, sh, pos, /*N=*/0, lane, s, kv);
+  }
+  if (pos < s.sink) return;
+  float y[4];
+  load4(k, dtype, sh * kDim + 4 * lane, y);
+  const int64_t row = sh * t.rcap + (pos - s.sink);
+  encode_key_warp(y, lane, sm, rp, t.ids + row * kSub, t.rec + row * kRecBytes);
+}
+
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key); -0 and +0 map to the same key.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  if (x == 0.f) x = 0.f;
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 }  // namespace paris

@@ -21,6 +21,7 @@ constexpr int kOffStride = 264;        // 257 bucket offsets, padded
 constexpr int kAttnSplit = 128;        // attention rows per partial block
 constexpr int kPartStride = kDim + 4;  // m, l, pad, pad, o[128]
 constexpr int kMaxBins = 256;          // vote values 0..255
+constexpr int kMaxChunks = 256;        // chunks per (sequence, KV head): 4M Retrieval-zone keys
 
 // RSQ-IP magnitude levels and midpoints, rounded to float32 once, and
 // float32(sqrt(d)).
@@ -89,14 +90,29 @@ struct RetrieveArgs {
   int32_t* cand_idx;  // [batch*Hq][cmax]
   float* cand_est;
   int64_t cmax;
+  int32_t* plan;      // [batch*Hq][plan_stride]: T, then (candidates before, T-keys allowed) per chunk
+  int plan_stride;
+  uint32_t* counter_vote;    // [batch*Hq] tiles finished, reset by the last one
+  uint32_t* counter_select;  // [batch*Hq]
+  uint32_t* minmax;          // [batch*Hq][2] order keys of the smallest / largest estimate
   // outputs
   int32_t* topk_idx;  // [batch*Hq][k]
   float* topk_score;  // may be null
 };
-cudaError_t launch_qprep(const void* q, int dtype, const RetrieveArgs& a, cudaStream_t st);
-cudaError_t launch_vote(const RetrieveArgs& a, cudaStream_t st);
-cudaError_t launch_select_rerank(const RetrieveArgs& a, cudaStream_t st);
-cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st);
+
+// A decode-token append fused into the vote kernel (one warp per
+// (sequence, KV head), in the tiles of chunk 0).
+struct AppendFuse {
+  const void* k;
+  const void* v;
+  int dtype;
+  int64_t pos;
+  KvStore kv;
+};
+
+size_t vote_smem_bytes(int rho);
+cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st);
+cudaError_t launch_select(const RetrieveArgs& a, cudaStream_t st);
 cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_t st);
 
 // ---- sparse attention ---------------------------------------------------
@@ -109,11 +125,11 @@ struct AttendArgs {
   float* part;                // [batch*Hq][nsplit_max][kPartStride]
   int nsplit_max;
   uint32_t* status;
+  uint32_t* counter;          // [batch*Hq] splits finished, reset by the last one
   __nv_bfloat16* out;
 };
 int attend_splits(const AttendArgs& a);
-cudaError_t launch_attn_partial(const void* q, int dtype, const AttendArgs& a, int nsplit, cudaStream_t st);
-cudaError_t launch_attn_combine(const AttendArgs& a, int nsplit, cudaStream_t st);
+cudaError_t launch_attend(const void* q, int dtype, const AttendArgs& a, cudaStream_t st);
 
 // Status word bits.
 constexpr uint32_t kStatusBadIndex = 1u;

@@ -39,13 +39,15 @@ _SIGNATURES = {
                                         ctypes.c_void_p, ctypes.c_size_t]),
     "paris_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
     "paris_rsq_levels": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "paris_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p]),
     "paris_launch_counts": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "paris_profile_begin": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "paris_profile_end": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
 }
 
-KERNELS = ["place_kv", "encode", "build_index", "append", "qprep", "vote", "select_rerank", "topk",
-           "attn_partial", "attn_combine", "fill"]
+KERNELS = ["place_kv", "encode", "build_index", "append", "vote", "select", "attend", "fill"]
 
 
 class paris_config(ctypes.Structure):
@@ -176,6 +178,13 @@ class Context:
     def paris_sparse_attend(self, q, topk_idx, out, stream=None):
         _check(load().paris_sparse_attend(self._h, _ptr(q), _dtype_code(q), _ptr(topk_idx), _ptr(out),
                                           _stream(stream)), self._h)
+
+    def paris_decode_step(self, k, v, q, topk_idx, topk_score, out, stream=None) -> int:
+        k_eff = ctypes.c_int64()
+        _check(load().paris_decode_step(self._h, _ptr(k), _ptr(v), _dtype_code(k), _ptr(q), _dtype_code(q),
+                                        _ptr(topk_idx), _ptr(topk_score), _ptr(out), ctypes.byref(k_eff),
+                                        _stream(stream)), self._h)
+        return k_eff.value
 
     def paris_get_state(self) -> dict:
         st = paris_state()

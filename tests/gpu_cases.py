@@ -71,9 +71,11 @@ def make_case(T: int, seed: int = 1, dtype=torch.bfloat16, K=None, **cfg_kw) -> 
     return c
 
 
-def append(c: Case, k: np.ndarray, v: np.ndarray):
-    """Append one token per (sequence, KV head): k, v float32 [batch, Hkv, d]."""
-    c.ctx.paris_append_decode(to_dev(k, c.dtype), to_dev(v, c.dtype))
+def append(c: Case, k: np.ndarray, v: np.ndarray, device: bool = True):
+    """Append one token per (sequence, KV head): k, v float32 [batch, Hkv, d].
+    device=False only updates the host-side mirror (the library already has it)."""
+    if device:
+        c.ctx.paris_append_decode(to_dev(k, c.dtype), to_dev(v, c.dtype))
     c.K = np.concatenate([c.K, as_seen(k, c.dtype)[:, :, None, :]], axis=2)
     c.V = np.concatenate([c.V, as_seen(v, c.dtype)[:, :, None, :]], axis=2)
     c.zones.append()

@@ -192,3 +192,35 @@ def test_retrieval_zone_in_host_memory_matches_hbm():
         g.append(b, k, v)
     qd, idx, k_eff = g.check_retrieve(b, g.queries_from_zone(b, step=5))
     g.check_attention(b, qd, idx, k_eff)
+
+
+def test_decode_step_equals_the_three_calls():
+    """paris_decode_step (append fused into the vote kernel) gives exactly
+    what append + retrieve + sparse_attend give, across flushes."""
+    kw = dict(seed=24, batch=2, n_kv_heads=2, n_q_heads=4, sink=16, local=64, update_buf=16, topk=64,
+              cand_bp=500, rho=4)
+    a = g.make_case(16 + 20000 + 64, **kw)
+    b = g.make_case(16 + 20000 + 64, **kw)
+    shp = (2, 4, 64)
+    for t in range(60):
+        k = synth.drift_keys(24, 2, 2, t, 128, a.scale, rate=0.3)
+        v = synth.decode_values(24, 2, 2, t, 128)
+        q = g.queries_from_zone(a, step=t)
+        kd, vd, qd = g.to_dev(k, torch.bfloat16), g.to_dev(v, torch.bfloat16), g.to_dev(q, torch.bfloat16)
+        ia = torch.empty(shp, dtype=torch.int32, device="cuda")
+        sa = torch.empty(shp, dtype=torch.float32, device="cuda")
+        oa = torch.empty((2, 4, 128), dtype=torch.bfloat16, device="cuda")
+        ib, sb, ob = torch.empty_like(ia), torch.empty_like(sa), torch.empty_like(oa)
+        a.ctx.paris_append_decode(kd, vd)
+        ka = a.ctx.paris_retrieve(qd, ia, sa)
+        a.ctx.paris_sparse_attend(qd, ia, oa)
+        kb = b.ctx.paris_decode_step(kd, vd, qd, ib, sb, ob)
+        torch.cuda.synchronize()
+        assert ka == kb
+        assert torch.equal(ia, ib) and torch.equal(sa, sb) and torch.equal(oa, ob), t
+        g.append(a, k, v, device=False)  # host-side mirror of what both contexts now hold
+        if t % 20 == 19:
+            g.check_state(a)
+            qd2, idx, k_eff = g.check_retrieve(a, q)
+            g.check_attention(a, qd2, idx, k_eff)
+    assert a.ctx.paris_get_state()["n_flushes"] == b.ctx.paris_get_state()["n_flushes"] > 0
