@@ -280,7 +280,7 @@ def run_ours(args, rank, world):
             a[1] += n
     del g_prof
     kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
-    us_retrieve = sum(1e3 * prof[k][0] for k in ("vote", "select", "fill")) / args.steps
+    us_retrieve = sum(1e3 * prof[k][0] for k in ("vote", "compact", "rerank", "fill")) / args.steps
     us_attend = 1e3 * prof["attend"][0] / args.steps
     us_append = sum(1e3 * prof[k][0] for k in ("append", "build_index")) / args.steps
 
@@ -293,7 +293,9 @@ def run_ours(args, rank, world):
         # votes read back (1 B per key and query head), candidate records
         # (64 B codes + 64 B w) gathered, candidate index + estimate written,
         # top-k index + estimate written
-        "select": b * hq * (int(Nmean) + C * (128 + 8) + keff * 8),
+        "rerank": b * hq * (C * (4 + 128 + 4) + keff * 8),
+        # votes read (1 B per key and query head), candidate positions written
+        "compact": b * hq * (int(Nmean) + C * 4),
         # retrieved K and V rows, plus the window rows once per KV head
         "attend": b * hq * keff * 4 * d + b * hkv * nwin * 4 * d,
     }
@@ -305,7 +307,7 @@ def run_ours(args, rank, world):
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom),
                 "algorithmic_bytes": alg[dom]}
-    retr_bytes = alg["select"] + b * hq * (w["rho"] * w["n_sub"]) * (Nmean / 256) * 2
+    retr_bytes = alg["rerank"] + b * hq * (w["rho"] * w["n_sub"]) * (Nmean / 256) * 2
     retrieve_frac = retr_bytes / (us_retrieve * 1e-6) / 1e9 / peak
 
     # end to end through the public API with host buffers

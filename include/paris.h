@@ -150,7 +150,7 @@ paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtyp
 
 /* One decode step: exactly paris_append_decode(k, v), then
  * paris_retrieve(q, ...), then paris_sparse_attend(q, topk_idx, out), with the
- * same arguments and results, in three kernels instead of five: the append
+ * same arguments and results, in four kernels instead of five: the append
  * rides in the vote kernel unless it fills the Update Buffer (then the flush
  * and index rebuild run first).  k, v: device, kv_dtype, [batch][Hkv][d];
  * q: device, q_dtype, [batch][Hq][d]; outputs as in the two calls.          */
@@ -197,12 +197,13 @@ typedef enum {
   PARIS_KERNEL_ENCODE = 1,      /* prefill: SRHT, bucket ids, codes, w                   */
   PARIS_KERNEL_BUILD_INDEX = 2, /* per-chunk inverted bucket index                       */
   PARIS_KERNEL_APPEND = 3,      /* standalone decode append (store + encode one token)   */
-  PARIS_KERNEL_VOTE = 4,        /* query rotation, top-rho centroids, collision votes,
-                                   candidate plan (and a fused append in decode steps)  */
-  PARIS_KERNEL_SELECT = 5,      /* candidate selection, RSQ-IP estimates, top-k          */
-  PARIS_KERNEL_ATTEND = 6,      /* sparse attention and the merge of its splits          */
-  PARIS_KERNEL_FILL = 7,        /* empty-result fill                                     */
-  PARIS_KERNEL_COUNT = 8
+  PARIS_KERNEL_VOTE = 4,        /* query rotation, top-rho centroids, collision votes
+                                   (and a fused append in decode steps)                 */
+  PARIS_KERNEL_COMPACT = 5,     /* candidate selection (ordered compaction)              */
+  PARIS_KERNEL_RERANK = 6,      /* RSQ-IP estimates of the candidates, top-k             */
+  PARIS_KERNEL_ATTEND = 7,      /* sparse attention and the merge of its splits          */
+  PARIS_KERNEL_FILL = 8,        /* empty-result fill                                     */
+  PARIS_KERNEL_COUNT = 9
 } paris_kernel;
 
 /* Cumulative kernel launches of this context since paris_create, per

@@ -7,12 +7,14 @@
 // "Unified Virtual Addressing (UVA) offloading" and "Sliding-window update
 // mechanism" (Sink and Local on the GPU, the history offloaded).
 //
-// Split-row flash decoding: block (split, sequence x query head) runs an
-// online softmax over kAttnSplit rows of the head's row list (window rows
-// first, then the retrieved rows) and writes (max, sum, o); the last split
-// of a query head to finish merges all splits (atomic counter after a
-// memory fence, no waiting).  Decode has one query row per head, so the work
-// is a gather plus matrix-vector products: CUDA cores, not tensor cores.
+// Split-row flash decoding: block (split, sequence x query head) stages the
+// K and V rows of its kAttnSplit rows (window rows first, then the retrieved
+// rows) in shared memory with asynchronous 16-byte copies, all in flight at
+// once, then computes softmax(q K^T / sqrt(d)) V for them and writes
+// (max, sum, o); the last split of a query head to finish merges the splits
+// (atomic counter after a memory fence, no waiting).  Decode has one query
+// row per head, so the work is a gather plus matrix-vector products: CUDA
+// cores, not tensor cores.
 #include <float.h>
 
 #include "paris_device.cuh"
@@ -20,21 +22,25 @@
 namespace paris {
 namespace {
 
-constexpr int kAttnThreads = 128;  // 4 warps x 32 rows
-constexpr int kRowsPerIter = 8;
+constexpr int kAttnThreads = 128;
+constexpr int kKStride = kDim + 8;  // bf16 elements per staged K row: 272 B keeps 16-byte reads conflict-free
 static_assert(kAttnThreads == kDim && kAttnThreads == kAttnSplit, "one thread per row and per output dimension");
 
-__device__ __forceinline__ float4 bf16x4_to_float4(uint2 u) {
-  return make_float4(bf16_bits_to_float(u.x & 0xffffu), bf16_bits_to_float(u.x >> 16),
-                     bf16_bits_to_float(u.y & 0xffffu), bf16_bits_to_float(u.y >> 16));
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
 }
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict__ q, int dtype, AttendArgs a,
                                                         int64_t nsink, int64_t nwin, int nsplit, float qscale) {
-  __shared__ const __nv_bfloat16* s_k[kAttnSplit];
-  __shared__ const __nv_bfloat16* s_v[kAttnSplit];
-  __shared__ float s_m[4], s_l[4];
-  __shared__ float s_o[4][kDim];
+  extern __shared__ __align__(16) uint16_t smem[];
+  uint16_t* ks = smem;                          // [kAttnSplit][kKStride]
+  uint16_t* vs = smem + kAttnSplit * kKStride;  // [kAttnSplit][kDim]
+  __shared__ float qf[kDim];
+  __shared__ float p[kAttnSplit];
+  __shared__ float red[8];
   __shared__ int s_last;
   const int split = blockIdx.x;
   const int sq = blockIdx.y;
@@ -42,112 +48,87 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   const int64_t sh = (int64_t)seq * a.s.hkv + kvh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t R = nwin + a.k_eff;
-  const int64_t r0 = (int64_t)split * kAttnSplit;
   const int ring = a.s.local + a.s.ubuf;
 
-  // row addresses of the split (nullptr: no row)
-  {
-    const int64_t r = r0 + tid;
-    const __nv_bfloat16 *kp = nullptr, *vp = nullptr;
-    if (r < R) {
-      if (r < nwin) {
-        int64_t slot = r;
-        if (r >= nsink) {
-          const int64_t pos = a.s.sink + a.N + (r - nsink);
-          slot = a.s.sink + (pos - a.s.sink) % ring;
-        }
-        kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
-        vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
-      } else {
-        const int64_t pos = __ldg(a.topk_idx + (int64_t)sq * a.k + (r - nwin));
-        if (pos >= a.s.sink && pos < a.s.sink + a.N) {
-          kp = a.kv.st_k + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
-          vp = a.kv.st_v + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
-        } else if (pos >= 0) {
-          atomicOr(a.status, kStatusBadIndex);
-        }
+  // row `tid` of the split: find it and copy its K and V rows
+  const int64_t r = (int64_t)split * kAttnSplit + tid;
+  const __nv_bfloat16 *kp = nullptr, *vp = nullptr;
+  if (r < R) {
+    if (r < nwin) {
+      int64_t slot = r;
+      if (r >= nsink) {
+        const int64_t pos = a.s.sink + a.N + (r - nsink);
+        slot = a.s.sink + (pos - a.s.sink) % ring;
+      }
+      kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
+      vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
+    } else {
+      const int64_t pos = __ldg(a.topk_idx + (int64_t)sq * a.k + (r - nwin));
+      if (pos >= a.s.sink && pos < a.s.sink + a.N) {
+        kp = a.kv.st_k + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
+        vp = a.kv.st_v + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
+      } else if (pos >= 0) {
+        atomicOr(a.status, kStatusBadIndex);
       }
     }
-    s_k[tid] = kp;
-    s_v[tid] = vp;
   }
-  float qv[4];
-  load4(q, dtype, (int64_t)sq * kDim + 4 * lane, qv);
+  if (kp) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) qv[i] *= qscale;
+    for (int j = 0; j < kDim / 8; ++j) {
+      cp_async16(ks + tid * kKStride + 8 * j, kp + 8 * j);
+      cp_async16(vs + tid * kDim + 8 * j, vp + 8 * j);
+    }
+  } else {
+    // no row: zeros, so the weighted V sum below reads finite values
+#pragma unroll
+    for (int j = 0; j < kDim / 8; ++j) *reinterpret_cast<uint4*>(vs + tid * kDim + 8 * j) = make_uint4(0, 0, 0, 0);
+  }
+  qf[tid] = load1(q, dtype, (int64_t)sq * kDim + tid) * qscale;
+  cp_async_wait_all();
   __syncthreads();
 
-  float m = -FLT_MAX, l = 0.f;
-  float o[4] = {0.f, 0.f, 0.f, 0.f};
-  // warp w takes rows 32w .. 32w + 31 of the split, kRowsPerIter at a time,
-  // K and V of all of them in flight together
-#pragma unroll 1
-  for (int rb = 32 * warp; rb < 32 * warp + 32; rb += kRowsPerIter) {
-    uint2 kr[kRowsPerIter], vr[kRowsPerIter];
-    bool valid[kRowsPerIter];
+  // score of row tid (log2 domain)
+  float s = -FLT_MAX;
+  if (kp) {
+    float acc = 0.f;
 #pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const __nv_bfloat16* kp = s_k[rb + u];
-      const __nv_bfloat16* vp = s_v[rb + u];
-      valid[u] = kp != nullptr;
-      kr[u] = valid[u] ? *reinterpret_cast<const uint2*>(kp + 4 * lane) : make_uint2(0, 0);
-      vr[u] = valid[u] ? *reinterpret_cast<const uint2*>(vp + 4 * lane) : make_uint2(0, 0);
+    for (int j = 0; j < kDim / 8; ++j) {
+      const uint4 kv8 = *reinterpret_cast<const uint4*>(ks + tid * kKStride + 8 * j);
+      const uint32_t w[4] = {kv8.x, kv8.y, kv8.z, kv8.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc += qf[8 * j + 2 * i] * bf16_bits_to_float(w[i] & 0xffffu);
+        acc += qf[8 * j + 2 * i + 1] * bf16_bits_to_float(w[i] >> 16);
+      }
     }
-    float sc[kRowsPerIter];
-#pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const float4 kf = bf16x4_to_float4(kr[u]);
-      sc[u] = qv[0] * kf.x + qv[1] * kf.y + qv[2] * kf.z + qv[3] * kf.w;
-    }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) {
-#pragma unroll
-      for (int u = 0; u < kRowsPerIter; ++u) sc[u] += __shfl_xor_sync(kFull, sc[u], s);
-    }
-    float mn = m;
-#pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u)
-      if (valid[u]) mn = fmaxf(mn, sc[u]);
-    const float corr = exp2f(m - mn);
-    l *= corr;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] *= corr;
-    m = mn;
-#pragma unroll
-    for (int u = 0; u < kRowsPerIter; ++u) {
-      const float pr = valid[u] ? exp2f(sc[u] - m) : 0.f;
-      const float4 vf = bf16x4_to_float4(vr[u]);
-      l += pr;
-      o[0] += pr * vf.x;
-      o[1] += pr * vf.y;
-      o[2] += pr * vf.z;
-      o[3] += pr * vf.w;
-    }
+    s = acc;
   }
-  if (lane == 0) {
-    s_m[warp] = m;
-    s_l[warp] = l;
-  }
+  float mx = s;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) s_o[warp][4 * lane + i] = o[i];
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  if (lane == 0) red[warp] = mx;
   __syncthreads();
-  float* part = a.part + (int64_t)sq * a.nsplit_max * kPartStride;
-  {
-    const float M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
-    float f[4], L = 0.f;
+  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  const float pr = kp ? exp2f(s - M) : 0.f;
+  p[tid] = pr;
+  float l = pr;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      f[w] = s_l[w] > 0.f ? exp2f(s_m[w] - M) : 0.f;
-      L += s_l[w] * f[w];
-    }
-    float* out = part + (int64_t)split * kPartStride;
-    const int d = tid;  // kAttnThreads == kDim
-    out[4 + d] = s_o[0][d] * f[0] + s_o[1][d] * f[1] + s_o[2][d] * f[2] + s_o[3][d] * f[3];
-    if (tid == 0) {
-      out[0] = M;
-      out[1] = L;
-    }
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+  if (lane == 0) red[4 + warp] = l;
+  __syncthreads();
+  const float L = red[4] + red[5] + red[6] + red[7];
+  // o[d] for d = tid over the split's rows
+  const int nrows = (int)min64(kAttnSplit, R - (int64_t)split * kAttnSplit);
+  float acc = 0.f;
+  for (int rr = 0; rr < nrows; ++rr) acc += p[rr] * bf16_bits_to_float(vs[rr * kDim + tid]);
+  float* part = a.part + (int64_t)sq * a.nsplit_max * kPartStride;
+  float* out = part + (int64_t)split * kPartStride;
+  out[4 + tid] = acc;
+  if (tid == 0) {
+    out[0] = M;
+    out[1] = L;
   }
+
   // the last split of the query head merges all splits
   __threadfence();
   __syncthreads();
@@ -156,7 +137,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   if (!s_last) return;
   __threadfence();
   const int d = tid;
-  float M = -FLT_MAX;
+  float Mx = -FLT_MAX;
   for (int s0 = 0; s0 < nsplit; s0 += 8) {
     float mm[8], ll[8];
 #pragma unroll
@@ -167,31 +148,33 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-      if (ll[u] > 0.f) M = fmaxf(M, mm[u]);
+      if (ll[u] > 0.f) Mx = fmaxf(Mx, mm[u]);
   }
-  float L = 0.f, acc = 0.f;
+  float Lt = 0.f, ot = 0.f;
   for (int s0 = 0; s0 < nsplit; s0 += 8) {
     float mm[8], ll[8], oo[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const bool in = s0 + u < nsplit;
-      const float* p = part + (int64_t)(s0 + u) * kPartStride;
-      mm[u] = in ? __ldcg(p) : 0.f;
-      ll[u] = in ? __ldcg(p + 1) : 0.f;
-      oo[u] = in ? __ldcg(p + 4 + d) : 0.f;
+      const float* pp = part + (int64_t)(s0 + u) * kPartStride;
+      mm[u] = in ? __ldcg(pp) : 0.f;
+      ll[u] = in ? __ldcg(pp + 1) : 0.f;
+      oo[u] = in ? __ldcg(pp + 4 + d) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (ll[u] > 0.f) {
-        const float f = exp2f(mm[u] - M);
-        L += ll[u] * f;
-        acc += oo[u] * f;
+        const float f = exp2f(mm[u] - Mx);
+        Lt += ll[u] * f;
+        ot += oo[u] * f;
       }
     }
   }
-  a.out[(int64_t)sq * kDim + d] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
+  a.out[(int64_t)sq * kDim + d] = __float2bfloat16_rn(Lt > 0.f ? ot / Lt : 0.f);
   if (tid == 0) a.counter[sq] = 0;
 }
+
+constexpr size_t kAttendSmem = (size_t)kAttnSplit * (kKStride + kDim) * sizeof(uint16_t);
 
 }  // namespace
 
@@ -205,10 +188,17 @@ int attend_splits(const AttendArgs& a) {
 cudaError_t launch_attend(const void* q, int dtype, const AttendArgs& a, cudaStream_t st) {
   const int nsplit = attend_splits(a);
   if (nsplit > a.nsplit_max) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttendSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   const int64_t nsink = min64(a.s.sink, a.T);
   const int64_t nwin = nsink + a.n_local_buf;
   const float qscale = 1.4426950408889634f / sqrtf((float)kDim);
-  k_attend<<<dim3(nsplit, a.s.batch * a.s.hq), kAttnThreads, 0, st>>>(q, dtype, a, nsink, nwin, nsplit, qscale);
+  k_attend<<<dim3(nsplit, a.s.batch * a.s.hq), kAttnThreads, kAttendSmem, st>>>(q, dtype, a, nsink, nwin, nsplit,
+                                                                                 qscale);
   return cudaGetLastError();
 }
 

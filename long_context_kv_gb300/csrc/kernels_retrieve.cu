@@ -1,16 +1,18 @@
-// Retrieval kernels of ParisKV: (A) query preparation + collision votes +
-// candidate plan, (B) candidate selection + RSQ-IP rerank + top-k.
+// Retrieval kernels of ParisKV.
+//
+//   k_vote     query preparation + collision votes, one block per tile
+//              (chunk of kChunk Retrieval-zone keys, sequence x query head);
+//   k_compact  candidate selection (ordered compaction), same tiles;
+//   k_rerank   RSQ-IP estimates of every candidate, blocks spread evenly over
+//              the candidates of each query head; the last block of a query
+//              head takes its top-k.
 //
 // ParisKV: Fast and Drift-Robust KV-Cache Retrieval for Long-Context LLMs --
 // Methodology 2, "Coarse candidate generation (collision-based)" and
 // "Candidate reranking (RSQ-IP)", "Estimation":
 //   <k, q> ~ ||q||_2 sum_b w_{i,b} <v_{i,b}, q~_b>.
-//
-// Both kernels run one block per tile = (chunk of kChunk Retrieval-zone
-// keys, sequence x query head).  The per-query-head reductions (the
-// candidate plan after A, the top-k after B) are done by the last block of
-// the query head to finish, found with an atomic counter after a memory
-// fence; no block ever waits for another.
+// The last-block reduction finds its block with an atomic counter after a
+// memory fence; no block ever waits for another.
 #include <float.h>
 
 #include "paris_device.cuh"
@@ -19,13 +21,16 @@ namespace paris {
 namespace {
 
 constexpr int kVoteThreads = 256;
-constexpr int kSelThreads = 256;
-constexpr int kTopBins = 2048;         // = 8 * kSelThreads
-constexpr int kRankMax = 512;          // threshold-bin size resolved by pairwise ranks
-constexpr int kStageMax = kChunk / 2;  // candidate keys the top-k stages in shared memory
+constexpr int kCompactThreads = 256;
+constexpr int kRerankThreads = 256;
+constexpr int kRerankPer = 3;                      // candidates per thread, all loads in flight together
+constexpr int kTopBins = 8 * kRerankThreads;       // 2048
+constexpr int kRankMax = 512;                      // threshold-bin size resolved by pairwise ranks
+constexpr int kTopRegs = 32;                       // candidates per thread the top-k holds in registers
+constexpr int kHistRegs = 8;                       // histogram cells per thread held by k_compact
 
 // ===========================================================================
-// (A) query preparation, votes, plan
+// k_vote
 // ===========================================================================
 //
 // Query preparation (every tile recomputes the rotation and the hot
@@ -37,17 +42,14 @@ constexpr int kStageMax = kChunk / 2;  // candidate keys the top-k stages in sha
 //   (score desc, id asc) get weight rho - r (rank r) or 1 (flat).
 // Votes: each key of the chunk sits in exactly one bucket per subspace, so
 // walking the hot buckets' lists and adding their weights gives every key
-// sum_b weight_b(id_{i,b}) (one byte per key, at most 255).
-// Plan (last tile of the query head): T = the largest vote value whose
-// suffix count reaches C; keys above T are candidates, then keys equal to T
-// in ascending index order until C.  Per chunk: candidates in earlier
-// chunks, and how many keys equal to T the chunk may still take.
+// sum_b weight_b(id_{i,b}) (one byte per key, at most 255).  The tile
+// writes its votes and their histogram.
 struct VoteArgs {
   Tables t;
   SignMask sm;
   Shape s;
-  int rho, flat, nbins, nch, plan_stride;
-  int64_t N, C;
+  int rho, flat, nbins;
+  int64_t N;
   const void* q;
   int qdtype;
   float* qt;
@@ -55,8 +57,6 @@ struct VoteArgs {
   uint32_t* hot;
   uint8_t* votes;
   uint32_t* hist;
-  int32_t* plan;
-  uint32_t* counter;
   // fused append of one decode token (k_new == nullptr: none)
   const void* k_new;
   const void* v_new;
@@ -76,11 +76,8 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   uint32_t* hwt = hpre + nhot + 1;                                       // nhot
   __shared__ float qs[kDim], zs[kDim];
   __shared__ uint32_t hist[kMaxBins];
-  __shared__ uint32_t s_gt[kMaxChunks], s_eq[kMaxChunks];
   __shared__ uint32_t tmp[33];
   __shared__ float s_zn;
-  __shared__ int s_last, s_T;
-  __shared__ int64_t s_quota;
 
   const int c = blockIdx.x, sq = blockIdx.y;
   const int seq = sq / a.s.hq, qh = sq - seq * a.s.hq, kvh = qh / a.s.g;
@@ -204,21 +201,23 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   }
   __syncthreads();
   const uint32_t total = hpre[nhot];
-  for (uint32_t f0 = tid; f0 < total; f0 += 8 * blockDim.x) {
+  // thread t takes 8 consecutive list entries: one search, then linear steps
+  for (uint32_t f0 = 8 * tid; f0 < total; f0 += 8 * blockDim.x) {
+    int e = 0, hi = nhot - 1;  // last e with hpre[e] <= f0 (a non-empty list)
+    while (e < hi) {
+      const int mid = (e + hi + 1) >> 1;
+      if (hpre[mid] <= f0) e = mid; else hi = mid - 1;
+    }
     uint32_t key[8], wt[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint32_t f = f0 + u * blockDim.x;
+      const uint32_t f = f0 + u;
       wt[u] = 0;
       key[u] = 0;
       if (f < total) {
-        int lo = 0, hi = nhot - 1;  // last e with hpre[e] <= f
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (hpre[mid] <= f) lo = mid; else hi = mid - 1;
-        }
-        key[u] = __ldg(ent + hbeg[lo] + (f - hpre[lo]));
-        wt[u] = hwt[lo];
+        while (hpre[e + 1] <= f) ++e;
+        key[u] = __ldg(ent + hbeg[e] + (f - hpre[e]));
+        wt[u] = hwt[e];
       }
     }
 #pragma unroll
@@ -247,34 +246,71 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   block_excl_scan(nz, tmp, &nz_total);
   uint32_t* hout = a.hist + ((int64_t)sq * a.t.nchunk + c) * kMaxBins;
   for (int s = tid; s < a.nbins; s += blockDim.x) hout[s] = s == 0 ? (uint32_t)len - nz_total : hist[s];
+}
 
-  // -- phase 4: the last tile of the query head writes the plan --------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&a.counter[sq], 1u) == (uint32_t)(a.nch - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const uint32_t* hin = a.hist + (int64_t)sq * a.t.nchunk * kMaxBins;
-  for (int s = tid; s < kMaxBins; s += blockDim.x) {
-    uint32_t tot = 0;
-    if (s < a.nbins) {
-      for (int c0 = 0; c0 < a.nch; c0 += 8) {
-        uint32_t x[8];
+// ===========================================================================
+// k_compact
+// ===========================================================================
+//
+// The candidates are the first C keys by (votes desc, index asc): with T the
+// largest vote value whose suffix count reaches C, every key above T and the
+// lowest-index keys equal to T, up to C.  Each tile derives T and its own
+// offsets from all chunk histograms of its query head, then writes its
+// candidates' positions at their place in the ascending-position list.
+struct CompactArgs {
+  int nbins, nch, sink, nchunk;
+  int64_t N, C, cmax;
+  const uint8_t* votes;
+  const uint32_t* hist;
+  int32_t* cand_idx;
+};
+
+__global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
+  __shared__ __align__(16) uint32_t vsm[kChunk / 4];
+  __shared__ uint32_t tot[kMaxBins];
+  __shared__ uint32_t tmp[33];
+  __shared__ int s_T;
+  __shared__ int64_t s_quota;
+  const int c = blockIdx.x, sq = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t base = (int64_t)c * kChunk;
+  const int len = (int)min64(kChunk, a.N - base);
+  const int nitems = a.nch * a.nbins;
+  const uint32_t* h = a.hist + (int64_t)sq * a.nchunk * kMaxBins;
+
+  for (int i = tid; i < kMaxBins; i += blockDim.x) tot[i] = 0;
+  // loads in flight together: histogram cells and this chunk's votes
+  uint32_t hv[kHistRegs];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = c0 + u < a.nch ? __ldcg(hin + (int64_t)(c0 + u) * kMaxBins + s) : 0u;
+  for (int u = 0; u < kHistRegs; ++u) {
+    const int i = tid + u * blockDim.x;
+    hv[u] = i < nitems ? __ldcg(h + (int64_t)(i / a.nbins) * kMaxBins + i % a.nbins) : 0u;
+  }
+  {
+    const uint4* vin = reinterpret_cast<const uint4*>(a.votes + (int64_t)sq * a.nchunk * kChunk + base);
+    uint4 x[kChunk / 16 / kCompactThreads];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) tot += x[u];
-      }
-    }
-    hist[s] = tot;
+    for (int u = 0; u < kChunk / 16 / kCompactThreads; ++u) x[u] = __ldcg(vin + tid + u * kCompactThreads);
+#pragma unroll
+    for (int u = 0; u < kChunk / 16 / kCompactThreads; ++u)
+      reinterpret_cast<uint4*>(vsm)[tid + u * kCompactThreads] = x[u];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kHistRegs; ++u) {
+    const int i = tid + u * blockDim.x;
+    if (i < nitems && hv[u]) atomicAdd(&tot[i % a.nbins], hv[u]);
+  }
+  for (int i = tid + kHistRegs * blockDim.x; i < nitems; i += blockDim.x) {
+    const uint32_t x = __ldcg(h + (int64_t)(i / a.nbins) * kMaxBins + i % a.nbins);
+    if (x) atomicAdd(&tot[i % a.nbins], x);
   }
   __syncthreads();
   if (warp == 0) {
     // suffix sums from the top vote value down: lane l owns values 255-8l .. 248-8l
     uint32_t part = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) part += hist[255 - 8 * lane - i];
+    for (int i = 0; i < 8; ++i) part += tot[255 - 8 * lane - i];
     const uint32_t inc = warp_incl_scan(part, lane);
     const uint32_t exc = inc - part;
     const uint32_t C = (uint32_t)a.C;
@@ -284,11 +320,11 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
       int T = 255 - 8 * lane;
       for (int i = 0; i < 8; ++i) {
         const int s = 255 - 8 * lane - i;
-        if (run + hist[s] >= C) {
+        if (run + tot[s] >= C) {
           T = s;
           break;
         }
-        run += hist[s];
+        run += tot[s];
       }
       s_T = owner < 0 ? 0 : T;
       s_quota = (int64_t)a.C - (owner < 0 ? 0 : run);
@@ -296,271 +332,44 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   }
   __syncthreads();
   const int T = s_T;
-  // keys above T and equal to T in every chunk: one warp per chunk
-  for (int cc = warp; cc < a.nch; cc += kVoteThreads / 32) {
-    uint32_t x[8];
+  const int64_t quota = s_quota;
+  // keys above T / equal to T in the chunks before this one
+  uint32_t gt = 0, eq = 0;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int s = T + 1 + lane + 32 * u;
-      x[u] = s < a.nbins ? __ldcg(hin + (int64_t)cc * kMaxBins + s) : 0u;
-    }
-    uint32_t g = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) g += x[u];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(kFull, g, o);
-    if (lane == 0) {
-      s_gt[cc] = g;
-      s_eq[cc] = __ldcg(hin + (int64_t)cc * kMaxBins + T);
+  for (int u = 0; u < kHistRegs; ++u) {
+    const int i = tid + u * blockDim.x;
+    if (i < nitems && i / a.nbins < c) {
+      const int s = i % a.nbins;
+      gt += s > T ? hv[u] : 0u;
+      eq += s == T ? hv[u] : 0u;
     }
   }
-  __syncthreads();
-  if (tid == 0) {
-    int32_t* pl = a.plan + (int64_t)sq * a.plan_stride;
-    pl[0] = T;
-    int64_t gt_before = 0, eq_before = 0;
-    const int64_t quota = s_quota;
-    for (int cc = 0; cc < a.nch; ++cc) {
-      pl[1 + 2 * cc] = (int32_t)(gt_before + min64(eq_before, quota));
-      pl[2 + 2 * cc] = (int32_t)max64(0, quota - eq_before);
-      gt_before += s_gt[cc];
-      eq_before += s_eq[cc];
+  for (int i = tid + kHistRegs * blockDim.x; i < nitems; i += blockDim.x) {
+    if (i / a.nbins < c) {
+      const int s = i % a.nbins;
+      const uint32_t x = __ldcg(h + (int64_t)(i / a.nbins) * kMaxBins + s);
+      gt += s > T ? x : 0u;
+      eq += s == T ? x : 0u;
     }
-    a.counter[sq] = 0;
   }
-}
+  uint32_t gt_before, eq_before;
+  block_excl_scan(gt, tmp, &gt_before);
+  block_excl_scan(eq, tmp, &eq_before);
+  const int64_t sel_before = gt_before + min64(eq_before, quota);
+  const int64_t eq_allow = max64(0, quota - (int64_t)eq_before);
 
-// ===========================================================================
-// (B) selection, rerank, top-k
-// ===========================================================================
-//
-// Estimate, float32 in this order:
-//   acc = 0; for b: dot = 0; for j: dot = dot + v_{b,j} q~_{b,j};
-//   acc = acc + w_b dot;   est = ||q|| acc,
-// where v_{b,j} q~_{b,j} comes from a per-query table of the 16 possible
-// products of each coordinate (sign bit x 8 levels), each rounded once.
-// Top-k (last tile of the query head): the k_eff-th best (estimate desc,
-// position asc) candidate is found from a 2048-bin histogram over the
-// estimates' range (bins are monotone in the estimate, so only the
-// threshold bin needs exact ranks) or, for a degenerate range, an 8-bit
-// radix select; every candidate at least as good is kept, listed in
-// ascending position order.
-struct SelectArgs {
-  Tables t;
-  RsqParams rp;
-  Shape s;
-  int nch, plan_stride;
-  int64_t N, C, k, k_eff, cmax;
-  const float* qt;
-  const float* qnorm;
-  const uint8_t* votes;
-  const int32_t* plan;
-  int32_t* cand_idx;
-  float* cand_est;
-  uint32_t* minmax;  // [batch*Hq][2] order keys, reset to (max, 0) after use
-  uint32_t* counter;
-  int32_t* out_idx;
-  float* out_score;
-};
-
-__device__ __forceinline__ float rerank_one(const uint4* rp4, const float* tq, float qn) {
-  uint32_t cw[16];
-  float ww[16];
+  // ordered compaction: thread t owns keys [64t, 64t + 64) = words [16t, 16t + 16)
+  constexpr int kWords = kChunk / 4 / kCompactThreads;
+  const int k0 = tid * 4 * kWords;
+  uint32_t vw[kWords];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 x = __ldg(rp4 + i);
-    cw[4 * i] = x.x; cw[4 * i + 1] = x.y; cw[4 * i + 2] = x.z; cw[4 * i + 3] = x.w;
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 x = __ldg(rp4 + 4 + i);
-    ww[4 * i] = __uint_as_float(x.x); ww[4 * i + 1] = __uint_as_float(x.y);
-    ww[4 * i + 2] = __uint_as_float(x.z); ww[4 * i + 3] = __uint_as_float(x.w);
-  }
-  float acc = 0.f;
-#pragma unroll
-  for (int b = 0; b < kSub; ++b) {
-    float dot = 0.f;
-#pragma unroll
-    for (int j = 0; j < kM; ++j) dot = __fadd_rn(dot, tq[(b * kM + j) * 16 + ((cw[b] >> (4 * j)) & 15u)]);
-    acc = __fadd_rn(acc, __fmul_rn(ww[b], dot));
-  }
-  return __fmul_rn(qn, acc);
-}
-
-// The kk-th best (key desc, position asc) of C candidates, 1 <= kk < C, where
-// key_at(i) is the order key of candidate i.  All threads get the result.
-template <typename KeyAt>
-__device__ void kth_best(int64_t C, int64_t kk, uint32_t kmin, uint32_t kmax, KeyAt key_at, uint32_t* bins,
-                         uint32_t* list, uint32_t* tmp, uint32_t* out_key, int64_t* out_pos) {
-  __shared__ uint32_t s_b, s_above, s_m, s_key;
-  __shared__ int64_t s_pos;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const float fmin = key_to_float(kmin), fmax = key_to_float(kmax);
-  const float range = fmax - fmin;
-  bool linear = kmax > kmin && range > 0.f && range <= FLT_MAX;
-  const float scale = linear ? (float)kTopBins / range : 0.f;
-  linear = linear && scale > 0.f && scale <= FLT_MAX;
-  if (linear) {
-    for (int i = tid; i < kTopBins; i += nt) bins[i] = 0;
-    if (tid == 0) s_m = 0;
-    __syncthreads();
-    for (int64_t i = tid; i < C; i += nt) {
-      const float e = key_to_float(key_at(i));
-      atomicAdd(&bins[min(kTopBins - 1, (int)((e - fmin) * scale))], 1u);
-    }
-    __syncthreads();
-    // thread t owns bins 2047 - 8t .. 2040 - 8t
-    uint32_t part = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) part += bins[kTopBins - 1 - 8 * tid - i];
-    uint32_t tot;
-    const uint32_t exc = block_excl_scan(part, tmp, &tot);
-    if (exc < (uint32_t)kk && exc + part >= (uint32_t)kk) {
-      uint32_t run = exc;
-      for (int i = 0; i < 8; ++i) {
-        const int bb = kTopBins - 1 - 8 * tid - i;
-        if (run + bins[bb] >= (uint32_t)kk) {
-          s_b = (uint32_t)bb;
-          s_above = run;
-          break;
-        }
-        run += bins[bb];
-      }
-    }
-    __syncthreads();
-    const int bstar = (int)s_b;
-    for (int64_t i = tid; i < C; i += nt) {
-      const float e = key_to_float(key_at(i));
-      if (min(kTopBins - 1, (int)((e - fmin) * scale)) == bstar) {
-        const uint32_t slot = atomicAdd(&s_m, 1u);
-        if (slot < kRankMax) list[slot] = (uint32_t)i;
-      }
-    }
-    __syncthreads();
-    const uint32_t m = s_m;
-    if (m <= kRankMax) {
-      const uint32_t need = (uint32_t)kk - s_above;  // 1 <= need <= m
-      for (uint32_t x = tid; x < m; x += nt) {
-        const uint32_t pi = list[x], ki = key_at(pi);
-        uint32_t rank = 0;
-        for (uint32_t y = 0; y < m; ++y) {
-          const uint32_t pj = list[y], kj = key_at(pj);
-          rank += (kj > ki || (kj == ki && pj < pi)) ? 1u : 0u;
-        }
-        if (rank == need - 1) {
-          s_key = ki;
-          s_pos = pi;
-        }
-      }
-      __syncthreads();
-      *out_key = s_key;
-      *out_pos = s_pos;
-      return;
-    }
-  }
-  // radix select of the kk-th largest key, 8 bits at a time
-  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)kk;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += nt) bins[i] = 0;
-    __syncthreads();
-    for (int64_t i = tid; i < C; i += nt) {
-      const uint32_t key = key_at(i);
-      if ((key & mask) == prefix) atomicAdd(&bins[(key >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (tid < 32) {  // lane t owns digits 255 - 8t .. 248 - 8t
-      uint32_t part = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) part += bins[255 - 8 * tid - i];
-      const uint32_t inc = warp_incl_scan(part, tid);
-      const uint32_t exc = inc - part;
-      if (exc < remaining && inc >= remaining) {
-        uint32_t run = exc;
-        for (int i = 0; i < 8; ++i) {
-          const int dg = 255 - 8 * tid - i;
-          if (run + bins[dg] >= remaining) {
-            s_b = (uint32_t)dg;
-            s_above = run;
-            break;
-          }
-          run += bins[dg];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= s_b << shift;
-    mask |= 255u << shift;
-    remaining -= s_above;
-    __syncthreads();
-  }
-  // the remaining-th lowest position among keys equal to prefix
-  const int64_t per = (C + nt - 1) / nt;
-  const int64_t i0 = min64(C, tid * per), i1 = min64(C, i0 + per);
-  uint32_t n_eq = 0;
-  for (int64_t i = i0; i < i1; ++i) n_eq += key_at(i) == prefix ? 1u : 0u;
-  uint32_t tot;
-  const uint32_t before = block_excl_scan(n_eq, tmp, &tot);
-  if (before < remaining && before + n_eq >= remaining) {
-    uint32_t seen = before;
-    for (int64_t i = i0; i < i1; ++i) {
-      if (key_at(i) == prefix && ++seen == remaining) {
-        s_pos = i;
-        break;
-      }
-    }
-  }
-  __syncthreads();
-  *out_key = prefix;
-  *out_pos = s_pos;
-}
-
-__global__ void __launch_bounds__(kSelThreads, 2) k_select(SelectArgs a) {
-  __shared__ float tq[kDim * 16];
-  __shared__ __align__(16) uint32_t keys32[kStageMax];  // u16 candidate keys, later staged order keys
-  __shared__ uint32_t list[kRankMax];
-  __shared__ uint32_t tmp[33];
-  __shared__ uint32_t s_min[kSelThreads / 32], s_max[kSelThreads / 32];
-  __shared__ int s_last;
-  uint16_t* keys = reinterpret_cast<uint16_t*>(keys32);
-
-  const int c = blockIdx.x, sq = blockIdx.y;
-  const int seq = sq / a.s.hq, qh = sq - seq * a.s.hq, kvh = qh / a.s.g;
-  const int64_t sh = (int64_t)seq * a.s.hkv + kvh;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t base = (int64_t)c * kChunk;
-  const int len = (int)min64(kChunk, a.N - base);
-
-  // -- loads: plan, this chunk's votes, q~ -> product table ------------------
-  const int32_t* pl = a.plan + (int64_t)sq * a.plan_stride;
-  const int T = __ldcg(pl);
-  const int64_t sel_before = __ldcg(pl + 1 + 2 * c);
-  const int64_t eq_allow = __ldcg(pl + 2 + 2 * c);
-  constexpr int kPer = kChunk / kSelThreads;  // 64 keys per thread
-  const int k0 = tid * kPer;
-  const uint4* vin = reinterpret_cast<const uint4*>(a.votes + (int64_t)sq * a.t.nchunk * kChunk + base + k0);
-  uint32_t vw[kPer / 4];
-#pragma unroll
-  for (int i = 0; i < kPer / 16; ++i) {
-    const uint4 x = __ldcg(vin + i);
+  for (int i = 0; i < kWords / 4; ++i) {
+    const uint4 x = reinterpret_cast<const uint4*>(vsm)[tid * (kWords / 4) + i];
     vw[4 * i] = x.x; vw[4 * i + 1] = x.y; vw[4 * i + 2] = x.z; vw[4 * i + 3] = x.w;
   }
-  {
-    const int coord = tid >> 1, nb0 = (tid & 1) * 8;
-    const float qv = __ldcg(a.qt + (int64_t)sq * kDim + coord);
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int nib = nb0 + n;
-      const float l = a.rp.lev[nib & 7];
-      tq[coord * 16 + nib] = __fmul_rn((nib & 8) ? -l : l, qv);
-    }
-  }
-  const float qn = __ldcg(a.qnorm + sq);
-
-  // -- ordered compaction of this chunk's candidates ------------------------
   uint32_t n_eq = 0, n_gt = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
+  for (int i = 0; i < 4 * kWords; ++i) {
     const uint32_t v = (vw[i >> 2] >> (8 * (i & 3))) & 0xffu;
     const bool in = k0 + i < len;
     n_eq += (in && v == (uint32_t)T) ? 1u : 0u;
@@ -571,104 +380,382 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(SelectArgs a) {
   const uint32_t eq_take = (uint32_t)max64(0, min64((int64_t)n_eq, eq_allow - (int64_t)eq_rank0));
   uint32_t nsel;
   uint32_t pos = block_excl_scan(n_gt + eq_take, tmp, &nsel);
-  {
-    uint32_t eq_seen = 0;
+  int32_t* out = a.cand_idx + (int64_t)sq * a.cmax + sel_before;
+  uint32_t eq_seen = 0;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const uint32_t v = (vw[i >> 2] >> (8 * (i & 3))) & 0xffu;
-      const bool in = k0 + i < len;
-      bool take = in && v > (uint32_t)T;
-      if (in && v == (uint32_t)T) {
-        take = eq_seen < eq_take;
-        ++eq_seen;
-      }
-      if (take) keys[pos++] = (uint16_t)(k0 + i);
+  for (int i = 0; i < 4 * kWords; ++i) {
+    const uint32_t v = (vw[i >> 2] >> (8 * (i & 3))) & 0xffu;
+    const bool in = k0 + i < len;
+    bool take = in && v > (uint32_t)T;
+    if (in && v == (uint32_t)T) {
+      take = eq_seen < eq_take;
+      ++eq_seen;
     }
+    if (take) out[pos++] = (int32_t)(a.sink + base + k0 + i);
   }
-  __syncthreads();
+}
 
-  // -- rerank: one candidate per thread, 128 bytes in flight each ----------
-  int32_t* cidx = a.cand_idx + (int64_t)sq * a.cmax + sel_before;
-  float* cest = a.cand_est + (int64_t)sq * a.cmax + sel_before;
-  const uint8_t* rec = a.t.rec + (sh * a.t.rcap + base) * kRecBytes;
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (uint32_t r = tid; r < nsel; r += blockDim.x) {
-    const uint32_t key = keys[r];
-    const float e = rerank_one(reinterpret_cast<const uint4*>(rec + (int64_t)key * kRecBytes), tq, qn);
-    cidx[r] = (int32_t)(a.s.sink + base + key);
-    cest[r] = e;
-    kmin = min(kmin, order_key(e));
-    kmax = max(kmax, order_key(e));
-  }
+// ===========================================================================
+// k_rerank
+// ===========================================================================
+//
+// Estimate, float32 in this order:
+//   acc = 0; for b: dot = 0; for j: dot = dot + v_{b,j} q~_{b,j};
+//   acc = acc + w_b dot;   est = ||q|| acc,
+// where v_{b,j} q~_{b,j} comes from a per-query table of the 16 possible
+// products of each coordinate (sign bit x 8 levels), each rounded once.
+// Top-k (last block of the query head): the k_eff-th best (estimate desc,
+// position asc) candidate is found from a 2048-bin histogram over the
+// estimates' range (bins are monotone in the estimate, so only the
+// threshold bin needs exact ranks) or, for a degenerate range, an 8-bit
+// radix select; every candidate at least as good is kept, listed in
+// ascending position order.
+struct RerankArgs {
+  Tables t;
+  RsqParams rp;
+  int hq, g, sink, nblk;
+  int64_t C, k, k_eff, cmax;
+  const float* qt;
+  const float* qnorm;
+  const int32_t* cand_idx;
+  float* cand_est;
+  uint32_t* counter;
+  int32_t* out_idx;
+  float* out_score;
+};
+
+__device__ __forceinline__ float rerank_record(const uint4 (&x)[8], const float* tq, float qn) {
+  float acc = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+  for (int b = 0; b < kSub; ++b) {
+    const uint4 cq = x[b >> 2];
+    const uint32_t cw = (b & 3) == 0 ? cq.x : (b & 3) == 1 ? cq.y : (b & 3) == 2 ? cq.z : cq.w;
+    const uint4 wq = x[4 + (b >> 2)];
+    const float w = __uint_as_float((b & 3) == 0 ? wq.x : (b & 3) == 1 ? wq.y : (b & 3) == 2 ? wq.z : wq.w);
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < kM; ++j) dot = __fadd_rn(dot, tq[(b * kM + j) * 16 + ((cw >> (4 * j)) & 15u)]);
+    acc = __fadd_rn(acc, __fmul_rn(w, dot));
   }
-  if (lane == 0) {
-    s_min[warp] = kmin;
-    s_max[warp] = kmax;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    for (int w = 1; w < kSelThreads / 32; ++w) {
-      kmin = min(kmin, s_min[w]);
-      kmax = max(kmax, s_max[w]);
-    }
-    if (nsel) {
-      atomicMin(&a.minmax[2 * sq], kmin);
-      atomicMax(&a.minmax[2 * sq + 1], kmax);
-    }
-  }
+  return __fmul_rn(qn, acc);
+}
 
-  // -- the last tile of the query head takes the top-k ----------------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&a.counter[sq], 1u) == (uint32_t)(a.nch - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+// Top-k of one query head's C candidates by the block (blockDim == kRerankThreads).
+__device__ void topk_block(const RerankArgs& a, int sq, float* bins_f, uint32_t* tmp) {
+  __shared__ uint32_t s_b, s_above, s_m, s_kkey;
+  __shared__ int64_t s_kpos;
+  __shared__ uint32_t s_list_key[kRankMax], s_list_pos[kRankMax];
+  __shared__ uint32_t s_min[kRerankThreads / 32], s_max[kRerankThreads / 32];
+  uint32_t* bins = reinterpret_cast<uint32_t*>(bins_f);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t C = a.C, kk = a.k_eff;
   const float* est = a.cand_est + (int64_t)sq * a.cmax;
   const int32_t* cid = a.cand_idx + (int64_t)sq * a.cmax;
   int32_t* oi = a.out_idx + (int64_t)sq * a.k;
   float* os = a.out_score ? a.out_score + (int64_t)sq * a.k : nullptr;
-  const uint32_t gmin = __ldcg(a.minmax + 2 * sq), gmax = __ldcg(a.minmax + 2 * sq + 1);
-  const bool staged = C <= kStageMax;
-  if (staged)
-    for (int64_t i = tid; i < C; i += blockDim.x) keys32[i] = order_key(__ldcg(est + i));
-  __syncthreads();
-  auto key_at = [&](int64_t i) -> uint32_t { return staged ? keys32[i] : order_key(__ldcg(est + i)); };
-  uint32_t kstar = 0;
-  int64_t pstar = C - 1;
-  if (kk < C) kth_best(C, kk, gmin, gmax, key_at, reinterpret_cast<uint32_t*>(tq), list, tmp, &kstar, &pstar);
-  // ordered compaction: keep (key, position) at least as good as (kstar, pstar)
-  const int64_t per = (C + blockDim.x - 1) / blockDim.x;
-  const int64_t i0 = min64(C, tid * per), i1 = min64(C, i0 + per);
-  uint32_t cnt = 0;
-  for (int64_t i = i0; i < i1; ++i) {
-    const uint32_t key = key_at(i);
-    cnt += (kk >= C || key > kstar || (key == kstar && i <= pstar)) ? 1u : 0u;
-  }
-  uint32_t tot;
-  uint32_t opos = block_excl_scan(cnt, tmp, &tot);
-  for (int64_t i = i0; i < i1; ++i) {
-    const uint32_t key = key_at(i);
-    if (kk >= C || key > kstar || (key == kstar && i <= pstar)) {
-      oi[opos] = __ldcg(cid + i);
-      if (os) os[opos] = __ldcg(est + i);
-      ++opos;
+  const int64_t per = (C + kRerankThreads - 1) / kRerankThreads;
+  const int64_t i0 = min64(C, tid * per);
+  const int n = (int)(min64(C, i0 + per) - i0);
+
+  if (per > kTopRegs) {
+    // large candidate sets: the same selection, reading the candidates from L2
+    // (radix select, then the remaining-th lowest position among ties)
+    uint32_t prefix = 0, mask = 0, remaining = (uint32_t)kk;
+    if (kk < C) {
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += blockDim.x) bins[i] = 0;
+        __syncthreads();
+        for (int64_t i = tid; i < C; i += blockDim.x) {
+          const uint32_t key = order_key(__ldcg(est + i));
+          if ((key & mask) == prefix) atomicAdd(&bins[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+          uint32_t part = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) part += bins[255 - 8 * lane - i];
+          const uint32_t inc = warp_incl_scan(part, lane);
+          const uint32_t exc = inc - part;
+          if (exc < remaining && inc >= remaining) {
+            uint32_t run = exc;
+            for (int i = 0; i < 8; ++i) {
+              const int dg = 255 - 8 * lane - i;
+              if (run + bins[dg] >= remaining) {
+                s_b = (uint32_t)dg;
+                s_above = run;
+                break;
+              }
+              run += bins[dg];
+            }
+          }
+        }
+        __syncthreads();
+        prefix |= s_b << shift;
+        mask |= 255u << shift;
+        remaining -= s_above;
+        __syncthreads();
+      }
+    }
+    uint32_t n_eq = 0;
+    for (int64_t i = i0; i < i0 + n; ++i) n_eq += order_key(__ldcg(est + i)) == prefix ? 1u : 0u;
+    uint32_t tot;
+    const uint32_t before = block_excl_scan(n_eq, tmp, &tot);
+    if (kk < C && before < remaining && before + n_eq >= remaining) {
+      uint32_t seen = before;
+      for (int64_t i = i0; i < i0 + n; ++i)
+        if (order_key(__ldcg(est + i)) == prefix && ++seen == remaining) {
+          s_kpos = i;
+          break;
+        }
+    }
+    __syncthreads();
+    const int64_t pstar = kk < C ? s_kpos : C;
+    uint32_t cnt = 0;
+    for (int64_t i = i0; i < i0 + n; ++i) {
+      const uint32_t key = order_key(__ldcg(est + i));
+      cnt += (kk >= C || key > prefix || (key == prefix && i <= pstar)) ? 1u : 0u;
+    }
+    uint32_t opos = block_excl_scan(cnt, tmp, &tot);
+    for (int64_t i = i0; i < i0 + n; ++i) {
+      const float e = __ldcg(est + i);
+      const uint32_t key = order_key(e);
+      if (kk >= C || key > prefix || (key == prefix && i <= pstar)) {
+        oi[opos] = __ldcg(cid + i);
+        if (os) os[opos] = e;
+        ++opos;
+      }
+    }
+  } else {
+    // the thread's contiguous slice of candidates, all loads in flight together
+    float e[kTopRegs];
+    int32_t ix[kTopRegs];
+#pragma unroll
+    for (int u = 0; u < kTopRegs; ++u) {
+      e[u] = u < n ? __ldcg(est + i0 + u) : 0.f;
+      ix[u] = u < n ? __ldcg(cid + i0 + u) : 0;
+    }
+    uint32_t kstar = 0;
+    int64_t pstar = C;
+    if (kk < C) {
+      uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+      for (int u = 0; u < kTopRegs; ++u)
+        if (u < n) {
+          kmin = min(kmin, order_key(e[u]));
+          kmax = max(kmax, order_key(e[u]));
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
+      }
+      if (lane == 0) {
+        s_min[warp] = kmin;
+        s_max[warp] = kmax;
+      }
+      for (int i = tid; i < kTopBins; i += blockDim.x) bins[i] = 0;
+      if (tid == 0) s_m = 0;
+      __syncthreads();
+      kmin = s_min[0];
+      kmax = s_max[0];
+      for (int w = 1; w < kRerankThreads / 32; ++w) {
+        kmin = min(kmin, s_min[w]);
+        kmax = max(kmax, s_max[w]);
+      }
+      const float fmin = key_to_float(kmin), fmax = key_to_float(kmax);
+      const float range = fmax - fmin;
+      bool linear = kmax > kmin && range > 0.f && range <= FLT_MAX;
+      const float scale = linear ? (float)kTopBins / range : 0.f;
+      linear = linear && scale > 0.f && scale <= FLT_MAX;
+      bool resolved = false;
+      if (linear) {
+        // bins are a monotone function of the estimate (-0 counted as +0)
+        auto bin_of = [&](float v) { return min(kTopBins - 1, (int)((key_to_float(order_key(v)) - fmin) * scale)); };
+#pragma unroll
+        for (int u = 0; u < kTopRegs; ++u)
+          if (u < n) atomicAdd(&bins[bin_of(e[u])], 1u);
+        __syncthreads();
+        uint32_t part = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part += bins[kTopBins - 1 - 8 * tid - i];
+        uint32_t tot;
+        const uint32_t exc = block_excl_scan(part, tmp, &tot);
+        if (exc < (uint32_t)kk && exc + part >= (uint32_t)kk) {
+          uint32_t run = exc;
+          for (int i = 0; i < 8; ++i) {
+            const int bb = kTopBins - 1 - 8 * tid - i;
+            if (run + bins[bb] >= (uint32_t)kk) {
+              s_b = (uint32_t)bb;
+              s_above = run;
+              break;
+            }
+            run += bins[bb];
+          }
+        }
+        __syncthreads();
+        const int bstar = (int)s_b;
+#pragma unroll
+        for (int u = 0; u < kTopRegs; ++u)
+          if (u < n && bin_of(e[u]) == bstar) {
+            const uint32_t slot = atomicAdd(&s_m, 1u);
+            if (slot < kRankMax) {
+              s_list_key[slot] = order_key(e[u]);
+              s_list_pos[slot] = (uint32_t)(i0 + u);
+            }
+          }
+        __syncthreads();
+        const uint32_t m = s_m;
+        if (m <= kRankMax) {
+          const uint32_t need = (uint32_t)kk - s_above;  // 1 <= need <= m
+          for (uint32_t x = tid; x < m; x += blockDim.x) {
+            const uint32_t ki = s_list_key[x], pi = s_list_pos[x];
+            uint32_t rank = 0;
+            for (uint32_t y = 0; y < m; ++y) {
+              const uint32_t kj = s_list_key[y], pj = s_list_pos[y];
+              rank += (kj > ki || (kj == ki && pj < pi)) ? 1u : 0u;
+            }
+            if (rank == need - 1) {
+              s_kkey = ki;
+              s_kpos = pi;
+            }
+          }
+          __syncthreads();
+          kstar = s_kkey;
+          pstar = s_kpos;
+          resolved = true;
+        }
+      }
+      if (!resolved) {
+        uint32_t prefix = 0, mask = 0, remaining = (uint32_t)kk;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+          for (int i = tid; i < 256; i += blockDim.x) bins[i] = 0;
+          __syncthreads();
+#pragma unroll
+          for (int u = 0; u < kTopRegs; ++u) {
+            const uint32_t key = order_key(e[u]);
+            if (u < n && (key & mask) == prefix) atomicAdd(&bins[(key >> shift) & 255u], 1u);
+          }
+          __syncthreads();
+          if (warp == 0) {
+            uint32_t part = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part += bins[255 - 8 * lane - i];
+            const uint32_t inc = warp_incl_scan(part, lane);
+            const uint32_t exc = inc - part;
+            if (exc < remaining && inc >= remaining) {
+              uint32_t run = exc;
+              for (int i = 0; i < 8; ++i) {
+                const int dg = 255 - 8 * lane - i;
+                if (run + bins[dg] >= remaining) {
+                  s_b = (uint32_t)dg;
+                  s_above = run;
+                  break;
+                }
+                run += bins[dg];
+              }
+            }
+          }
+          __syncthreads();
+          prefix |= s_b << shift;
+          mask |= 255u << shift;
+          remaining -= s_above;
+          __syncthreads();
+        }
+        uint32_t n_eq = 0;
+#pragma unroll
+        for (int u = 0; u < kTopRegs; ++u) n_eq += (u < n && order_key(e[u]) == prefix) ? 1u : 0u;
+        uint32_t tot;
+        const uint32_t before = block_excl_scan(n_eq, tmp, &tot);
+        if (before < remaining && before + n_eq >= remaining) {
+          uint32_t seen = before;
+#pragma unroll
+          for (int u = 0; u < kTopRegs; ++u)
+            if (u < n && order_key(e[u]) == prefix && ++seen == remaining) s_kpos = i0 + u;
+        }
+        __syncthreads();
+        kstar = prefix;
+        pstar = s_kpos;
+      }
+    }
+    // ordered compaction: keep (key, position) at least as good as (kstar, pstar)
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kTopRegs; ++u) {
+      const uint32_t key = order_key(e[u]);
+      cnt += (u < n && (kk >= C || key > kstar || (key == kstar && i0 + u <= pstar))) ? 1u : 0u;
+    }
+    uint32_t tot;
+    uint32_t opos = block_excl_scan(cnt, tmp, &tot);
+#pragma unroll
+    for (int u = 0; u < kTopRegs; ++u) {
+      const uint32_t key = order_key(e[u]);
+      if (u < n && (kk >= C || key > kstar || (key == kstar && i0 + u <= pstar))) {
+        oi[opos] = ix[u];
+        if (os) os[opos] = e[u];
+        ++opos;
+      }
     }
   }
   for (int64_t i = kk + tid; i < a.k; i += blockDim.x) {
     oi[i] = -1;
     if (os) os[i] = -INFINITY;
   }
-  if (tid == 0) {
-    a.minmax[2 * sq] = 0xffffffffu;
-    a.minmax[2 * sq + 1] = 0u;
-    a.counter[sq] = 0;
+}
+
+__global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
+  __shared__ float tq[kDim * 16];
+  __shared__ uint32_t tmp[33];
+  __shared__ int s_last;
+  const int blk = blockIdx.x, sq = blockIdx.y;
+  const int seq = sq / a.hq, qh = sq - seq * a.hq, kvh = qh / a.g;
+  const int64_t sh = (int64_t)seq * (a.hq / a.g) + kvh;
+  const int tid = threadIdx.x;
+  const int64_t r0 = (int64_t)blk * kRerankPer * kRerankThreads;
+
+  // loads in flight together: q~ for the product table, candidate positions
+  const float qv = __ldcg(a.qt + (int64_t)sq * kDim + (tid >> 1));
+  const float qn = __ldcg(a.qnorm + sq);
+  int32_t pos[kRerankPer];
+#pragma unroll
+  for (int p = 0; p < kRerankPer; ++p) {
+    const int64_t r = r0 + p * kRerankThreads + tid;
+    pos[p] = r < a.C ? __ldcg(a.cand_idx + (int64_t)sq * a.cmax + r) : -1;
   }
+  {
+    const int coord = tid >> 1, nb0 = (tid & 1) * 8;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const int nib = nb0 + n;
+      const float l = a.rp.lev[nib & 7];
+      tq[coord * 16 + nib] = __fmul_rn((nib & 8) ? -l : l, qv);
+    }
+  }
+  // the candidates' 128-byte records
+  const uint8_t* rec = a.t.rec + sh * a.t.rcap * kRecBytes;
+  uint4 x[kRerankPer][8];
+#pragma unroll
+  for (int p = 0; p < kRerankPer; ++p) {
+    const uint4* rp4 = reinterpret_cast<const uint4*>(rec + (int64_t)max(0, pos[p] - a.sink) * kRecBytes);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[p][i] = pos[p] >= 0 ? __ldg(rp4 + i) : make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  float* cest = a.cand_est + (int64_t)sq * a.cmax;
+#pragma unroll
+  for (int p = 0; p < kRerankPer; ++p) {
+    const int64_t r = r0 + p * kRerankThreads + tid;
+    if (pos[p] >= 0) cest[r] = rerank_record(x[p], tq, qn);
+  }
+
+  // the last block of the query head takes the top-k
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&a.counter[sq], 1u) == (uint32_t)(a.nblk - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  topk_block(a, sq, tq, tmp);
+  if (tid == 0) a.counter[sq] = 0;
 }
 
 __global__ void k_fill_empty(int32_t* idx, float* score, int64_t n) {
@@ -699,10 +786,7 @@ cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const A
   v.rho = a.rho;
   v.flat = a.flat;
   v.nbins = a.nbins;
-  v.nch = a.nchunk_active;
-  v.plan_stride = a.plan_stride;
   v.N = a.N;
-  v.C = a.C;
   v.q = q;
   v.qdtype = dtype;
   v.qt = a.qt;
@@ -710,8 +794,6 @@ cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const A
   v.hot = a.hot;
   v.votes = a.votes;
   v.hist = a.hist;
-  v.plan = a.plan;
-  v.counter = a.counter_vote;
   v.k_new = ap ? ap->k : nullptr;
   v.v_new = ap ? ap->v : nullptr;
   v.kvdtype = ap ? ap->dtype : 0;
@@ -729,29 +811,42 @@ cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const A
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(const RetrieveArgs& a, cudaStream_t st) {
-  SelectArgs s;
-  s.t = a.t;
-  s.rp = a.rp;
-  s.s = a.s;
-  s.nch = a.nchunk_active;
-  s.plan_stride = a.plan_stride;
-  s.N = a.N;
-  s.C = a.C;
-  s.k = a.k;
-  s.k_eff = a.k_eff;
-  s.cmax = a.cmax;
-  s.qt = a.qt;
-  s.qnorm = a.qnorm;
-  s.votes = a.votes;
-  s.plan = a.plan;
-  s.cand_idx = a.cand_idx;
-  s.cand_est = a.cand_est;
-  s.minmax = a.minmax;
-  s.counter = a.counter_select;
-  s.out_idx = a.topk_idx;
-  s.out_score = a.topk_score;
-  k_select<<<dim3(a.nchunk_active, a.s.batch * a.s.hq), kSelThreads, 0, st>>>(s);
+cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st) {
+  CompactArgs c;
+  c.nbins = a.nbins;
+  c.nch = a.nchunk_active;
+  c.sink = a.s.sink;
+  c.nchunk = a.t.nchunk;
+  c.N = a.N;
+  c.C = a.C;
+  c.cmax = a.cmax;
+  c.votes = a.votes;
+  c.hist = a.hist;
+  c.cand_idx = a.cand_idx;
+  k_compact<<<dim3(a.nchunk_active, a.s.batch * a.s.hq), kCompactThreads, 0, st>>>(c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st) {
+  RerankArgs r;
+  r.t = a.t;
+  r.rp = a.rp;
+  r.hq = a.s.hq;
+  r.g = a.s.g;
+  r.sink = a.s.sink;
+  r.nblk = (int)((a.C + kRerankPer * kRerankThreads - 1) / (kRerankPer * kRerankThreads));
+  r.C = a.C;
+  r.k = a.k;
+  r.k_eff = a.k_eff;
+  r.cmax = a.cmax;
+  r.qt = a.qt;
+  r.qnorm = a.qnorm;
+  r.cand_idx = a.cand_idx;
+  r.cand_est = a.cand_est;
+  r.counter = a.counter_select;
+  r.out_idx = a.topk_idx;
+  r.out_score = a.topk_score;
+  k_rerank<<<dim3(r.nblk, a.s.batch * a.s.hq), kRerankThreads, 0, st>>>(r);
   return cudaGetLastError();
 }
 

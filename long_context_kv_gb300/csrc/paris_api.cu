@@ -40,10 +40,7 @@ struct paris_ctx {
   float* cand_est;
   float* part;
   uint32_t* status;
-  int32_t* plan;
-  int plan_stride;
-  uint32_t* counters;  // [3][batch*Hq]: vote, select, attend
-  uint32_t* minmax;    // [batch*Hq][2]
+  uint32_t* counters;  // [2][batch*Hq]: rerank blocks, attention splits finished
   std::string err;
   // accounting
   int64_t launches[PARIS_KERNEL_COUNT];
@@ -149,8 +146,8 @@ void lloyd_max_levels(int m, double lev[8], double thr[7]) {
 
 void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
-                 c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status, c->plan,
-                 c->counters, c->minmax};
+                 c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status,
+                 c->counters};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_store) {
@@ -205,12 +202,7 @@ RetrieveArgs retrieve_args(paris_ctx* c, int32_t* topk_idx, float* topk_score) {
   a.cand_idx = c->cand_idx;
   a.cand_est = c->cand_est;
   a.cmax = c->cmax;
-  a.plan = c->plan;
-  a.plan_stride = c->plan_stride;
-  const int64_t bq = (int64_t)c->s.batch * c->s.hq;
-  a.counter_vote = c->counters;
-  a.counter_select = c->counters + bq;
-  a.minmax = c->minmax;
+  a.counter_select = c->counters;
   a.topk_idx = topk_idx;
   a.topk_score = topk_score;
   return a;
@@ -229,7 +221,7 @@ AttendArgs attend_args(paris_ctx* c, const int32_t* topk_idx, void* out_bf16) {
   a.part = c->part;
   a.nsplit_max = c->nsplit_max;
   a.status = c->status;
-  a.counter = c->counters + 2 * (int64_t)c->s.batch * c->s.hq;
+  a.counter = c->counters + (int64_t)c->s.batch * c->s.hq;
   a.out = static_cast<__nv_bfloat16*>(out_bf16);
   return a;
 }
@@ -277,7 +269,8 @@ paris_status retrieve_launch(paris_ctx* c, const void* q, paris_dtype dtype, int
   }
   const RetrieveArgs a = retrieve_args(c, topk_idx, topk_score);
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_VOTE, s, [&] { return launch_vote(q, dtype, a, fuse, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_SELECT, s, [&] { return launch_select(a, s); }));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_COMPACT, s, [&] { return launch_compact(a, s); }));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_RERANK, s, [&] { return launch_rerank(a, s); }));
   *k_eff = a.k_eff;
   return PARIS_OK;
 }
@@ -322,7 +315,6 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
     delete c;
     return fail(nullptr, PARIS_EINVAL, "max_ctx - sink must be at most %d tokens", kMaxChunks * kChunk);
   }
-  c->plan_stride = 1 + 2 * c->nchunk;
   c->cmax = std::max<int64_t>(1, candidate_count(c->rcap, f.cand_bp, f.topk));
   c->nsplit_max = (int)((f.sink + f.local + f.update_buf + f.topk + kAttnSplit - 1) / kAttnSplit) + 1;
   std::memset(&c->sm, 0, sizeof c->sm);
@@ -381,19 +373,9 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   TRY(dalloc(c, &c->cand_est, (size_t)bq * c->cmax * sizeof(float), "candidate estimates"));
   TRY(dalloc(c, &c->part, (size_t)bq * c->nsplit_max * kPartStride * sizeof(float), "attention partials"));
   TRY(dalloc(c, &c->status, sizeof(uint32_t), "status word"));
-  TRY(dalloc(c, &c->plan, (size_t)bq * c->plan_stride * sizeof(int32_t), "candidate plan"));
-  TRY(dalloc(c, &c->counters, (size_t)3 * bq * sizeof(uint32_t), "tile counters"));
-  TRY(dalloc(c, &c->minmax, (size_t)2 * bq * sizeof(uint32_t), "estimate range"));
+  TRY(dalloc(c, &c->counters, (size_t)2 * bq * sizeof(uint32_t), "block counters"));
   cudaError_t e = cudaMemset(c->status, 0, sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)3 * bq * sizeof(uint32_t));
-  if (e == cudaSuccess) {
-    std::vector<uint32_t> mm((size_t)2 * bq);
-    for (size_t i = 0; i < mm.size(); i += 2) {
-      mm[i] = 0xffffffffu;
-      mm[i + 1] = 0u;
-    }
-    e = cudaMemcpy(c->minmax, mm.data(), mm.size() * sizeof(uint32_t), cudaMemcpyHostToDevice);
-  }
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)2 * bq * sizeof(uint32_t));
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "initialising the context"));
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "cudaDeviceSynchronize"));

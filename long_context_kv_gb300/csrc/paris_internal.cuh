@@ -90,11 +90,7 @@ struct RetrieveArgs {
   int32_t* cand_idx;  // [batch*Hq][cmax]
   float* cand_est;
   int64_t cmax;
-  int32_t* plan;      // [batch*Hq][plan_stride]: T, then (candidates before, T-keys allowed) per chunk
-  int plan_stride;
-  uint32_t* counter_vote;    // [batch*Hq] tiles finished, reset by the last one
-  uint32_t* counter_select;  // [batch*Hq]
-  uint32_t* minmax;          // [batch*Hq][2] order keys of the smallest / largest estimate
+  uint32_t* counter_select;  // [batch*Hq] rerank blocks finished, reset by the last one
   // outputs
   int32_t* topk_idx;  // [batch*Hq][k]
   float* topk_score;  // may be null
@@ -112,7 +108,8 @@ struct AppendFuse {
 
 size_t vote_smem_bytes(int rho);
 cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st);
-cudaError_t launch_select(const RetrieveArgs& a, cudaStream_t st);
+cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st);
+cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st);
 cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_t st);
 
 // ---- sparse attention ---------------------------------------------------
