@@ -179,11 +179,14 @@ paris_status paris_check_device(paris_ctx* ctx);
  *  PARIS_DUMP_QNORM    seq, q head:         float  [1] ||q||
  *  PARIS_DUMP_HOT      seq, q head:         uint32 [B][rho] centroid id | weight << 16
  *  PARIS_DUMP_LEVELS   (seq, head ignored): float  [15] 8 levels, 7 thresholds
- *  PARIS_DUMP_KV       seq, KV head:        uint16 [2][T][d] bf16 K then V by position */
+ *  PARIS_DUMP_KV       seq, KV head:        uint16 [2][T][d] bf16 K then V by position
+ *  PARIS_DUMP_TRACE    (seq, head ignored): uint64 [64] phase timestamps (ns, GPU
+ *                      global timer) of the last kernels, recorded only when the
+ *                      environment had PARIS_TRACE=1 at paris_create */
 enum {
   PARIS_DUMP_IDS = 0, PARIS_DUMP_CODES = 1, PARIS_DUMP_W = 2, PARIS_DUMP_VOTES = 3,
   PARIS_DUMP_CANDS = 4, PARIS_DUMP_CAND_EST = 5, PARIS_DUMP_QT = 6, PARIS_DUMP_QNORM = 7,
-  PARIS_DUMP_HOT = 8, PARIS_DUMP_LEVELS = 9, PARIS_DUMP_KV = 10
+  PARIS_DUMP_HOT = 8, PARIS_DUMP_LEVELS = 9, PARIS_DUMP_KV = 10, PARIS_DUMP_TRACE = 11
 };
 paris_status paris_debug_dump(paris_ctx* ctx, int what, int seq, int head, void* dst, size_t bytes);
 

@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t R = nwin + a.k_eff;
   const int ring = a.s.local + a.s.ubuf;
+  uint64_t* tr = (split == 0 && sq == 0) ? a.trace : nullptr;
+  trace_mark(tr, kTrAttend0);
 
   // row `tid` of the split: find it and copy its K and V rows
   const int64_t r = (int64_t)split * kAttnSplit + tid;
@@ -86,6 +88,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   qf[tid] = load1(q, dtype, (int64_t)sq * kDim + tid) * qscale;
   cp_async_wait_all();
   __syncthreads();
+  trace_mark(tr, kTrAttend1);
 
   // score of row tid (log2 domain)
   float s = -FLT_MAX;
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
     out[1] = L;
   }
 
+  trace_mark(tr, kTrAttend2);
   // the last split of the query head merges all splits
   __threadfence();
   __syncthreads();
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (sq == 0) trace_mark(a.trace, kTrAttend3);
   const int d = tid;
   float Mx = -FLT_MAX;
   for (int s0 = 0; s0 < nsplit; s0 += 8) {
@@ -172,6 +177,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   }
   a.out[(int64_t)sq * kDim + d] = __float2bfloat16_rn(Lt > 0.f ? ot / Lt : 0.f);
   if (tid == 0) a.counter[sq] = 0;
+  if (sq == 0) trace_mark(a.trace, kTrAttend4);
 }
 
 constexpr size_t kAttendSmem = (size_t)kAttnSplit * (kKStride + kDim) * sizeof(uint16_t);

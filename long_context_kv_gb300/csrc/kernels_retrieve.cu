@@ -64,6 +64,7 @@ struct VoteArgs {
   int64_t pos;
   KvStore kv;
   RsqParams rp;
+  uint64_t* trace;
 };
 
 __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
@@ -85,6 +86,8 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t base = (int64_t)c * kChunk;
   const int len = (int)min64(kChunk, a.N - base);
+  uint64_t* tr = (c == 0 && sq == 0) ? a.trace : nullptr;
+  trace_mark(tr, kTrVote0);
 
   // -- phase 0: clear, rotate the query, fused append ------------------------
   for (int i = tid; i < kChunk / 16; i += blockDim.x) reinterpret_cast<uint4*>(votes)[i] = make_uint4(0, 0, 0, 0);
@@ -103,6 +106,7 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   }
   __syncthreads();
 
+  trace_mark(tr, kTrVote1);
   // -- phase 1: norms (tile 0), centroid scores, hot centroids --------------
   if (c == 0 && tid == 32) {
     float acc = 0.f;
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   }
   __syncthreads();
 
+  trace_mark(tr, kTrVote2);
   // -- phase 2: walk the hot buckets' lists ---------------------------------
   const uint32_t* off = a.t.off + ((sh * a.t.nchunk + c) * kSub) * kOffStride;
   const uint16_t* ent = a.t.ent + ((sh * a.t.nchunk + c) * kSub) * (int64_t)kChunk;
@@ -226,6 +231,7 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   }
   __syncthreads();
 
+  trace_mark(tr, kTrVote3);
   // -- phase 3: histogram of the chunk's votes, votes out --------------------
   uint8_t* vout = a.votes + (int64_t)sq * a.t.nchunk * kChunk + base;
   uint32_t nz = 0;
@@ -246,6 +252,7 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   block_excl_scan(nz, tmp, &nz_total);
   uint32_t* hout = a.hist + ((int64_t)sq * a.t.nchunk + c) * kMaxBins;
   for (int s = tid; s < a.nbins; s += blockDim.x) hout[s] = s == 0 ? (uint32_t)len - nz_total : hist[s];
+  trace_mark(tr, kTrVote4);
 }
 
 // ===========================================================================
@@ -263,6 +270,7 @@ struct CompactArgs {
   const uint8_t* votes;
   const uint32_t* hist;
   int32_t* cand_idx;
+  uint64_t* trace;
 };
 
 __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
@@ -277,6 +285,8 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
   const int len = (int)min64(kChunk, a.N - base);
   const int nitems = a.nch * a.nbins;
   const uint32_t* h = a.hist + (int64_t)sq * a.nchunk * kMaxBins;
+  uint64_t* tr = (c == 0 && sq == 0) ? a.trace : nullptr;
+  trace_mark(tr, kTrCompact0);
 
   for (int i = tid; i < kMaxBins; i += blockDim.x) tot[i] = 0;
   // loads in flight together: histogram cells and this chunk's votes
@@ -296,6 +306,7 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
       reinterpret_cast<uint4*>(vsm)[tid + u * kCompactThreads] = x[u];
   }
   __syncthreads();
+  trace_mark(tr, kTrCompact1);
 #pragma unroll
   for (int u = 0; u < kHistRegs; ++u) {
     const int i = tid + u * blockDim.x;
@@ -393,6 +404,7 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
     }
     if (take) out[pos++] = (int32_t)(a.sink + base + k0 + i);
   }
+  trace_mark(tr, kTrCompact2);
 }
 
 // ===========================================================================
@@ -422,6 +434,7 @@ struct RerankArgs {
   uint32_t* counter;
   int32_t* out_idx;
   float* out_score;
+  uint64_t* trace;
 };
 
 __device__ __forceinline__ float rerank_record(const uint4 (&x)[8], const float* tq, float qn) {
@@ -456,6 +469,8 @@ __device__ void topk_block(const RerankArgs& a, int sq, float* bins_f, uint32_t*
   const int64_t per = (C + kRerankThreads - 1) / kRerankThreads;
   const int64_t i0 = min64(C, tid * per);
   const int n = (int)(min64(C, i0 + per) - i0);
+  uint64_t* tr = sq == 0 ? a.trace : nullptr;
+  trace_mark(tr, kTrTopk0);
 
   if (per > kTopRegs) {
     // large candidate sets: the same selection, reading the candidates from L2
@@ -534,6 +549,8 @@ __device__ void topk_block(const RerankArgs& a, int sq, float* bins_f, uint32_t*
       e[u] = u < n ? __ldcg(est + i0 + u) : 0.f;
       ix[u] = u < n ? __ldcg(cid + i0 + u) : 0;
     }
+    __syncthreads();
+    trace_mark(tr, kTrTopk1);
     uint32_t kstar = 0;
     int64_t pstar = C;
     if (kk < C) {
@@ -593,6 +610,7 @@ __device__ void topk_block(const RerankArgs& a, int sq, float* bins_f, uint32_t*
           }
         }
         __syncthreads();
+        trace_mark(tr, kTrTopk2);
         const int bstar = (int)s_b;
 #pragma unroll
         for (int u = 0; u < kTopRegs; ++u)
@@ -677,6 +695,7 @@ __device__ void topk_block(const RerankArgs& a, int sq, float* bins_f, uint32_t*
         pstar = s_kpos;
       }
     }
+    trace_mark(tr, kTrTopk3);
     // ordered compaction: keep (key, position) at least as good as (kstar, pstar)
     uint32_t cnt = 0;
 #pragma unroll
@@ -700,6 +719,7 @@ __device__ void topk_block(const RerankArgs& a, int sq, float* bins_f, uint32_t*
     oi[i] = -1;
     if (os) os[i] = -INFINITY;
   }
+  trace_mark(tr, kTrTopk4);
 }
 
 __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
@@ -711,6 +731,8 @@ __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
   const int64_t sh = (int64_t)seq * (a.hq / a.g) + kvh;
   const int tid = threadIdx.x;
   const int64_t r0 = (int64_t)blk * kRerankPer * kRerankThreads;
+  uint64_t* tr = (blk == 0 && sq == 0) ? a.trace : nullptr;
+  trace_mark(tr, kTrRerank0);
 
   // loads in flight together: q~ for the product table, candidate positions
   const float qv = __ldcg(a.qt + (int64_t)sq * kDim + (tid >> 1));
@@ -740,6 +762,7 @@ __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
     for (int i = 0; i < 8; ++i) x[p][i] = pos[p] >= 0 ? __ldg(rp4 + i) : make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
+  trace_mark(tr, kTrRerank1);
   float* cest = a.cand_est + (int64_t)sq * a.cmax;
 #pragma unroll
   for (int p = 0; p < kRerankPer; ++p) {
@@ -747,11 +770,13 @@ __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
     if (pos[p] >= 0) cest[r] = rerank_record(x[p], tq, qn);
   }
 
+  trace_mark(tr, kTrRerank2);
   // the last block of the query head takes the top-k
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(&a.counter[sq], 1u) == (uint32_t)(a.nblk - 1);
   __syncthreads();
+  trace_mark(tr, kTrRerank3);
   if (!s_last) return;
   __threadfence();
   topk_block(a, sq, tq, tmp);
@@ -800,6 +825,7 @@ cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const A
   v.pos = ap ? ap->pos : 0;
   v.kv = ap ? ap->kv : KvStore{};
   v.rp = a.rp;
+  v.trace = a.trace;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -823,6 +849,7 @@ cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st) {
   c.votes = a.votes;
   c.hist = a.hist;
   c.cand_idx = a.cand_idx;
+  c.trace = a.trace;
   k_compact<<<dim3(a.nchunk_active, a.s.batch * a.s.hq), kCompactThreads, 0, st>>>(c);
   return cudaGetLastError();
 }
@@ -846,6 +873,7 @@ cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st) {
   r.counter = a.counter_select;
   r.out_idx = a.topk_idx;
   r.out_score = a.topk_score;
+  r.trace = a.trace;
   k_rerank<<<dim3(r.nblk, a.s.batch * a.s.hq), kRerankThreads, 0, st>>>(r);
   return cudaGetLastError();
 }

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -41,6 +42,8 @@ struct paris_ctx {
   float* part;
   uint32_t* status;
   uint32_t* counters;  // [2][batch*Hq]: rerank blocks, attention splits finished
+  uint64_t* trace;     // kTraceSlots phase timestamps
+  bool tracing;        // PARIS_TRACE=1 in the environment at creation
   std::string err;
   // accounting
   int64_t launches[PARIS_KERNEL_COUNT];
@@ -147,7 +150,7 @@ void lloyd_max_levels(int m, double lev[8], double thr[7]) {
 void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
                  c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status,
-                 c->counters};
+                 c->counters, c->trace};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_store) {
@@ -203,6 +206,7 @@ RetrieveArgs retrieve_args(paris_ctx* c, int32_t* topk_idx, float* topk_score) {
   a.cand_est = c->cand_est;
   a.cmax = c->cmax;
   a.counter_select = c->counters;
+  a.trace = c->tracing ? c->trace : nullptr;
   a.topk_idx = topk_idx;
   a.topk_score = topk_score;
   return a;
@@ -222,6 +226,7 @@ AttendArgs attend_args(paris_ctx* c, const int32_t* topk_idx, void* out_bf16) {
   a.nsplit_max = c->nsplit_max;
   a.status = c->status;
   a.counter = c->counters + (int64_t)c->s.batch * c->s.hq;
+  a.trace = c->tracing ? c->trace : nullptr;
   a.out = static_cast<__nv_bfloat16*>(out_bf16);
   return a;
 }
@@ -374,8 +379,14 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   TRY(dalloc(c, &c->part, (size_t)bq * c->nsplit_max * kPartStride * sizeof(float), "attention partials"));
   TRY(dalloc(c, &c->status, sizeof(uint32_t), "status word"));
   TRY(dalloc(c, &c->counters, (size_t)2 * bq * sizeof(uint32_t), "block counters"));
+  TRY(dalloc(c, &c->trace, kTraceSlots * sizeof(uint64_t), "phase trace"));
+  {
+    const char* env = std::getenv("PARIS_TRACE");
+    c->tracing = env != nullptr && env[0] == '1';
+  }
   cudaError_t e = cudaMemset(c->status, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)2 * bq * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->trace, 0, kTraceSlots * sizeof(uint64_t));
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "initialising the context"));
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "cudaDeviceSynchronize"));
@@ -602,6 +613,10 @@ paris_status paris_debug_dump(paris_ctx* c, int what, int seq, int head, void* d
       }
       return PARIS_OK;
     }
+    case PARIS_DUMP_TRACE:
+      if ((st = need(kTraceSlots * sizeof(uint64_t))) != PARIS_OK) return st;
+      PARIS_CUDA(c, cudaMemcpy(dst, c->trace, kTraceSlots * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+      return PARIS_OK;
     default:
       return fail(c, PARIS_EINVAL, "unknown dump %d", what);
   }

@@ -11,6 +11,16 @@ constexpr unsigned kFull = 0xffffffffu;
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
+// Phase trace: thread 0 of a chosen block stores the global nanosecond timer
+// into trace[slot] (trace == nullptr: tracing off).
+__device__ __forceinline__ void trace_mark(uint64_t* trace, int slot) {
+  if (trace != nullptr && threadIdx.x == 0) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    trace[slot] = t;
+  }
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
 
 // Four consecutive elements [i, i+4) of a float32 (dtype 0) or bf16 (dtype 1)

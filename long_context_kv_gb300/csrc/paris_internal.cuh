@@ -91,6 +91,7 @@ struct RetrieveArgs {
   float* cand_est;
   int64_t cmax;
   uint32_t* counter_select;  // [batch*Hq] rerank blocks finished, reset by the last one
+  uint64_t* trace;           // phase timestamps (nullptr: off)
   // outputs
   int32_t* topk_idx;  // [batch*Hq][k]
   float* topk_score;  // may be null
@@ -123,6 +124,7 @@ struct AttendArgs {
   int nsplit_max;
   uint32_t* status;
   uint32_t* counter;          // [batch*Hq] splits finished, reset by the last one
+  uint64_t* trace;            // phase timestamps (nullptr: off)
   __nv_bfloat16* out;
 };
 int attend_splits(const AttendArgs& a);
@@ -130,5 +132,16 @@ cudaError_t launch_attend(const void* q, int dtype, const AttendArgs& a, cudaStr
 
 // Status word bits.
 constexpr uint32_t kStatusBadIndex = 1u;
+
+// Phase-trace slots (block (0, 0) of each kernel, and the reducing block of
+// query head 0).
+constexpr int kTraceSlots = 64;
+enum TraceSlot {
+  kTrVote0 = 0, kTrVote1, kTrVote2, kTrVote3, kTrVote4,
+  kTrCompact0 = 8, kTrCompact1, kTrCompact2,
+  kTrRerank0 = 16, kTrRerank1, kTrRerank2, kTrRerank3,
+  kTrTopk0 = 20, kTrTopk1, kTrTopk2, kTrTopk3, kTrTopk4, kTrTopk5,
+  kTrAttend0 = 32, kTrAttend1, kTrAttend2, kTrAttend3, kTrAttend4
+};
 
 }  // namespace paris

@@ -19,7 +19,7 @@ PARIS_OK, PARIS_EINVAL, PARIS_ENOMEM, PARIS_ECUDA, PARIS_ESTATE, PARIS_ECAPACITY
 PARIS_F32, PARIS_BF16 = 0, 1
 PARIS_VOTE_RANK, PARIS_VOTE_FLAT = 0, 1
 (DUMP_IDS, DUMP_CODES, DUMP_W, DUMP_VOTES, DUMP_CANDS, DUMP_CAND_EST, DUMP_QT, DUMP_QNORM, DUMP_HOT,
- DUMP_LEVELS, DUMP_KV) = range(11)
+ DUMP_LEVELS, DUMP_KV, DUMP_TRACE) = range(12)
 
 # Every function the header declares, with its ctypes signature.
 _SIGNATURES = {
@@ -218,6 +218,7 @@ class Context:
             DUMP_VOTES: ((N,), np.uint8), DUMP_CANDS: ((C,), np.int32), DUMP_CAND_EST: ((C,), np.float32),
             DUMP_QT: ((d,), np.float32), DUMP_QNORM: ((1,), np.float32), DUMP_HOT: ((B, rho), np.uint32),
             DUMP_LEVELS: ((15,), np.float32), DUMP_KV: ((2, T, d), np.uint16),
+            DUMP_TRACE: ((64,), np.uint64),
         }
         shape, dt = shapes[what]
         out = np.zeros(shape, dtype=dt)
