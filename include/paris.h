@@ -148,6 +148,25 @@ paris_status paris_retrieve(paris_ctx* ctx, const void* q, paris_dtype dtype, in
 paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtype,
                                  const int32_t* topk_idx, void* out_bf16, void* stream);
 
+/* The same sparse attention as paris_sparse_attend (same arguments, same
+ * result), for callers that must not allocate device memory: code running
+ * while another component owns the device allocator, or a serving loop whose
+ * device memory budget is fixed up front.  Its per-call scratch (the split
+ * partials and merge counters) lives in one fixed area compiled into the
+ * library (about 545 KB, held by every GPU that loads the library until the
+ * process exits) instead of in the context, and the call allocates nothing.
+ * The pages have no counterpart; this is a property of this library.
+ * Limit: batch x n_q_heads x splits <= 1024, with splits =
+ * ceil((tokens in Sink, Local and Update Buffer + k_eff) / 128), and
+ * batch x n_q_heads <= 1024; larger calls return PARIS_EINVAL.  The first call
+ * on a device looks up the area's device address once (cudaGetSymbolAddress
+ * with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one area, which keeps the last call's
+ * contents: calls that may overlap on the GPU (different streams, or
+ * different host threads) race and must be serialised by the caller.      */
+paris_status paris_sparse_attend_noalloc(paris_ctx* ctx, const void* q, paris_dtype dtype,
+                                         const int32_t* topk_idx, void* out_bf16, void* stream);
+
 /* One decode step: exactly paris_append_decode(k, v), then
  * paris_retrieve(q, ...), then paris_sparse_attend(q, topk_idx, out), with the
  * same arguments and results, in four kernels instead of five: the append

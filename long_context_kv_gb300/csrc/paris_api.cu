@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -666,6 +667,74 @@ paris_status paris_profile_end(paris_ctx* c, double* total_ms, int64_t* launches
     if (launches) launches[i] = n[i];
   }
   if (first != cudaSuccess) return cuda_fail(c, first, "profile events");
+  return PARIS_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Sparse attention without per-call scratch of the context
+// ---------------------------------------------------------------------------
+namespace {
+
+// Scratch of paris_sparse_attend_noalloc: one float row of kPartStride per
+// (sequence, query head, split) for the split partials, then one counter per
+// (sequence, query head) for the merge.  Compiled into the library, so every
+// GPU that loads it holds these ~545 KB until the process exits.
+constexpr int kNoAllocPartRows = 1024;
+constexpr int kNoAllocHeads = 1024;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocPartRows * kPartStride + kNoAllocHeads];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+paris_status noalloc_scratch(paris_ctx* c, float** out) {
+  int dev = 0;
+  PARIS_CUDA(c, cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(c, PARIS_EINVAL, "device %d not supported", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetSymbolAddress(attention scratch)");
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return PARIS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+paris_status paris_sparse_attend_noalloc(paris_ctx* c, const void* q, paris_dtype dtype, const int32_t* topk_idx,
+                                         void* out_bf16, void* stream) {
+  if (!c) return fail(nullptr, PARIS_EINVAL, "ctx is NULL");
+  paris_status st = check_dtype(c, dtype);
+  if (st != PARIS_OK) return st;
+  if (!q || !out_bf16 || (!topk_idx && c->N > 0)) return fail(c, PARIS_EINVAL, "q, topk_idx and out must not be NULL");
+  AttendArgs a = attend_args(c, topk_idx, out_bf16);
+  const int nsplit = attend_splits(a);
+  const int64_t bq = (int64_t)c->s.batch * c->s.hq;
+  if (bq * nsplit > kNoAllocPartRows || bq > kNoAllocHeads)
+    return fail(c, PARIS_EINVAL,
+                "paris_sparse_attend_noalloc: batch x query heads x splits = %lld x %d exceeds its fixed scratch of "
+                "%d rows (splits = ceil((sink + local + buffer + k) / %d))",
+                (long long)bq, nsplit, kNoAllocPartRows, kAttnSplit);
+  float* scratch = nullptr;
+  st = noalloc_scratch(c, &scratch);
+  if (st != PARIS_OK) return st;
+  a.part = scratch;
+  a.nsplit_max = nsplit;
+  a.counter = reinterpret_cast<uint32_t*>(scratch + (size_t)kNoAllocPartRows * kPartStride);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the merge counters must start at zero (the partial rows are always written before they are read)
+  PARIS_CUDA(c, cudaMemsetAsync(a.counter, 0, (size_t)bq * sizeof(uint32_t), s));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTEND, s, [&] { return launch_attend(q, dtype, a, s); }));
   return PARIS_OK;
 }
 

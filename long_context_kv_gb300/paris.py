@@ -39,6 +39,8 @@ _SIGNATURES = {
                                         ctypes.c_void_p, ctypes.c_size_t]),
     "paris_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
     "paris_rsq_levels": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "paris_sparse_attend_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "paris_decode_step": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p]),
@@ -178,6 +180,11 @@ class Context:
     def paris_sparse_attend(self, q, topk_idx, out, stream=None):
         _check(load().paris_sparse_attend(self._h, _ptr(q), _dtype_code(q), _ptr(topk_idx), _ptr(out),
                                           _stream(stream)), self._h)
+
+    def paris_sparse_attend_noalloc(self, q, topk_idx, out, stream=None):
+        """paris_sparse_attend with its scratch in the library's fixed area (no allocation)."""
+        _check(load().paris_sparse_attend_noalloc(self._h, _ptr(q), _dtype_code(q), _ptr(topk_idx), _ptr(out),
+                                                  _stream(stream)), self._h)
 
     def paris_decode_step(self, k, v, q, topk_idx, topk_score, out, stream=None) -> int:
         k_eff = ctypes.c_int64()
