@@ -280,7 +280,7 @@ def run_ours(args, rank, world):
             a[1] += n
     del g_prof
     kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
-    us_retrieve = sum(1e3 * prof[k][0] for k in ("vote", "compact", "rerank", "fill")) / args.steps
+    us_retrieve = sum(1e3 * prof[k][0] for k in ("vote", "compact", "rerank", "topk", "fill")) / args.steps
     us_attend = 1e3 * prof["attend"][0] / args.steps
     us_append = sum(1e3 * prof[k][0] for k in ("append", "build_index")) / args.steps
 
@@ -293,7 +293,9 @@ def run_ours(args, rank, world):
         # votes read back (1 B per key and query head), candidate records
         # (64 B codes + 64 B w) gathered, candidate index + estimate written,
         # top-k index + estimate written
-        "rerank": b * hq * (C * (4 + 128 + 4) + keff * 8),
+        "rerank": b * hq * C * (4 + 128 + 4),
+        # estimates and positions read, top-k positions and estimates written
+        "topk": b * hq * (C * 8 + keff * 8),
         # votes read (1 B per key and query head), candidate positions written
         "compact": b * hq * (int(Nmean) + C * 4),
         # retrieved K and V rows, plus the window rows once per KV head

@@ -169,7 +169,7 @@ paris_status paris_sparse_attend_noalloc(paris_ctx* ctx, const void* q, paris_dt
 
 /* One decode step: exactly paris_append_decode(k, v), then
  * paris_retrieve(q, ...), then paris_sparse_attend(q, topk_idx, out), with the
- * same arguments and results, in four kernels instead of five: the append
+ * same arguments and results, in five kernels instead of six: the append
  * rides in the vote kernel unless it fills the Update Buffer (then the flush
  * and index rebuild run first).  k, v: device, kv_dtype, [batch][Hkv][d];
  * q: device, q_dtype, [batch][Hq][d]; outputs as in the two calls.          */
@@ -222,10 +222,11 @@ typedef enum {
   PARIS_KERNEL_VOTE = 4,        /* query rotation, top-rho centroids, collision votes
                                    (and a fused append in decode steps)                 */
   PARIS_KERNEL_COMPACT = 5,     /* candidate selection (ordered compaction)              */
-  PARIS_KERNEL_RERANK = 6,      /* RSQ-IP estimates of the candidates, top-k             */
-  PARIS_KERNEL_ATTEND = 7,      /* sparse attention and the merge of its splits          */
-  PARIS_KERNEL_FILL = 8,        /* empty-result fill                                     */
-  PARIS_KERNEL_COUNT = 9
+  PARIS_KERNEL_RERANK = 6,      /* RSQ-IP estimates of the candidates                    */
+  PARIS_KERNEL_TOPK = 7,        /* top-k of the estimates                                */
+  PARIS_KERNEL_ATTEND = 8,      /* sparse attention and the merge of its splits          */
+  PARIS_KERNEL_FILL = 9,        /* empty-result fill                                     */
+  PARIS_KERNEL_COUNT = 10
 } paris_kernel;
 
 /* Cumulative kernel launches of this context since paris_create, per

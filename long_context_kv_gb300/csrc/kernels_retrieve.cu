@@ -21,13 +21,18 @@ namespace paris {
 namespace {
 
 constexpr int kVoteThreads = 256;
-constexpr int kCompactThreads = 256;
+constexpr int kCompactThreads = 512;
 constexpr int kRerankThreads = 256;
 constexpr int kRerankPer = 3;                      // candidates per thread, all loads in flight together
-constexpr int kTopBins = 8 * kRerankThreads;       // 2048
-constexpr int kRankMax = 512;                      // threshold-bin size resolved by pairwise ranks
-constexpr int kTopRegs = 32;                       // candidates per thread the top-k holds in registers
-constexpr int kHistRegs = 8;                       // histogram cells per thread held by k_compact
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkRegs = 8;                       // candidates per thread the top-k holds in registers
+constexpr int kHistRegs = 4;                       // histogram cells per thread held by k_compact
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // ===========================================================================
 // k_vote
@@ -67,12 +72,13 @@ struct VoteArgs {
   uint64_t* trace;
 };
 
-__global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
+__global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
   extern __shared__ __align__(16) uint32_t dyn[];
   const int nhot = kSub * a.rho;
   uint32_t* votes = dyn;                                                 // kChunk / 4 words
   float* sc = reinterpret_cast<float*>(votes + kChunk / 4);              // [kSub][kCentroids]
-  uint32_t* hbeg = reinterpret_cast<uint32_t*>(sc + kSub * kCentroids);  // nhot
+  uint32_t* offs = reinterpret_cast<uint32_t*>(sc + kSub * kCentroids);  // [kSub][kOffStride]
+  uint32_t* hbeg = offs + kSub * kOffStride;                             // nhot
   uint32_t* hpre = hbeg + nhot;                                          // nhot + 1
   uint32_t* hwt = hpre + nhot + 1;                                       // nhot
   __shared__ float qs[kDim], zs[kDim];
@@ -89,7 +95,10 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   uint64_t* tr = (c == 0 && sq == 0) ? a.trace : nullptr;
   trace_mark(tr, kTrVote0);
 
-  // -- phase 0: clear, rotate the query, fused append ------------------------
+  // -- phase 0: prefetch the chunk's bucket offsets, clear, rotate the query,
+  //    fused append --------------------------------------------------------
+  const uint32_t* off_g = a.t.off + ((sh * a.t.nchunk + c) * kSub) * kOffStride;
+  for (int i = tid; i < kSub * kOffStride / 4; i += blockDim.x) cp_async16(offs + 4 * i, off_g + 4 * i);
   for (int i = tid; i < kChunk / 16; i += blockDim.x) reinterpret_cast<uint4*>(votes)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < kMaxBins; i += blockDim.x) hist[i] = 0;
   if (warp == 0) {
@@ -108,18 +117,24 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
 
   trace_mark(tr, kTrVote1);
   // -- phase 1: norms (tile 0), centroid scores, hot centroids --------------
-  if (c == 0 && tid == 32) {
+  if (c == 0 && (tid == 32 || tid == 64)) {
+    // sequential sum of squares; the products do not depend on the sum, so
+    // they are formed ahead of the chain
+    const float* src = tid == 32 ? qs : zs;
     float acc = 0.f;
-    for (int j = 0; j < kDim; ++j) acc = __fadd_rn(acc, __fmul_rn(qs[j], qs[j]));
-    a.qnorm[sq] = __fsqrt_rn(acc);
-  }
-  if (c == 0 && tid == 64) {
-    float acc = 0.f;
-    for (int j = 0; j < kDim; ++j) acc = __fadd_rn(acc, __fmul_rn(zs[j], zs[j]));
-    s_zn = __fsqrt_rn(acc);
+#pragma unroll
+    for (int j0 = 0; j0 < kDim; j0 += 32) {
+      float sqv[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sqv[j] = __fmul_rn(src[j0 + j], src[j0 + j]);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc = __fadd_rn(acc, sqv[j]);
+    }
+    if (tid == 32) a.qnorm[sq] = __fsqrt_rn(acc);
+    else s_zn = __fsqrt_rn(acc);
   }
   for (int cid = tid; cid < kCentroids; cid += blockDim.x) {
-#pragma unroll 4
+#pragma unroll
     for (int b = 0; b < kSub; ++b) {
       float acc = 0.f;
 #pragma unroll
@@ -135,46 +150,49 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
     const float zn = s_zn;
     a.qt[(int64_t)sq * kDim + tid] = zn > 0.f ? __fdiv_rn(zs[tid], zn) : 0.f;
   }
-  for (int b = warp; b < kSub; b += kVoteThreads / 32) {
-    float v[8];
+  // top rho per subspace by (score desc, id asc): warp w takes subspaces w and
+  // w + 8 together; lane l holds ids l + 32 i as order keys (0 = taken)
+  {
+    constexpr int kW = kVoteThreads / 32;
+    uint32_t key[2][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = sc[b * kCentroids + lane + 32 * i];
-    uint32_t taken = 0;
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) key[h][i] = order_key(sc[(warp + kW * h) * kCentroids + lane + 32 * i]);
     for (int r = 0; r < a.rho; ++r) {
-      float best = -FLT_MAX;
-      int bid = 0x7fffffff;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int id = lane + 32 * i;
-        if (!((taken >> i) & 1u) && (v[i] > best || (v[i] == best && id < bid))) {
-          best = v[i];
-          bid = id;
-        }
-      }
+      for (int h = 0; h < 2; ++h) {
+        uint32_t bk = 0;
+        int bi = 0;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ob = __shfl_xor_sync(kFull, best, o);
-        const int oid = __shfl_xor_sync(kFull, bid, o);
-        if (ob > best || (ob == best && oid < bid)) {
-          best = ob;
-          bid = oid;
+        for (int i = 0; i < 8; ++i)
+          if (key[h][i] > bk) {  // strict: among equal keys the lowest id of the lane stays
+            bk = key[h][i];
+            bi = i;
+          }
+        const uint32_t wmax = __reduce_max_sync(kFull, bk);
+        const uint32_t bid = __reduce_min_sync(kFull, bk == wmax && bk != 0 ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+        if ((int)(bid & 31) == lane) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i == (int)(bid >> 5)) key[h][i] = 0;
         }
-      }
-      if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-      if (lane == 0) {
-        const uint32_t wgt = a.flat ? 1u : (uint32_t)(a.rho - r);
-        const int e = b * a.rho + r;
-        hbeg[e] = (uint32_t)bid;
-        hwt[e] = wgt;
-        if (c == 0) a.hot[(int64_t)sq * nhot + e] = (uint32_t)bid | (wgt << 16);
+        if (lane == 0) {
+          const int b = warp + kW * h;
+          const uint32_t wgt = a.flat ? 1u : (uint32_t)(a.rho - r);
+          const int e = b * a.rho + r;
+          hbeg[e] = bid;
+          hwt[e] = wgt;
+          if (c == 0) a.hot[(int64_t)sq * nhot + e] = bid | (wgt << 16);
+        }
       }
     }
   }
+  cp_async_wait_all();
   __syncthreads();
-
   trace_mark(tr, kTrVote2);
+
   // -- phase 2: walk the hot buckets' lists ---------------------------------
-  const uint32_t* off = a.t.off + ((sh * a.t.nchunk + c) * kSub) * kOffStride;
   const uint16_t* ent = a.t.ent + ((sh * a.t.nchunk + c) * kSub) * (int64_t)kChunk;
   {
     const int per = (nhot + blockDim.x - 1) / blockDim.x;  // <= 16
@@ -187,8 +205,8 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
       if (i < per && e < nhot) {
         const int b = e / a.rho;
         const uint32_t id = hbeg[e];
-        const uint32_t beg = __ldg(off + b * kOffStride + id);
-        const uint32_t end = __ldg(off + b * kOffStride + id + 1);
+        const uint32_t beg = offs[b * kOffStride + id];
+        const uint32_t end = offs[b * kOffStride + id + 1];
         lens[i] = end - beg;
         hbeg[e] = (uint32_t)b * kChunk + beg;
       }
@@ -206,16 +224,18 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   }
   __syncthreads();
   const uint32_t total = hpre[nhot];
-  // thread t takes 8 consecutive list entries: one search, then linear steps
-  for (uint32_t f0 = 8 * tid; f0 < total; f0 += 8 * blockDim.x) {
+  // thread t takes 16 consecutive list entries: one search, then linear steps;
+  // all 16 loads in flight together
+  constexpr int kWalk = 16;
+  for (uint32_t f0 = kWalk * tid; f0 < total; f0 += kWalk * blockDim.x) {
     int e = 0, hi = nhot - 1;  // last e with hpre[e] <= f0 (a non-empty list)
     while (e < hi) {
       const int mid = (e + hi + 1) >> 1;
       if (hpre[mid] <= f0) e = mid; else hi = mid - 1;
     }
-    uint32_t key[8], wt[8];
+    uint32_t key[kWalk], wt[kWalk];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < kWalk; ++u) {
       const uint32_t f = f0 + u;
       wt[u] = 0;
       key[u] = 0;
@@ -226,7 +246,7 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
       }
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
+    for (int u = 0; u < kWalk; ++u)
       if (wt[u]) atomicAdd(&votes[key[u] >> 2], wt[u] << ((key[u] & 3) * 8));
   }
   __syncthreads();
@@ -234,7 +254,7 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
   trace_mark(tr, kTrVote3);
   // -- phase 3: histogram of the chunk's votes, votes out --------------------
   uint8_t* vout = a.votes + (int64_t)sq * a.t.nchunk * kChunk + base;
-  uint32_t nz = 0;
+  uint32_t nz = 0, small = 0;
   for (int i = tid; i < kChunk / 16; i += blockDim.x) {
     const uint4 w4 = reinterpret_cast<const uint4*>(votes)[i];
     reinterpret_cast<uint4*>(vout)[i] = w4;
@@ -242,11 +262,17 @@ __global__ void __launch_bounds__(kVoteThreads) k_vote(VoteArgs a) {
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       const uint32_t v = (ws[k >> 2] >> (8 * (k & 3))) & 0xffu;
-      if (v && 16 * i + k < len) {
-        atomicAdd(&hist[v], 1u);
-        ++nz;
-      }
+      const bool in = v != 0 && 16 * i + k < len;
+      if (in && v <= 4) small += 1u << (8 * (v - 1));  // per-thread counts <= 64 fit a byte
+      else if (in) atomicAdd(&hist[v], 1u);
+      nz += in ? 1u : 0u;
     }
+  }
+  // the common small vote values: warp sums of the packed counters
+#pragma unroll
+  for (int v = 1; v <= 4; ++v) {
+    const uint32_t cnt = __reduce_add_sync(kFull, (small >> (8 * (v - 1))) & 0xffu);
+    if (lane == 0 && cnt) atomicAdd(&hist[v], cnt);
   }
   uint32_t nz_total;
   block_excl_scan(nz, tmp, &nz_total);
@@ -273,10 +299,30 @@ struct CompactArgs {
   uint64_t* trace;
 };
 
+// Sums of two values over the block (every thread gets both).  `red` holds
+// 2 * 32 words of shared memory.
+__device__ __forceinline__ void block_sum2(uint32_t& x, uint32_t& y, uint32_t* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  x = __reduce_add_sync(kFull, x);
+  y = __reduce_add_sync(kFull, y);
+  if (lane == 0) {
+    red[warp] = x;
+    red[32 + warp] = y;
+  }
+  __syncthreads();
+  x = 0;
+  y = 0;
+  for (int w = 0; w < nw; ++w) {
+    x += red[w];
+    y += red[32 + w];
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
-  __shared__ __align__(16) uint32_t vsm[kChunk / 4];
   __shared__ uint32_t tot[kMaxBins];
   __shared__ uint32_t tmp[33];
+  __shared__ uint32_t red[64];
   __shared__ int s_T;
   __shared__ int64_t s_quota;
   const int c = blockIdx.x, sq = blockIdx.y;
@@ -296,14 +342,16 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
     const int i = tid + u * blockDim.x;
     hv[u] = i < nitems ? __ldcg(h + (int64_t)(i / a.nbins) * kMaxBins + i % a.nbins) : 0u;
   }
+  constexpr int kPer = kChunk / kCompactThreads;  // 32 keys per thread
+  const int k0 = tid * kPer;
+  uint32_t vw[kPer / 4];
   {
-    const uint4* vin = reinterpret_cast<const uint4*>(a.votes + (int64_t)sq * a.nchunk * kChunk + base);
-    uint4 x[kChunk / 16 / kCompactThreads];
+    const uint4* vin = reinterpret_cast<const uint4*>(a.votes + (int64_t)sq * a.nchunk * kChunk + base + k0);
 #pragma unroll
-    for (int u = 0; u < kChunk / 16 / kCompactThreads; ++u) x[u] = __ldcg(vin + tid + u * kCompactThreads);
-#pragma unroll
-    for (int u = 0; u < kChunk / 16 / kCompactThreads; ++u)
-      reinterpret_cast<uint4*>(vsm)[tid + u * kCompactThreads] = x[u];
+    for (int i = 0; i < kPer / 16; ++i) {
+      const uint4 x = __ldcg(vin + i);
+      vw[4 * i] = x.x; vw[4 * i + 1] = x.y; vw[4 * i + 2] = x.z; vw[4 * i + 3] = x.w;
+    }
   }
   __syncthreads();
   trace_mark(tr, kTrCompact1);
@@ -345,42 +393,32 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
   const int T = s_T;
   const int64_t quota = s_quota;
   // keys above T / equal to T in the chunks before this one
-  uint32_t gt = 0, eq = 0;
+  uint32_t gt_before = 0, eq_before = 0;
 #pragma unroll
   for (int u = 0; u < kHistRegs; ++u) {
     const int i = tid + u * blockDim.x;
     if (i < nitems && i / a.nbins < c) {
       const int s = i % a.nbins;
-      gt += s > T ? hv[u] : 0u;
-      eq += s == T ? hv[u] : 0u;
+      gt_before += s > T ? hv[u] : 0u;
+      eq_before += s == T ? hv[u] : 0u;
     }
   }
   for (int i = tid + kHistRegs * blockDim.x; i < nitems; i += blockDim.x) {
     if (i / a.nbins < c) {
       const int s = i % a.nbins;
       const uint32_t x = __ldcg(h + (int64_t)(i / a.nbins) * kMaxBins + s);
-      gt += s > T ? x : 0u;
-      eq += s == T ? x : 0u;
+      gt_before += s > T ? x : 0u;
+      eq_before += s == T ? x : 0u;
     }
   }
-  uint32_t gt_before, eq_before;
-  block_excl_scan(gt, tmp, &gt_before);
-  block_excl_scan(eq, tmp, &eq_before);
+  block_sum2(gt_before, eq_before, red);
   const int64_t sel_before = gt_before + min64(eq_before, quota);
   const int64_t eq_allow = max64(0, quota - (int64_t)eq_before);
 
-  // ordered compaction: thread t owns keys [64t, 64t + 64) = words [16t, 16t + 16)
-  constexpr int kWords = kChunk / 4 / kCompactThreads;
-  const int k0 = tid * 4 * kWords;
-  uint32_t vw[kWords];
-#pragma unroll
-  for (int i = 0; i < kWords / 4; ++i) {
-    const uint4 x = reinterpret_cast<const uint4*>(vsm)[tid * (kWords / 4) + i];
-    vw[4 * i] = x.x; vw[4 * i + 1] = x.y; vw[4 * i + 2] = x.z; vw[4 * i + 3] = x.w;
-  }
+  // ordered compaction: thread t owns keys [32t, 32t + 32)
   uint32_t n_eq = 0, n_gt = 0;
 #pragma unroll
-  for (int i = 0; i < 4 * kWords; ++i) {
+  for (int i = 0; i < kPer; ++i) {
     const uint32_t v = (vw[i >> 2] >> (8 * (i & 3))) & 0xffu;
     const bool in = k0 + i < len;
     n_eq += (in && v == (uint32_t)T) ? 1u : 0u;
@@ -394,7 +432,7 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
   int32_t* out = a.cand_idx + (int64_t)sq * a.cmax + sel_before;
   uint32_t eq_seen = 0;
 #pragma unroll
-  for (int i = 0; i < 4 * kWords; ++i) {
+  for (int i = 0; i < kPer; ++i) {
     const uint32_t v = (vw[i >> 2] >> (8 * (i & 3))) & 0xffu;
     const bool in = k0 + i < len;
     bool take = in && v > (uint32_t)T;
@@ -417,11 +455,10 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
 // where v_{b,j} q~_{b,j} comes from a per-query table of the 16 possible
 // products of each coordinate (sign bit x 8 levels), each rounded once.
 // Top-k (last block of the query head): the k_eff-th best (estimate desc,
-// position asc) candidate is found from a 2048-bin histogram over the
-// estimates' range (bins are monotone in the estimate, so only the
-// threshold bin needs exact ranks) or, for a degenerate range, an 8-bit
-// radix select; every candidate at least as good is kept, listed in
-// ascending position order.
+// position asc) candidate is found by a search over the 32-bit order keys of
+// the estimates with block-wide counts (three probes per round), then the
+// lowest positions among keys equal to it; every candidate at least as good
+// is kept, listed in ascending position order.
 struct RerankArgs {
   Tables t;
   RsqParams rp;
@@ -453,279 +490,8 @@ __device__ __forceinline__ float rerank_record(const uint4 (&x)[8], const float*
   return __fmul_rn(qn, acc);
 }
 
-// Top-k of one query head's C candidates by the block (blockDim == kRerankThreads).
-__device__ void topk_block(const RerankArgs& a, int sq, float* bins_f, uint32_t* tmp) {
-  __shared__ uint32_t s_b, s_above, s_m, s_kkey;
-  __shared__ int64_t s_kpos;
-  __shared__ uint32_t s_list_key[kRankMax], s_list_pos[kRankMax];
-  __shared__ uint32_t s_min[kRerankThreads / 32], s_max[kRerankThreads / 32];
-  uint32_t* bins = reinterpret_cast<uint32_t*>(bins_f);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t C = a.C, kk = a.k_eff;
-  const float* est = a.cand_est + (int64_t)sq * a.cmax;
-  const int32_t* cid = a.cand_idx + (int64_t)sq * a.cmax;
-  int32_t* oi = a.out_idx + (int64_t)sq * a.k;
-  float* os = a.out_score ? a.out_score + (int64_t)sq * a.k : nullptr;
-  const int64_t per = (C + kRerankThreads - 1) / kRerankThreads;
-  const int64_t i0 = min64(C, tid * per);
-  const int n = (int)(min64(C, i0 + per) - i0);
-  uint64_t* tr = sq == 0 ? a.trace : nullptr;
-  trace_mark(tr, kTrTopk0);
-
-  if (per > kTopRegs) {
-    // large candidate sets: the same selection, reading the candidates from L2
-    // (radix select, then the remaining-th lowest position among ties)
-    uint32_t prefix = 0, mask = 0, remaining = (uint32_t)kk;
-    if (kk < C) {
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) bins[i] = 0;
-        __syncthreads();
-        for (int64_t i = tid; i < C; i += blockDim.x) {
-          const uint32_t key = order_key(__ldcg(est + i));
-          if ((key & mask) == prefix) atomicAdd(&bins[(key >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        if (warp == 0) {
-          uint32_t part = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) part += bins[255 - 8 * lane - i];
-          const uint32_t inc = warp_incl_scan(part, lane);
-          const uint32_t exc = inc - part;
-          if (exc < remaining && inc >= remaining) {
-            uint32_t run = exc;
-            for (int i = 0; i < 8; ++i) {
-              const int dg = 255 - 8 * lane - i;
-              if (run + bins[dg] >= remaining) {
-                s_b = (uint32_t)dg;
-                s_above = run;
-                break;
-              }
-              run += bins[dg];
-            }
-          }
-        }
-        __syncthreads();
-        prefix |= s_b << shift;
-        mask |= 255u << shift;
-        remaining -= s_above;
-        __syncthreads();
-      }
-    }
-    uint32_t n_eq = 0;
-    for (int64_t i = i0; i < i0 + n; ++i) n_eq += order_key(__ldcg(est + i)) == prefix ? 1u : 0u;
-    uint32_t tot;
-    const uint32_t before = block_excl_scan(n_eq, tmp, &tot);
-    if (kk < C && before < remaining && before + n_eq >= remaining) {
-      uint32_t seen = before;
-      for (int64_t i = i0; i < i0 + n; ++i)
-        if (order_key(__ldcg(est + i)) == prefix && ++seen == remaining) {
-          s_kpos = i;
-          break;
-        }
-    }
-    __syncthreads();
-    const int64_t pstar = kk < C ? s_kpos : C;
-    uint32_t cnt = 0;
-    for (int64_t i = i0; i < i0 + n; ++i) {
-      const uint32_t key = order_key(__ldcg(est + i));
-      cnt += (kk >= C || key > prefix || (key == prefix && i <= pstar)) ? 1u : 0u;
-    }
-    uint32_t opos = block_excl_scan(cnt, tmp, &tot);
-    for (int64_t i = i0; i < i0 + n; ++i) {
-      const float e = __ldcg(est + i);
-      const uint32_t key = order_key(e);
-      if (kk >= C || key > prefix || (key == prefix && i <= pstar)) {
-        oi[opos] = __ldcg(cid + i);
-        if (os) os[opos] = e;
-        ++opos;
-      }
-    }
-  } else {
-    // the thread's contiguous slice of candidates, all loads in flight together
-    float e[kTopRegs];
-    int32_t ix[kTopRegs];
-#pragma unroll
-    for (int u = 0; u < kTopRegs; ++u) {
-      e[u] = u < n ? __ldcg(est + i0 + u) : 0.f;
-      ix[u] = u < n ? __ldcg(cid + i0 + u) : 0;
-    }
-    __syncthreads();
-    trace_mark(tr, kTrTopk1);
-    uint32_t kstar = 0;
-    int64_t pstar = C;
-    if (kk < C) {
-      uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-      for (int u = 0; u < kTopRegs; ++u)
-        if (u < n) {
-          kmin = min(kmin, order_key(e[u]));
-          kmax = max(kmax, order_key(e[u]));
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        kmin = min(kmin, __shfl_xor_sync(kFull, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(kFull, kmax, o));
-      }
-      if (lane == 0) {
-        s_min[warp] = kmin;
-        s_max[warp] = kmax;
-      }
-      for (int i = tid; i < kTopBins; i += blockDim.x) bins[i] = 0;
-      if (tid == 0) s_m = 0;
-      __syncthreads();
-      kmin = s_min[0];
-      kmax = s_max[0];
-      for (int w = 1; w < kRerankThreads / 32; ++w) {
-        kmin = min(kmin, s_min[w]);
-        kmax = max(kmax, s_max[w]);
-      }
-      const float fmin = key_to_float(kmin), fmax = key_to_float(kmax);
-      const float range = fmax - fmin;
-      bool linear = kmax > kmin && range > 0.f && range <= FLT_MAX;
-      const float scale = linear ? (float)kTopBins / range : 0.f;
-      linear = linear && scale > 0.f && scale <= FLT_MAX;
-      bool resolved = false;
-      if (linear) {
-        // bins are a monotone function of the estimate (-0 counted as +0)
-        auto bin_of = [&](float v) { return min(kTopBins - 1, (int)((key_to_float(order_key(v)) - fmin) * scale)); };
-#pragma unroll
-        for (int u = 0; u < kTopRegs; ++u)
-          if (u < n) atomicAdd(&bins[bin_of(e[u])], 1u);
-        __syncthreads();
-        uint32_t part = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) part += bins[kTopBins - 1 - 8 * tid - i];
-        uint32_t tot;
-        const uint32_t exc = block_excl_scan(part, tmp, &tot);
-        if (exc < (uint32_t)kk && exc + part >= (uint32_t)kk) {
-          uint32_t run = exc;
-          for (int i = 0; i < 8; ++i) {
-            const int bb = kTopBins - 1 - 8 * tid - i;
-            if (run + bins[bb] >= (uint32_t)kk) {
-              s_b = (uint32_t)bb;
-              s_above = run;
-              break;
-            }
-            run += bins[bb];
-          }
-        }
-        __syncthreads();
-        trace_mark(tr, kTrTopk2);
-        const int bstar = (int)s_b;
-#pragma unroll
-        for (int u = 0; u < kTopRegs; ++u)
-          if (u < n && bin_of(e[u]) == bstar) {
-            const uint32_t slot = atomicAdd(&s_m, 1u);
-            if (slot < kRankMax) {
-              s_list_key[slot] = order_key(e[u]);
-              s_list_pos[slot] = (uint32_t)(i0 + u);
-            }
-          }
-        __syncthreads();
-        const uint32_t m = s_m;
-        if (m <= kRankMax) {
-          const uint32_t need = (uint32_t)kk - s_above;  // 1 <= need <= m
-          for (uint32_t x = tid; x < m; x += blockDim.x) {
-            const uint32_t ki = s_list_key[x], pi = s_list_pos[x];
-            uint32_t rank = 0;
-            for (uint32_t y = 0; y < m; ++y) {
-              const uint32_t kj = s_list_key[y], pj = s_list_pos[y];
-              rank += (kj > ki || (kj == ki && pj < pi)) ? 1u : 0u;
-            }
-            if (rank == need - 1) {
-              s_kkey = ki;
-              s_kpos = pi;
-            }
-          }
-          __syncthreads();
-          kstar = s_kkey;
-          pstar = s_kpos;
-          resolved = true;
-        }
-      }
-      if (!resolved) {
-        uint32_t prefix = 0, mask = 0, remaining = (uint32_t)kk;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-          for (int i = tid; i < 256; i += blockDim.x) bins[i] = 0;
-          __syncthreads();
-#pragma unroll
-          for (int u = 0; u < kTopRegs; ++u) {
-            const uint32_t key = order_key(e[u]);
-            if (u < n && (key & mask) == prefix) atomicAdd(&bins[(key >> shift) & 255u], 1u);
-          }
-          __syncthreads();
-          if (warp == 0) {
-            uint32_t part = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) part += bins[255 - 8 * lane - i];
-            const uint32_t inc = warp_incl_scan(part, lane);
-            const uint32_t exc = inc - part;
-            if (exc < remaining && inc >= remaining) {
-              uint32_t run = exc;
-              for (int i = 0; i < 8; ++i) {
-                const int dg = 255 - 8 * lane - i;
-                if (run + bins[dg] >= remaining) {
-                  s_b = (uint32_t)dg;
-                  s_above = run;
-                  break;
-                }
-                run += bins[dg];
-              }
-            }
-          }
-          __syncthreads();
-          prefix |= s_b << shift;
-          mask |= 255u << shift;
-          remaining -= s_above;
-          __syncthreads();
-        }
-        uint32_t n_eq = 0;
-#pragma unroll
-        for (int u = 0; u < kTopRegs; ++u) n_eq += (u < n && order_key(e[u]) == prefix) ? 1u : 0u;
-        uint32_t tot;
-        const uint32_t before = block_excl_scan(n_eq, tmp, &tot);
-        if (before < remaining && before + n_eq >= remaining) {
-          uint32_t seen = before;
-#pragma unroll
-          for (int u = 0; u < kTopRegs; ++u)
-            if (u < n && order_key(e[u]) == prefix && ++seen == remaining) s_kpos = i0 + u;
-        }
-        __syncthreads();
-        kstar = prefix;
-        pstar = s_kpos;
-      }
-    }
-    trace_mark(tr, kTrTopk3);
-    // ordered compaction: keep (key, position) at least as good as (kstar, pstar)
-    uint32_t cnt = 0;
-#pragma unroll
-    for (int u = 0; u < kTopRegs; ++u) {
-      const uint32_t key = order_key(e[u]);
-      cnt += (u < n && (kk >= C || key > kstar || (key == kstar && i0 + u <= pstar))) ? 1u : 0u;
-    }
-    uint32_t tot;
-    uint32_t opos = block_excl_scan(cnt, tmp, &tot);
-#pragma unroll
-    for (int u = 0; u < kTopRegs; ++u) {
-      const uint32_t key = order_key(e[u]);
-      if (u < n && (kk >= C || key > kstar || (key == kstar && i0 + u <= pstar))) {
-        oi[opos] = ix[u];
-        if (os) os[opos] = e[u];
-        ++opos;
-      }
-    }
-  }
-  for (int64_t i = kk + tid; i < a.k; i += blockDim.x) {
-    oi[i] = -1;
-    if (os) os[i] = -INFINITY;
-  }
-  trace_mark(tr, kTrTopk4);
-}
-
 __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
   __shared__ float tq[kDim * 16];
-  __shared__ uint32_t tmp[33];
-  __shared__ int s_last;
   const int blk = blockIdx.x, sq = blockIdx.y;
   const int seq = sq / a.hq, qh = sq - seq * a.hq, kvh = qh / a.g;
   const int64_t sh = (int64_t)seq * (a.hq / a.g) + kvh;
@@ -771,16 +537,164 @@ __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
   }
 
   trace_mark(tr, kTrRerank2);
-  // the last block of the query head takes the top-k
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&a.counter[sq], 1u) == (uint32_t)(a.nblk - 1);
-  __syncthreads();
-  trace_mark(tr, kTrRerank3);
-  if (!s_last) return;
-  __threadfence();
-  topk_block(a, sq, tq, tmp);
-  if (tid == 0) a.counter[sq] = 0;
+}
+
+// ===========================================================================
+// k_topk
+// ===========================================================================
+//
+// One block of 1024 threads per (sequence, query head).  The k_eff-th best
+// candidate by (estimate desc, position asc) is found by a radix select on
+// the 32-bit order keys of the estimates (8 bits per pass, counted in shared
+// memory), then the lowest positions among keys equal to it; every
+// candidate at least as good is kept, listed in ascending position order.
+// Thread t owns a contiguous slice of the candidates (in registers when the
+// slice has at most kTopkRegs of them).
+struct TopkArgs {
+  int64_t C, k, k_eff, cmax;
+  const int32_t* cand_idx;
+  const float* cand_est;
+  int32_t* out_idx;
+  float* out_score;
+  uint64_t* trace;
+};
+
+template <bool kInRegs>
+__device__ __forceinline__ void topk_select(const TopkArgs& a, int sq) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t tmp[33];
+  __shared__ uint32_t s_d, s_above;
+  __shared__ int64_t s_pos;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t C = a.C, kk = a.k_eff;
+  const float* est = a.cand_est + (int64_t)sq * a.cmax;
+  const int32_t* cid = a.cand_idx + (int64_t)sq * a.cmax;
+  int32_t* oi = a.out_idx + (int64_t)sq * a.k;
+  float* os = a.out_score ? a.out_score + (int64_t)sq * a.k : nullptr;
+  const int64_t per = (C + blockDim.x - 1) / blockDim.x;
+  const int64_t i0 = min64(C, tid * per);
+  const int n = (int)(min64(C, i0 + per) - i0);
+  uint64_t* tr = sq == 0 ? a.trace : nullptr;
+
+  float e[kTopkRegs];
+  int32_t ix[kTopkRegs];
+  if (kInRegs) {
+#pragma unroll
+    for (int u = 0; u < kTopkRegs; ++u) {
+      e[u] = u < n ? __ldcg(est + i0 + u) : 0.f;
+      ix[u] = u < n ? __ldcg(cid + i0 + u) : 0;
+    }
+  }
+  auto key_of = [&](int u) -> uint32_t { return order_key(kInRegs ? e[u] : __ldcg(est + i0 + u)); };
+  trace_mark(tr, kTrTopk1);
+  uint32_t prefix = 0, mask = 0, remaining = (uint32_t)kk;
+  int64_t pstar = C;
+  if (kk < C) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      if (kInRegs) {
+#pragma unroll
+        for (int u = 0; u < kTopkRegs; ++u) {
+          const uint32_t key = key_of(u);
+          if (u < n && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+      } else {
+        for (int u = 0; u < n; ++u) {
+          const uint32_t key = key_of(u);
+          if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {  // lane l owns digits 255 - 8l .. 248 - 8l
+        uint32_t part = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part += hist[255 - 8 * lane - i];
+        const uint32_t inc = warp_incl_scan(part, lane);
+        const uint32_t exc = inc - part;
+        if (exc < remaining && inc >= remaining) {
+          uint32_t run = exc;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t d = 255 - 8 * lane - i;
+            if (run < remaining && run + hist[d] >= remaining) {
+              s_d = d;
+              s_above = run;
+            }
+            run += hist[d];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= s_d << shift;
+      mask |= 255u << shift;
+      remaining -= s_above;
+    }
+    trace_mark(tr, kTrTopk2);
+    // `remaining` keys equal to prefix are kept: the lowest positions
+    uint32_t n_eq = 0;
+    if (kInRegs) {
+#pragma unroll
+      for (int u = 0; u < kTopkRegs; ++u) n_eq += (u < n && key_of(u) == prefix) ? 1u : 0u;
+    } else {
+      for (int u = 0; u < n; ++u) n_eq += key_of(u) == prefix ? 1u : 0u;
+    }
+    uint32_t tot;
+    const uint32_t before = block_excl_scan(n_eq, tmp, &tot);
+    if (before < remaining && before + n_eq >= remaining) {
+      uint32_t seen = before;
+      for (int u = 0; u < n; ++u)
+        if (key_of(u) == prefix && ++seen == remaining) {
+          s_pos = i0 + u;
+          break;
+        }
+    }
+    __syncthreads();
+    pstar = s_pos;
+  }
+  trace_mark(tr, kTrTopk3);
+  // ordered compaction: keep (key, position) at least as good as (prefix, pstar)
+  auto keep = [&](int u) {
+    const uint32_t key = key_of(u);
+    return kk >= C || key > prefix || (key == prefix && i0 + u <= pstar);
+  };
+  uint32_t cnt = 0;
+  if (kInRegs) {
+#pragma unroll
+    for (int u = 0; u < kTopkRegs; ++u) cnt += (u < n && keep(u)) ? 1u : 0u;
+  } else {
+    for (int u = 0; u < n; ++u) cnt += keep(u) ? 1u : 0u;
+  }
+  uint32_t tot;
+  uint32_t opos = block_excl_scan(cnt, tmp, &tot);
+  if (kInRegs) {
+#pragma unroll
+    for (int u = 0; u < kTopkRegs; ++u)
+      if (u < n && keep(u)) {
+        oi[opos] = ix[u];
+        if (os) os[opos] = e[u];
+        ++opos;
+      }
+  } else {
+    for (int u = 0; u < n; ++u)
+      if (keep(u)) {
+        oi[opos] = __ldcg(cid + i0 + u);
+        if (os) os[opos] = __ldcg(est + i0 + u);
+        ++opos;
+      }
+  }
+  for (int64_t i = kk + tid; i < a.k; i += blockDim.x) {
+    oi[i] = -1;
+    if (os) os[i] = -INFINITY;
+  }
+  trace_mark(tr, kTrTopk4);
+}
+
+__global__ void __launch_bounds__(kTopkThreads) k_topk(TopkArgs a) {
+  const int sq = blockIdx.x;
+  trace_mark(sq == 0 ? a.trace : nullptr, kTrTopk0);
+  if ((a.C + kTopkThreads - 1) / kTopkThreads <= kTopkRegs) topk_select<true>(a, sq);
+  else topk_select<false>(a, sq);
 }
 
 __global__ void k_fill_empty(int32_t* idx, float* score, int64_t n) {
@@ -800,7 +714,7 @@ cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_
 
 size_t vote_smem_bytes(int rho) {
   const int nhot = kSub * rho;
-  return (size_t)kChunk + (size_t)kSub * kCentroids * 4 + (size_t)(3 * nhot + 1) * 4;
+  return (size_t)kChunk + (size_t)kSub * kCentroids * 4 + (size_t)kSub * kOffStride * 4 + (size_t)(3 * nhot + 1) * 4;
 }
 
 cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st) {
@@ -875,6 +789,21 @@ cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st) {
   r.out_score = a.topk_score;
   r.trace = a.trace;
   k_rerank<<<dim3(r.nblk, a.s.batch * a.s.hq), kRerankThreads, 0, st>>>(r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st) {
+  TopkArgs t;
+  t.C = a.C;
+  t.k = a.k;
+  t.k_eff = a.k_eff;
+  t.cmax = a.cmax;
+  t.cand_idx = a.cand_idx;
+  t.cand_est = a.cand_est;
+  t.out_idx = a.topk_idx;
+  t.out_score = a.topk_score;
+  t.trace = a.trace;
+  k_topk<<<a.s.batch * a.s.hq, kTopkThreads, 0, st>>>(t);
   return cudaGetLastError();
 }
 

@@ -277,6 +277,7 @@ paris_status retrieve_launch(paris_ctx* c, const void* q, paris_dtype dtype, int
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_VOTE, s, [&] { return launch_vote(q, dtype, a, fuse, s); }));
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_COMPACT, s, [&] { return launch_compact(a, s); }));
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_RERANK, s, [&] { return launch_rerank(a, s); }));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_TOPK, s, [&] { return launch_topk(a, s); }));
   *k_eff = a.k_eff;
   return PARIS_OK;
 }
@@ -321,7 +322,8 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
     delete c;
     return fail(nullptr, PARIS_EINVAL, "max_ctx - sink must be at most %d tokens", kMaxChunks * kChunk);
   }
-  c->cmax = std::max<int64_t>(1, candidate_count(c->rcap, f.cand_bp, f.topk));
+  // rows of the candidate arrays start on 16-byte boundaries (staged by 16-byte copies)
+  c->cmax = (std::max<int64_t>(1, candidate_count(c->rcap, f.cand_bp, f.topk)) + 3) / 4 * 4;
   c->nsplit_max = (int)((f.sink + f.local + f.update_buf + f.topk + kAttnSplit - 1) / kAttnSplit) + 1;
   std::memset(&c->sm, 0, sizeof c->sm);
   for (int i = 0; i < kDim; ++i)

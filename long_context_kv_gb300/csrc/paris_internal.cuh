@@ -111,6 +111,7 @@ size_t vote_smem_bytes(int rho);
 cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st);
 cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st);
 cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st);
+cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st);
 cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_t st);
 
 // ---- sparse attention ---------------------------------------------------
