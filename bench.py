@@ -280,12 +280,13 @@ def run_ours(args, rank, world):
             a[1] += n
     del g_prof
     kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
-    us_retrieve = sum(1e3 * prof[k][0] for k in ("vote", "compact", "rerank", "topk", "fill")) / args.steps
+    us_retrieve = sum(1e3 * prof[k][0] for k in ("qprep", "vote", "compact", "rerank", "topk", "fill")) / args.steps
     us_attend = 1e3 * prof["attend"][0] / args.steps
     us_append = sum(1e3 * prof[k][0] for k in ("append", "build_index")) / args.steps
 
     # roofline of the dominant kernel (algorithmic bytes per launch)
     Nmean = sum(keys_per_step) / len(keys_per_step) / (b * hkv)
+    nch = -(-int(Nmean) // 16384)
     C = max((w["cand_bp"] * int(Nmean) + 9999) // 10000, min(w["topk"], int(Nmean)))
     keff = min(w["topk"], C)
     nwin = S + w["local"] + w["update_buf"] // 2
@@ -298,6 +299,9 @@ def run_ours(args, rank, world):
         "topk": b * hq * (C * 8 + keff * 8),
         # votes read (1 B per key and query head), candidate positions written
         "compact": b * hq * (int(Nmean) + C * 4),
+        # hot bucket lists (2 B per entry; rho B of 256 buckets per subspace),
+        # bucket offsets of every chunk, votes (1 B per key) and histograms written
+        "vote": b * hq * (2 * w["rho"] * w["n_sub"] * Nmean / 256 + nch * (16 * 264 * 4 + 1024) + Nmean),
         # retrieved K and V rows, plus the window rows once per KV head
         "attend": b * hq * keff * 4 * d + b * hkv * nwin * 4 * d,
     }

@@ -169,8 +169,8 @@ paris_status paris_sparse_attend_noalloc(paris_ctx* ctx, const void* q, paris_dt
 
 /* One decode step: exactly paris_append_decode(k, v), then
  * paris_retrieve(q, ...), then paris_sparse_attend(q, topk_idx, out), with the
- * same arguments and results, in five kernels instead of six: the append
- * rides in the vote kernel unless it fills the Update Buffer (then the flush
+ * same arguments and results, in six kernels instead of seven: the append
+ * rides in the query-preparation kernel unless it fills the Update Buffer (then the flush
  * and index rebuild run first).  k, v: device, kv_dtype, [batch][Hkv][d];
  * q: device, q_dtype, [batch][Hq][d]; outputs as in the two calls.          */
 paris_status paris_decode_step(paris_ctx* ctx, const void* k, const void* v, paris_dtype kv_dtype, const void* q,
@@ -199,9 +199,11 @@ paris_status paris_check_device(paris_ctx* ctx);
  *  PARIS_DUMP_HOT      seq, q head:         uint32 [B][rho] centroid id | weight << 16
  *  PARIS_DUMP_LEVELS   (seq, head ignored): float  [15] 8 levels, 7 thresholds
  *  PARIS_DUMP_KV       seq, KV head:        uint16 [2][T][d] bf16 K then V by position
- *  PARIS_DUMP_TRACE    (seq, head ignored): uint64 [64] phase timestamps (ns, GPU
+ *  PARIS_DUMP_TRACE    (seq, head ignored): uint64 phase timestamps (ns, GPU
  *                      global timer) of the last kernels, recorded only when the
- *                      environment had PARIS_TRACE=1 at paris_create */
+ *                      environment had PARIS_TRACE=1 at paris_create: 64 phase
+ *                      slots, then (start, after wait, -, end) of each of up to
+ *                      4096 blocks of 8 kernels; copies min(bytes, size) */
 enum {
   PARIS_DUMP_IDS = 0, PARIS_DUMP_CODES = 1, PARIS_DUMP_W = 2, PARIS_DUMP_VOTES = 3,
   PARIS_DUMP_CANDS = 4, PARIS_DUMP_CAND_EST = 5, PARIS_DUMP_QT = 6, PARIS_DUMP_QNORM = 7,
@@ -219,14 +221,15 @@ typedef enum {
   PARIS_KERNEL_ENCODE = 1,      /* prefill: SRHT, bucket ids, codes, w                   */
   PARIS_KERNEL_BUILD_INDEX = 2, /* per-chunk inverted bucket index                       */
   PARIS_KERNEL_APPEND = 3,      /* standalone decode append (store + encode one token)   */
-  PARIS_KERNEL_VOTE = 4,        /* query rotation, top-rho centroids, collision votes
-                                   (and a fused append in decode steps)                 */
-  PARIS_KERNEL_COMPACT = 5,     /* candidate selection (ordered compaction)              */
-  PARIS_KERNEL_RERANK = 6,      /* RSQ-IP estimates of the candidates                    */
-  PARIS_KERNEL_TOPK = 7,        /* top-k of the estimates                                */
-  PARIS_KERNEL_ATTEND = 8,      /* sparse attention and the merge of its splits          */
-  PARIS_KERNEL_FILL = 9,        /* empty-result fill                                     */
-  PARIS_KERNEL_COUNT = 10
+  PARIS_KERNEL_QPREP = 4,       /* query rotation, norms, top-rho centroids (and the fused
+                                   append of a decode step)                             */
+  PARIS_KERNEL_VOTE = 5,        /* collision votes over the inverted bucket index        */
+  PARIS_KERNEL_COMPACT = 6,     /* candidate selection (ordered compaction)              */
+  PARIS_KERNEL_RERANK = 7,      /* RSQ-IP estimates of the candidates                    */
+  PARIS_KERNEL_TOPK = 8,        /* top-k of the estimates                                */
+  PARIS_KERNEL_ATTEND = 9,      /* sparse attention and the merge of its splits          */
+  PARIS_KERNEL_FILL = 10,       /* empty-result fill                                     */
+  PARIS_KERNEL_COUNT = 11
 } paris_kernel;
 
 /* Cumulative kernel launches of this context since paris_create, per

@@ -12,7 +12,8 @@
 // rows) in shared memory with asynchronous 16-byte copies, all in flight at
 // once, then computes softmax(q K^T / sqrt(d)) V for them and writes
 // (max, sum, o); the last split of a query head to finish merges the splits
-// (atomic counter after a memory fence, no waiting).  Decode has one query
+// (atomic counter after a memory fence, no waiting), issuing its loads of
+// the splits' partial outputs in batches rather than one after another.  Decode has one query
 // row per head, so the work is a gather plus matrix-vector products: CUDA
 // cores, not tensor cores.
 #include <float.h>
@@ -24,7 +25,7 @@ namespace {
 
 constexpr int kAttnThreads = 128;
 constexpr int kKStride = kDim + 8;  // bf16 elements per staged K row: 272 B keeps 16-byte reads conflict-free
-static_assert(kAttnThreads == kDim && kAttnThreads == kAttnSplit, "one thread per row and per output dimension");
+static_assert(kAttnThreads == kDim && 2 * kAttnSplit == kAttnThreads, "one thread per output dimension, two per row");
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -40,6 +41,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   uint16_t* vs = smem + kAttnSplit * kKStride;  // [kAttnSplit][kDim]
   __shared__ float qf[kDim];
   __shared__ float p[kAttnSplit];
+  __shared__ float fs[kMaxSplits];
   __shared__ float red[8];
   __shared__ int s_last;
   const int split = blockIdx.x;
@@ -47,64 +49,77 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   const int seq = sq / a.s.hq, qh = sq - seq * a.s.hq, kvh = qh / a.s.g;
   const int64_t sh = (int64_t)seq * a.s.hkv + kvh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = tid >> 1, half = tid & 1;  // two threads per row, half a row each
   const int64_t R = nwin + a.k_eff;
   const int ring = a.s.local + a.s.ubuf;
   uint64_t* tr = (split == 0 && sq == 0) ? a.trace : nullptr;
   trace_mark(tr, kTrAttend0);
+  trace_block(a.trace, kTkAttend, 0);
 
-  // row `tid` of the split: find it and copy its K and V rows
-  const int64_t r = (int64_t)split * kAttnSplit + tid;
+  // find row `row` of the split and copy half of its K and V.  Window rows
+  // (written by earlier appends) and q are copied before the wait; the
+  // retrieved rows need the top-k, written by the preceding kernel.
+  const int64_t r = (int64_t)split * kAttnSplit + row;
   const __nv_bfloat16 *kp = nullptr, *vp = nullptr;
-  if (r < R) {
-    if (r < nwin) {
-      int64_t slot = r;
-      if (r >= nsink) {
-        const int64_t pos = a.s.sink + a.N + (r - nsink);
-        slot = a.s.sink + (pos - a.s.sink) % ring;
-      }
-      kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
-      vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
-    } else {
-      const int64_t pos = __ldg(a.topk_idx + (int64_t)sq * a.k + (r - nwin));
-      if (pos >= a.s.sink && pos < a.s.sink + a.N) {
-        kp = a.kv.st_k + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
-        vp = a.kv.st_v + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
-      } else if (pos >= 0) {
-        atomicOr(a.status, kStatusBadIndex);
-      }
+  const int c0 = half * (kDim / 2);
+  if (r < nwin) {
+    int64_t slot = r;
+    if (r >= nsink) {
+      const int64_t pos = a.s.sink + a.N + (r - nsink);
+      slot = a.s.sink + (pos - a.s.sink) % ring;
     }
-  }
-  if (kp) {
+    kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
+    vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
 #pragma unroll
-    for (int j = 0; j < kDim / 8; ++j) {
-      cp_async16(ks + tid * kKStride + 8 * j, kp + 8 * j);
-      cp_async16(vs + tid * kDim + 8 * j, vp + 8 * j);
+    for (int j = 0; j < kDim / 16; ++j) {
+      cp_async16(ks + row * kKStride + c0 + 8 * j, kp + c0 + 8 * j);
+      cp_async16(vs + row * kDim + c0 + 8 * j, vp + c0 + 8 * j);
     }
-  } else {
-    // no row: zeros, so the weighted V sum below reads finite values
-#pragma unroll
-    for (int j = 0; j < kDim / 8; ++j) *reinterpret_cast<uint4*>(vs + tid * kDim + 8 * j) = make_uint4(0, 0, 0, 0);
   }
   qf[tid] = load1(q, dtype, (int64_t)sq * kDim + tid) * qscale;
+  pdl_wait();
+  pdl_trigger();
+  trace_block(a.trace, kTkAttend, 1);
+  if (r >= nwin && r < R) {
+    const int64_t pos = __ldcg(a.topk_idx + (int64_t)sq * a.k + (r - nwin));
+    if (pos >= a.s.sink && pos < a.s.sink + a.N) {
+      kp = a.kv.st_k + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
+      vp = a.kv.st_v + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
+#pragma unroll
+      for (int j = 0; j < kDim / 16; ++j) {
+        cp_async16(ks + row * kKStride + c0 + 8 * j, kp + c0 + 8 * j);
+        cp_async16(vs + row * kDim + c0 + 8 * j, vp + c0 + 8 * j);
+      }
+    } else if (pos >= 0 && half == 0) {
+      atomicOr(a.status, kStatusBadIndex);
+    }
+  }
+  if (!kp) {
+    // no row: zeros, so the weighted V sum below reads finite values
+#pragma unroll
+    for (int j = 0; j < kDim / 16; ++j)
+      *reinterpret_cast<uint4*>(vs + row * kDim + c0 + 8 * j) = make_uint4(0, 0, 0, 0);
+  }
   cp_async_wait_all();
   __syncthreads();
   trace_mark(tr, kTrAttend1);
 
-  // score of row tid (log2 domain)
+  // score of the row (log2 domain): each thread half the dot product
   float s = -FLT_MAX;
-  if (kp) {
+  {
     float acc = 0.f;
 #pragma unroll
-    for (int j = 0; j < kDim / 8; ++j) {
-      const uint4 kv8 = *reinterpret_cast<const uint4*>(ks + tid * kKStride + 8 * j);
+    for (int j = 0; j < kDim / 16; ++j) {
+      const uint4 kv8 = *reinterpret_cast<const uint4*>(ks + row * kKStride + c0 + 8 * j);
       const uint32_t w[4] = {kv8.x, kv8.y, kv8.z, kv8.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        acc += qf[8 * j + 2 * i] * bf16_bits_to_float(w[i] & 0xffffu);
-        acc += qf[8 * j + 2 * i + 1] * bf16_bits_to_float(w[i] >> 16);
+        acc += qf[c0 + 8 * j + 2 * i] * bf16_bits_to_float(w[i] & 0xffffu);
+        acc += qf[c0 + 8 * j + 2 * i + 1] * bf16_bits_to_float(w[i] >> 16);
       }
     }
-    s = acc;
+    acc += __shfl_xor_sync(kFull, acc, 1);
+    if (kp) s = acc;
   }
   float mx = s;
 #pragma unroll
@@ -113,8 +128,8 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   __syncthreads();
   const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   const float pr = kp ? exp2f(s - M) : 0.f;
-  p[tid] = pr;
-  float l = pr;
+  if (half == 0) p[row] = pr;
+  float l = half == 0 ? pr : 0.f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
   if (lane == 0) red[4 + warp] = l;
@@ -133,6 +148,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   }
 
   trace_mark(tr, kTrAttend2);
+  trace_block(a.trace, kTkAttend, 2);
   // the last split of the query head merges all splits
   __threadfence();
   __syncthreads();
@@ -142,42 +158,49 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   __threadfence();
   if (sq == 0) trace_mark(a.trace, kTrAttend3);
   const int d = tid;
-  float Mx = -FLT_MAX;
-  for (int s0 = 0; s0 < nsplit; s0 += 8) {
-    float mm[8], ll[8];
+  // every thread's first batch of o loads goes out together with warp 0's
+  // loads of the splits' (max, sum)
+  constexpr int kBatch = 16;
+  float oo[kBatch];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const bool in = s0 + u < nsplit;
-      mm[u] = in ? __ldcg(part + (int64_t)(s0 + u) * kPartStride) : -FLT_MAX;
-      ll[u] = in ? __ldcg(part + (int64_t)(s0 + u) * kPartStride + 1) : 0.f;
+  for (int u = 0; u < kBatch; ++u) oo[u] = u < nsplit ? __ldcg(part + (int64_t)u * kPartStride + 4 + d) : 0.f;
+  if (warp == 0) {
+    float Mx = -FLT_MAX;
+    for (int s0 = lane; s0 < nsplit; s0 += 32) {
+      const float mm = __ldcg(part + (int64_t)s0 * kPartStride), ll = __ldcg(part + (int64_t)s0 * kPartStride + 1);
+      if (ll > 0.f) Mx = fmaxf(Mx, mm);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (ll[u] > 0.f) Mx = fmaxf(Mx, mm[u]);
+    for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(kFull, Mx, o));
+    float Lt = 0.f;
+    for (int s0 = lane; s0 < nsplit; s0 += 32) {
+      const float mm = __ldcg(part + (int64_t)s0 * kPartStride), ll = __ldcg(part + (int64_t)s0 * kPartStride + 1);
+      const float f = ll > 0.f ? exp2f(mm - Mx) : 0.f;
+      fs[s0] = f;
+      Lt += ll * f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Lt += __shfl_xor_sync(kFull, Lt, o);
+    if (lane == 0) red[0] = Lt;
   }
-  float Lt = 0.f, ot = 0.f;
-  for (int s0 = 0; s0 < nsplit; s0 += 8) {
-    float mm[8], ll[8], oo[8];
+  __syncthreads();
+  float ot = 0.f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const bool in = s0 + u < nsplit;
-      const float* pp = part + (int64_t)(s0 + u) * kPartStride;
-      mm[u] = in ? __ldcg(pp) : 0.f;
-      ll[u] = in ? __ldcg(pp + 1) : 0.f;
-      oo[u] = in ? __ldcg(pp + 4 + d) : 0.f;
-    }
+  for (int u = 0; u < kBatch; ++u)
+    if (u < nsplit) ot += oo[u] * fs[u];
+  for (int s0 = kBatch; s0 < nsplit; s0 += kBatch) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if (ll[u] > 0.f) {
-        const float f = exp2f(mm[u] - Mx);
-        Lt += ll[u] * f;
-        ot += oo[u] * f;
-      }
-    }
+    for (int u = 0; u < kBatch; ++u)
+      oo[u] = s0 + u < nsplit ? __ldcg(part + (int64_t)(s0 + u) * kPartStride + 4 + d) : 0.f;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (s0 + u < nsplit) ot += oo[u] * fs[s0 + u];
   }
+  const float Lt = red[0];
   a.out[(int64_t)sq * kDim + d] = __float2bfloat16_rn(Lt > 0.f ? ot / Lt : 0.f);
   if (tid == 0) a.counter[sq] = 0;
   if (sq == 0) trace_mark(a.trace, kTrAttend4);
+  trace_block(a.trace, kTkAttend, 3);
 }
 
 constexpr size_t kAttendSmem = (size_t)kAttnSplit * (kKStride + kDim) * sizeof(uint16_t);
@@ -203,9 +226,8 @@ cudaError_t launch_attend(const void* q, int dtype, const AttendArgs& a, cudaStr
   const int64_t nsink = min64(a.s.sink, a.T);
   const int64_t nwin = nsink + a.n_local_buf;
   const float qscale = 1.4426950408889634f / sqrtf((float)kDim);
-  k_attend<<<dim3(nsplit, a.s.batch * a.s.hq), kAttnThreads, kAttendSmem, st>>>(q, dtype, a, nsink, nwin, nsplit,
-                                                                                 qscale);
-  return cudaGetLastError();
+  return launch_pdl(k_attend, dim3(nsplit, a.s.batch * a.s.hq), dim3(kAttnThreads), kAttendSmem, st, q, dtype, a,
+                    nsink, nwin, nsplit, qscale);
 }
 
 }  // namespace paris

@@ -20,13 +20,14 @@
 namespace paris {
 namespace {
 
-constexpr int kVoteThreads = 256;
+constexpr int kVoteThreads = 512;
 constexpr int kCompactThreads = 512;
 constexpr int kRerankThreads = 256;
-constexpr int kRerankPer = 3;                      // candidates per thread, all loads in flight together
+constexpr int kRerankPer = 2;                      // candidates per thread, loads in flight together
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkRegs = 8;                       // candidates per thread the top-k holds in registers
-constexpr int kHistRegs = 4;                       // histogram cells per thread held by k_compact
+constexpr int kTopkStage = 24576;                  // candidates the top-k stages in shared memory (192 KB)
+constexpr int kHistRegs = 2;                       // histogram cells per thread held by k_compact
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -35,72 +36,50 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // ===========================================================================
-// k_vote
+// k_qprep
 // ===========================================================================
 //
-// Query preparation (every tile recomputes the rotation and the hot
-// centroids of its query; tile 0 also publishes q~ and ||q||):
+// One block per (sequence, query head); warp w < 16 owns subspace w.
 //   ||q|| = sqrt(sequential sum over the d inputs of q_j q_j);
 //   z = fwht(D q); ||z|| likewise; q~ = z / ||z|| (0 if ||z|| = 0);
 //   score of centroid c in subspace b = sequential sum over j of +-z_{b,j}
 //   (minus where bit j of c is set); the top rho per subspace by
 //   (score desc, id asc) get weight rho - r (rank r) or 1 (flat).
-// Votes: each key of the chunk sits in exactly one bucket per subspace, so
-// walking the hot buckets' lists and adding their weights gives every key
-// sum_b weight_b(id_{i,b}) (one byte per key, at most 255).  The tile
-// writes its votes and their histogram.
-struct VoteArgs {
-  Tables t;
+// Writes q~, ||q|| and the hot list (entry b * rho + r = id | weight << 16).
+// Warps 16 and 17 run the two norm chains; in a decode step warp 18 of the
+// first query head of each KV head appends the step's token.
+constexpr int kQprepThreads = 19 * 32;
+
+struct QprepArgs {
   SignMask sm;
   Shape s;
-  int rho, flat, nbins;
-  int64_t N;
+  int rho, flat;
   const void* q;
   int qdtype;
   float* qt;
   float* qnorm;
   uint32_t* hot;
-  uint8_t* votes;
-  uint32_t* hist;
-  // fused append of one decode token (k_new == nullptr: none)
-  const void* k_new;
+  const void* k_new;  // fused append (nullptr: none)
   const void* v_new;
   int kvdtype;
   int64_t pos;
   KvStore kv;
+  Tables t;
   RsqParams rp;
   uint64_t* trace;
 };
 
-__global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
-  extern __shared__ __align__(16) uint32_t dyn[];
-  const int nhot = kSub * a.rho;
-  uint32_t* votes = dyn;                                                 // kChunk / 4 words
-  float* sc = reinterpret_cast<float*>(votes + kChunk / 4);              // [kSub][kCentroids]
-  uint32_t* offs = reinterpret_cast<uint32_t*>(sc + kSub * kCentroids);  // [kSub][kOffStride]
-  uint32_t* hbeg = offs + kSub * kOffStride;                             // nhot
-  uint32_t* hpre = hbeg + nhot;                                          // nhot + 1
-  uint32_t* hwt = hpre + nhot + 1;                                       // nhot
+__global__ void __launch_bounds__(kQprepThreads) k_qprep(QprepArgs a) {
   __shared__ float qs[kDim], zs[kDim];
-  __shared__ uint32_t hist[kMaxBins];
-  __shared__ uint32_t tmp[33];
-  __shared__ float s_zn;
-
-  const int c = blockIdx.x, sq = blockIdx.y;
+  const int sq = blockIdx.x;
   const int seq = sq / a.s.hq, qh = sq - seq * a.s.hq, kvh = qh / a.s.g;
-  const int64_t sh = (int64_t)seq * a.s.hkv + kvh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t base = (int64_t)c * kChunk;
-  const int len = (int)min64(kChunk, a.N - base);
-  uint64_t* tr = (c == 0 && sq == 0) ? a.trace : nullptr;
+  trace_block(a.trace, kTkQprep, 0);
+  pdl_wait();
+  pdl_trigger();
+  trace_block(a.trace, kTkQprep, 1);
+  uint64_t* tr = sq == 0 ? a.trace : nullptr;
   trace_mark(tr, kTrVote0);
-
-  // -- phase 0: prefetch the chunk's bucket offsets, clear, rotate the query,
-  //    fused append --------------------------------------------------------
-  const uint32_t* off_g = a.t.off + ((sh * a.t.nchunk + c) * kSub) * kOffStride;
-  for (int i = tid; i < kSub * kOffStride / 4; i += blockDim.x) cp_async16(offs + 4 * i, off_g + 4 * i);
-  for (int i = tid; i < kChunk / 16; i += blockDim.x) reinterpret_cast<uint4*>(votes)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < kMaxBins; i += blockDim.x) hist[i] = 0;
   if (warp == 0) {
     float y[4];
     load4(a.q, a.qdtype, (int64_t)sq * kDim + 4 * lane, y);
@@ -110,112 +89,160 @@ __global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
     fwht128_warp(y, lane);
 #pragma unroll
     for (int i = 0; i < 4; ++i) zs[4 * lane + i] = y[i];
-  } else if (warp == kVoteThreads / 32 - 1 && a.k_new != nullptr && c == 0 && qh % a.s.g == 0) {
-    append_token_warp(a.k_new, a.v_new, a.kvdtype, a.pos, sh, lane, a.s, a.kv, a.t, a.sm, a.rp);
+  } else if (warp == 18 && a.k_new != nullptr && qh % a.s.g == 0) {
+    append_token_warp(a.k_new, a.v_new, a.kvdtype, a.pos, (int64_t)seq * a.s.hkv + kvh, lane, a.s, a.kv, a.t,
+                      a.sm, a.rp);
   }
   __syncthreads();
-
   trace_mark(tr, kTrVote1);
-  // -- phase 1: norms (tile 0), centroid scores, hot centroids --------------
-  if (c == 0 && (tid == 32 || tid == 64)) {
-    // sequential sum of squares; the products do not depend on the sum, so
-    // they are formed ahead of the chain
-    const float* src = tid == 32 ? qs : zs;
-    float acc = 0.f;
+  if (warp < kSub) {
+    // scores of centroids lane + 32 i, as order keys
+    const int b = warp;
+    uint32_t key[8];
 #pragma unroll
-    for (int j0 = 0; j0 < kDim; j0 += 32) {
-      float sqv[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) sqv[j] = __fmul_rn(src[j0 + j], src[j0 + j]);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) acc = __fadd_rn(acc, sqv[j]);
-    }
-    if (tid == 32) a.qnorm[sq] = __fsqrt_rn(acc);
-    else s_zn = __fsqrt_rn(acc);
-  }
-  for (int cid = tid; cid < kCentroids; cid += blockDim.x) {
-#pragma unroll
-    for (int b = 0; b < kSub; ++b) {
+    for (int i = 0; i < 8; ++i) {
+      const int cid = lane + 32 * i;
       float acc = 0.f;
 #pragma unroll
       for (int j = 0; j < kM; ++j) {
         const float zz = zs[b * kM + j];
         acc = __fadd_rn(acc, ((cid >> j) & 1) ? -zz : zz);
       }
-      sc[b * kCentroids + cid] = acc;
+      key[i] = order_key(acc);  // never 0 for a finite score
     }
-  }
-  __syncthreads();
-  if (c == 0 && tid < kDim) {
-    const float zn = s_zn;
-    a.qt[(int64_t)sq * kDim + tid] = zn > 0.f ? __fdiv_rn(zs[tid], zn) : 0.f;
-  }
-  // top rho per subspace by (score desc, id asc): warp w takes subspaces w and
-  // w + 8 together; lane l holds ids l + 32 i as order keys (0 = taken)
-  {
-    constexpr int kW = kVoteThreads / 32;
-    uint32_t key[2][8];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) key[h][i] = order_key(sc[(warp + kW * h) * kCentroids + lane + 32 * i]);
+    uint32_t* hot = a.hot + (int64_t)sq * kSub * a.rho + b * a.rho;
     for (int r = 0; r < a.rho; ++r) {
+      uint32_t bk = 0;
+      int bi = 0;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t bk = 0;
-        int bi = 0;
+      for (int i = 0; i < 8; ++i)
+        if (key[i] > bk) {  // strict: among equal keys the lowest id of the lane stays
+          bk = key[i];
+          bi = i;
+        }
+      const uint32_t wmax = __reduce_max_sync(kFull, bk);
+      const uint32_t bid = __reduce_min_sync(kFull, bk == wmax && bk != 0 ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+      if ((int)(bid & 31) == lane) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (key[h][i] > bk) {  // strict: among equal keys the lowest id of the lane stays
-            bk = key[h][i];
-            bi = i;
-          }
-        const uint32_t wmax = __reduce_max_sync(kFull, bk);
-        const uint32_t bid = __reduce_min_sync(kFull, bk == wmax && bk != 0 ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
-        if ((int)(bid & 31) == lane) {
+          if (i == (int)(bid >> 5)) key[i] = 0;
+      }
+      if (lane == 0) hot[r] = bid | ((a.flat ? 1u : (uint32_t)(a.rho - r)) << 16);
+    }
+  } else if (warp == 16 || warp == 17) {
+    // sequential sums of squares (the products are formed ahead of the chain)
+    const float* src = warp == 16 ? qs : zs;
+    float acc = 0.f;
+    if (lane == 0) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i == (int)(bid >> 5)) key[h][i] = 0;
-        }
-        if (lane == 0) {
-          const int b = warp + kW * h;
-          const uint32_t wgt = a.flat ? 1u : (uint32_t)(a.rho - r);
-          const int e = b * a.rho + r;
-          hbeg[e] = bid;
-          hwt[e] = wgt;
-          if (c == 0) a.hot[(int64_t)sq * nhot + e] = bid | (wgt << 16);
-        }
+      for (int j0 = 0; j0 < kDim; j0 += 32) {
+        float sqv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sqv[j] = __fmul_rn(src[j0 + j], src[j0 + j]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc = __fadd_rn(acc, sqv[j]);
+      }
+    }
+    const float nrm = __shfl_sync(kFull, __fsqrt_rn(acc), 0);
+    if (warp == 16) {
+      if (lane == 0) a.qnorm[sq] = nrm;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = 4 * lane + i;
+        a.qt[(int64_t)sq * kDim + j] = nrm > 0.f ? __fdiv_rn(zs[j], nrm) : 0.f;
       }
     }
   }
-  cp_async_wait_all();
-  __syncthreads();
   trace_mark(tr, kTrVote2);
+  trace_block(a.trace, kTkQprep, 3);
+}
 
-  // -- phase 2: walk the hot buckets' lists ---------------------------------
+// ===========================================================================
+// k_vote
+// ===========================================================================
+//
+// One block per tile (chunk of kChunk keys, sequence x query head).  Each key
+// of the chunk sits in exactly one bucket per subspace, so walking the lists
+// of the query's hot buckets and adding their weights gives every key
+// sum_b weight_b(id_{i,b}) (one byte per key, at most 255).  The tile writes
+// its votes and their histogram.
+struct VoteArgs {
+  Tables t;
+  Shape s;
+  int rho, nbins;
+  int64_t N;
+  const uint32_t* hot;
+  uint8_t* votes;
+  uint32_t* hist;
+  uint64_t* trace;
+};
+
+__global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
+  extern __shared__ __align__(16) uint32_t dyn[];
+  const int nhot = kSub * a.rho;
+  uint32_t* votes = dyn;                          // kChunk / 4 words
+  uint32_t* offs = votes + kChunk / 4;            // [kSub][kOffStride]
+  uint32_t* hbeg = offs + kSub * kOffStride;      // nhot
+  uint32_t* hpre = hbeg + nhot;                   // nhot + 1
+  uint32_t* hwt = hpre + nhot + 1;                // nhot
+  __shared__ uint32_t hist[kMaxBins];
+  __shared__ uint32_t tmp[33];
+
+  const int c = blockIdx.x, sq = blockIdx.y;
+  const int seq = sq / a.s.hq, qh = sq - seq * a.s.hq, kvh = qh / a.s.g;
+  const int64_t sh = (int64_t)seq * a.s.hkv + kvh;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t base = (int64_t)c * kChunk;
+  const int len = (int)min64(kChunk, a.N - base);
+  uint64_t* tr = (c == 0 && sq == 0) ? a.trace : nullptr;
+  trace_block(a.trace, kTkVote, 0);
+
+  // before the wait: the chunk's bucket offsets (written by the index build,
+  // never by the query preparation) and cleared counters
+  const uint32_t* off_g = a.t.off + ((sh * a.t.nchunk + c) * kSub) * kOffStride;
+  for (int i = tid; i < kSub * kOffStride / 4; i += blockDim.x) cp_async16(offs + 4 * i, off_g + 4 * i);
+  for (int i = tid; i < kChunk / 16; i += blockDim.x) reinterpret_cast<uint4*>(votes)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < kMaxBins; i += blockDim.x) hist[i] = 0;
+  pdl_wait();
+  pdl_trigger();
+  trace_block(a.trace, kTkVote, 1);
+  trace_mark(tr, kTrVote3);
+
+  // hot buckets: list begin and length
+  const uint32_t* hot = a.hot + (int64_t)sq * nhot;
   const uint16_t* ent = a.t.ent + ((sh * a.t.nchunk + c) * kSub) * (int64_t)kChunk;
   {
-    const int per = (nhot + blockDim.x - 1) / blockDim.x;  // <= 16
-    uint32_t lens[16];
+    constexpr int kHotPer = (kSub * kCentroids + kVoteThreads - 1) / kVoteThreads;  // hot entries per thread
+    const int per = (nhot + blockDim.x - 1) / blockDim.x;
+    uint32_t hv[kHotPer];
+#pragma unroll
+    for (int i = 0; i < kHotPer; ++i) {
+      const int e = tid * per + i;
+      hv[i] = (i < per && e < nhot) ? __ldcg(hot + e) : 0u;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    uint32_t lens[kHotPer];
     uint32_t my = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kHotPer; ++i) {
       const int e = tid * per + i;
       lens[i] = 0;
       if (i < per && e < nhot) {
         const int b = e / a.rho;
-        const uint32_t id = hbeg[e];
+        const uint32_t id = hv[i] & 0xffffu;
         const uint32_t beg = offs[b * kOffStride + id];
-        const uint32_t end = offs[b * kOffStride + id + 1];
-        lens[i] = end - beg;
+        lens[i] = offs[b * kOffStride + id + 1] - beg;
         hbeg[e] = (uint32_t)b * kChunk + beg;
+        hwt[e] = hv[i] >> 16;
       }
       my += lens[i];
     }
     uint32_t total;
     uint32_t run = block_excl_scan(my, tmp, &total);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kHotPer; ++i) {
       const int e = tid * per + i;
       if (i < per && e < nhot) hpre[e] = run;
       run += lens[i];
@@ -224,9 +251,9 @@ __global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
   }
   __syncthreads();
   const uint32_t total = hpre[nhot];
-  // thread t takes 16 consecutive list entries: one search, then linear steps;
-  // all 16 loads in flight together
-  constexpr int kWalk = 16;
+  // thread t takes kWalk consecutive list entries: one search, then linear
+  // steps; all kWalk loads in flight together
+  constexpr int kWalk = 8;
   for (uint32_t f0 = kWalk * tid; f0 < total; f0 += kWalk * blockDim.x) {
     int e = 0, hi = nhot - 1;  // last e with hpre[e] <= f0 (a non-empty list)
     while (e < hi) {
@@ -250,9 +277,9 @@ __global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
       if (wt[u]) atomicAdd(&votes[key[u] >> 2], wt[u] << ((key[u] & 3) * 8));
   }
   __syncthreads();
+  trace_mark(tr, kTrVote4);
 
-  trace_mark(tr, kTrVote3);
-  // -- phase 3: histogram of the chunk's votes, votes out --------------------
+  // histogram of the chunk's votes, votes out
   uint8_t* vout = a.votes + (int64_t)sq * a.t.nchunk * kChunk + base;
   uint32_t nz = 0, small = 0;
   for (int i = tid; i < kChunk / 16; i += blockDim.x) {
@@ -268,7 +295,6 @@ __global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
       nz += in ? 1u : 0u;
     }
   }
-  // the common small vote values: warp sums of the packed counters
 #pragma unroll
   for (int v = 1; v <= 4; ++v) {
     const uint32_t cnt = __reduce_add_sync(kFull, (small >> (8 * (v - 1))) & 0xffu);
@@ -278,7 +304,7 @@ __global__ void __launch_bounds__(kVoteThreads, 2) k_vote(VoteArgs a) {
   block_excl_scan(nz, tmp, &nz_total);
   uint32_t* hout = a.hist + ((int64_t)sq * a.t.nchunk + c) * kMaxBins;
   for (int s = tid; s < a.nbins; s += blockDim.x) hout[s] = s == 0 ? (uint32_t)len - nz_total : hist[s];
-  trace_mark(tr, kTrVote4);
+  trace_block(a.trace, kTkVote, 3);
 }
 
 // ===========================================================================
@@ -332,9 +358,13 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
   const int nitems = a.nch * a.nbins;
   const uint32_t* h = a.hist + (int64_t)sq * a.nchunk * kMaxBins;
   uint64_t* tr = (c == 0 && sq == 0) ? a.trace : nullptr;
+  for (int i = tid; i < kMaxBins; i += blockDim.x) tot[i] = 0;
+  trace_block(a.trace, kTkCompact, 0);
+  pdl_wait();
+  pdl_trigger();
+  trace_block(a.trace, kTkCompact, 1);
   trace_mark(tr, kTrCompact0);
 
-  for (int i = tid; i < kMaxBins; i += blockDim.x) tot[i] = 0;
   // loads in flight together: histogram cells and this chunk's votes
   uint32_t hv[kHistRegs];
 #pragma unroll
@@ -443,6 +473,7 @@ __global__ void __launch_bounds__(kCompactThreads, 2) k_compact(CompactArgs a) {
     if (take) out[pos++] = (int32_t)(a.sink + base + k0 + i);
   }
   trace_mark(tr, kTrCompact2);
+  trace_block(a.trace, kTkCompact, 3);
 }
 
 // ===========================================================================
@@ -490,7 +521,7 @@ __device__ __forceinline__ float rerank_record(const uint4 (&x)[8], const float*
   return __fmul_rn(qn, acc);
 }
 
-__global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
+__global__ void __launch_bounds__(kRerankThreads, 3) k_rerank(RerankArgs a) {
   __shared__ float tq[kDim * 16];
   const int blk = blockIdx.x, sq = blockIdx.y;
   const int seq = sq / a.hq, qh = sq - seq * a.hq, kvh = qh / a.g;
@@ -499,16 +530,12 @@ __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
   const int64_t r0 = (int64_t)blk * kRerankPer * kRerankThreads;
   uint64_t* tr = (blk == 0 && sq == 0) ? a.trace : nullptr;
   trace_mark(tr, kTrRerank0);
+  trace_block(a.trace, kTkRerank, 0);
 
-  // loads in flight together: q~ for the product table, candidate positions
+  // before the wait: q~ and ||q|| (written by the query preparation, three
+  // kernels back) and the product table
   const float qv = __ldcg(a.qt + (int64_t)sq * kDim + (tid >> 1));
   const float qn = __ldcg(a.qnorm + sq);
-  int32_t pos[kRerankPer];
-#pragma unroll
-  for (int p = 0; p < kRerankPer; ++p) {
-    const int64_t r = r0 + p * kRerankThreads + tid;
-    pos[p] = r < a.C ? __ldcg(a.cand_idx + (int64_t)sq * a.cmax + r) : -1;
-  }
   {
     const int coord = tid >> 1, nb0 = (tid & 1) * 8;
 #pragma unroll
@@ -517,6 +544,15 @@ __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
       const float l = a.rp.lev[nib & 7];
       tq[coord * 16 + nib] = __fmul_rn((nib & 8) ? -l : l, qv);
     }
+  }
+  pdl_wait();
+  pdl_trigger();
+  trace_block(a.trace, kTkRerank, 1);
+  int32_t pos[kRerankPer];
+#pragma unroll
+  for (int p = 0; p < kRerankPer; ++p) {
+    const int64_t r = r0 + p * kRerankThreads + tid;
+    pos[p] = r < a.C ? __ldcg(a.cand_idx + (int64_t)sq * a.cmax + r) : -1;
   }
   // the candidates' 128-byte records
   const uint8_t* rec = a.t.rec + sh * a.t.rcap * kRecBytes;
@@ -537,6 +573,7 @@ __global__ void __launch_bounds__(kRerankThreads, 2) k_rerank(RerankArgs a) {
   }
 
   trace_mark(tr, kTrRerank2);
+  trace_block(a.trace, kTkRerank, 3);
 }
 
 // ===========================================================================
@@ -559,69 +596,47 @@ struct TopkArgs {
   uint64_t* trace;
 };
 
-template <bool kInRegs>
-__device__ __forceinline__ void topk_select(const TopkArgs& a, int sq) {
+// E, I: the query head's estimates and positions (staged in shared memory,
+// or the global arrays).  Counting passes use strided ownership (i = t +
+// blockDim * u); the tie and output passes use contiguous slices so that the
+// result comes out in ascending position order.
+__device__ __forceinline__ void topk_select(const TopkArgs& a, int sq, const float* E, const int32_t* I) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t tmp[33];
   __shared__ uint32_t s_d, s_above;
   __shared__ int64_t s_pos;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nt = blockDim.x;
   const int64_t C = a.C, kk = a.k_eff;
-  const float* est = a.cand_est + (int64_t)sq * a.cmax;
-  const int32_t* cid = a.cand_idx + (int64_t)sq * a.cmax;
   int32_t* oi = a.out_idx + (int64_t)sq * a.k;
   float* os = a.out_score ? a.out_score + (int64_t)sq * a.k : nullptr;
-  const int64_t per = (C + blockDim.x - 1) / blockDim.x;
-  const int64_t i0 = min64(C, tid * per);
-  const int n = (int)(min64(C, i0 + per) - i0);
   uint64_t* tr = sq == 0 ? a.trace : nullptr;
-
-  float e[kTopkRegs];
-  int32_t ix[kTopkRegs];
-  if (kInRegs) {
-#pragma unroll
-    for (int u = 0; u < kTopkRegs; ++u) {
-      e[u] = u < n ? __ldcg(est + i0 + u) : 0.f;
-      ix[u] = u < n ? __ldcg(cid + i0 + u) : 0;
-    }
-  }
-  auto key_of = [&](int u) -> uint32_t { return order_key(kInRegs ? e[u] : __ldcg(est + i0 + u)); };
   trace_mark(tr, kTrTopk1);
   uint32_t prefix = 0, mask = 0, remaining = (uint32_t)kk;
   int64_t pstar = C;
+  const int64_t per = (C + nt - 1) / nt;
+  const int64_t i0 = min64(C, tid * per), i1 = min64(C, i0 + per);
   if (kk < C) {
     for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+      for (int i = tid; i < 256; i += nt) hist[i] = 0;
       __syncthreads();
-      if (kInRegs) {
-#pragma unroll
-        for (int u = 0; u < kTopkRegs; ++u) {
-          const uint32_t key = key_of(u);
-          if (u < n && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-        }
-      } else {
-        for (int u = 0; u < n; ++u) {
-          const uint32_t key = key_of(u);
-          if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-        }
+      for (int64_t i = tid; i < C; i += nt) {
+        const uint32_t key = order_key(E[i]);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (warp == 0) {  // lane l owns digits 255 - 8l .. 248 - 8l
-        uint32_t part = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) part += hist[255 - 8 * lane - i];
-        const uint32_t inc = warp_incl_scan(part, lane);
-        const uint32_t exc = inc - part;
-        if (exc < remaining && inc >= remaining) {
-          uint32_t run = exc;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t d = 255 - 8 * lane - i;
-            if (run < remaining && run + hist[d] >= remaining) {
-              s_d = d;
-              s_above = run;
-            }
-            run += hist[d];
+      {
+        // threads t < 256 own digit 255 - t: block-wide exclusive sums from the top
+        const uint32_t v = tid < 256 ? hist[255 - tid] : 0u;
+        const uint32_t inc = warp_incl_scan(v, lane);
+        if (tid < 256 && lane == 31) tmp[warp] = inc;
+        __syncthreads();
+        if (tid < 256) {
+          uint32_t off = 0;
+          for (int w = 0; w < warp; ++w) off += tmp[w];
+          const uint32_t exc = off + inc - v;
+          if (exc < remaining && exc + v >= remaining) {
+            s_d = 255 - tid;
+            s_above = exc;
           }
         }
       }
@@ -633,19 +648,14 @@ __device__ __forceinline__ void topk_select(const TopkArgs& a, int sq) {
     trace_mark(tr, kTrTopk2);
     // `remaining` keys equal to prefix are kept: the lowest positions
     uint32_t n_eq = 0;
-    if (kInRegs) {
-#pragma unroll
-      for (int u = 0; u < kTopkRegs; ++u) n_eq += (u < n && key_of(u) == prefix) ? 1u : 0u;
-    } else {
-      for (int u = 0; u < n; ++u) n_eq += key_of(u) == prefix ? 1u : 0u;
-    }
+    for (int64_t i = i0; i < i1; ++i) n_eq += order_key(E[i]) == prefix ? 1u : 0u;
     uint32_t tot;
     const uint32_t before = block_excl_scan(n_eq, tmp, &tot);
     if (before < remaining && before + n_eq >= remaining) {
       uint32_t seen = before;
-      for (int u = 0; u < n; ++u)
-        if (key_of(u) == prefix && ++seen == remaining) {
-          s_pos = i0 + u;
+      for (int64_t i = i0; i < i1; ++i)
+        if (order_key(E[i]) == prefix && ++seen == remaining) {
+          s_pos = i;
           break;
         }
     }
@@ -654,36 +664,23 @@ __device__ __forceinline__ void topk_select(const TopkArgs& a, int sq) {
   }
   trace_mark(tr, kTrTopk3);
   // ordered compaction: keep (key, position) at least as good as (prefix, pstar)
-  auto keep = [&](int u) {
-    const uint32_t key = key_of(u);
-    return kk >= C || key > prefix || (key == prefix && i0 + u <= pstar);
-  };
   uint32_t cnt = 0;
-  if (kInRegs) {
-#pragma unroll
-    for (int u = 0; u < kTopkRegs; ++u) cnt += (u < n && keep(u)) ? 1u : 0u;
-  } else {
-    for (int u = 0; u < n; ++u) cnt += keep(u) ? 1u : 0u;
+  for (int64_t i = i0; i < i1; ++i) {
+    const uint32_t key = order_key(E[i]);
+    cnt += (kk >= C || key > prefix || (key == prefix && i <= pstar)) ? 1u : 0u;
   }
   uint32_t tot;
   uint32_t opos = block_excl_scan(cnt, tmp, &tot);
-  if (kInRegs) {
-#pragma unroll
-    for (int u = 0; u < kTopkRegs; ++u)
-      if (u < n && keep(u)) {
-        oi[opos] = ix[u];
-        if (os) os[opos] = e[u];
-        ++opos;
-      }
-  } else {
-    for (int u = 0; u < n; ++u)
-      if (keep(u)) {
-        oi[opos] = __ldcg(cid + i0 + u);
-        if (os) os[opos] = __ldcg(est + i0 + u);
-        ++opos;
-      }
+  for (int64_t i = i0; i < i1; ++i) {
+    const float e = E[i];
+    const uint32_t key = order_key(e);
+    if (kk >= C || key > prefix || (key == prefix && i <= pstar)) {
+      oi[opos] = I[i];
+      if (os) os[opos] = e;
+      ++opos;
+    }
   }
-  for (int64_t i = kk + tid; i < a.k; i += blockDim.x) {
+  for (int64_t i = kk + tid; i < a.k; i += nt) {
     oi[i] = -1;
     if (os) os[i] = -INFINITY;
   }
@@ -691,10 +688,31 @@ __device__ __forceinline__ void topk_select(const TopkArgs& a, int sq) {
 }
 
 __global__ void __launch_bounds__(kTopkThreads) k_topk(TopkArgs a) {
+  extern __shared__ __align__(16) uint32_t stage[];
   const int sq = blockIdx.x;
+  trace_block(a.trace, kTkTopk, 0);
+  pdl_wait();
+  pdl_trigger();
+  trace_block(a.trace, kTkTopk, 1);
   trace_mark(sq == 0 ? a.trace : nullptr, kTrTopk0);
-  if ((a.C + kTopkThreads - 1) / kTopkThreads <= kTopkRegs) topk_select<true>(a, sq);
-  else topk_select<false>(a, sq);
+  const float* est = a.cand_est + (int64_t)sq * a.cmax;
+  const int32_t* cid = a.cand_idx + (int64_t)sq * a.cmax;
+  if (a.C <= kTopkStage) {
+    // 16-byte copies, all in flight together (rows start on 16-byte boundaries)
+    float* se = reinterpret_cast<float*>(stage);
+    int32_t* si = reinterpret_cast<int32_t*>(stage + ((a.C + 3) / 4) * 4);
+    const int nch = (int)((a.C + 3) / 4);
+    for (int i = threadIdx.x; i < nch; i += blockDim.x) {
+      cp_async16(se + 4 * i, est + 4 * i);
+      cp_async16(si + 4 * i, cid + 4 * i);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    topk_select(a, sq, se, si);
+  } else {
+    topk_select(a, sq, est, cid);
+  }
+  trace_block(a.trace, kTkTopk, 3);
 }
 
 __global__ void k_fill_empty(int32_t* idx, float* score, int64_t n) {
@@ -714,31 +732,41 @@ cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_
 
 size_t vote_smem_bytes(int rho) {
   const int nhot = kSub * rho;
-  return (size_t)kChunk + (size_t)kSub * kCentroids * 4 + (size_t)kSub * kOffStride * 4 + (size_t)(3 * nhot + 1) * 4;
+  return (size_t)kChunk + (size_t)kSub * kOffStride * 4 + (size_t)(3 * nhot + 1) * 4;
 }
 
-cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st) {
+cudaError_t launch_qprep(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st) {
+  QprepArgs p;
+  p.sm = a.sm;
+  p.s = a.s;
+  p.rho = a.rho;
+  p.flat = a.flat;
+  p.q = q;
+  p.qdtype = dtype;
+  p.qt = a.qt;
+  p.qnorm = a.qnorm;
+  p.hot = a.hot;
+  p.k_new = ap ? ap->k : nullptr;
+  p.v_new = ap ? ap->v : nullptr;
+  p.kvdtype = ap ? ap->dtype : 0;
+  p.pos = ap ? ap->pos : 0;
+  p.kv = ap ? ap->kv : KvStore{};
+  p.t = a.t;
+  p.rp = a.rp;
+  p.trace = a.trace;
+  return launch_pdl(k_qprep, dim3(a.s.batch * a.s.hq), dim3(kQprepThreads), 0, st, p);
+}
+
+cudaError_t launch_vote(const RetrieveArgs& a, cudaStream_t st) {
   VoteArgs v;
   v.t = a.t;
-  v.sm = a.sm;
   v.s = a.s;
   v.rho = a.rho;
-  v.flat = a.flat;
   v.nbins = a.nbins;
   v.N = a.N;
-  v.q = q;
-  v.qdtype = dtype;
-  v.qt = a.qt;
-  v.qnorm = a.qnorm;
   v.hot = a.hot;
   v.votes = a.votes;
   v.hist = a.hist;
-  v.k_new = ap ? ap->k : nullptr;
-  v.v_new = ap ? ap->v : nullptr;
-  v.kvdtype = ap ? ap->dtype : 0;
-  v.pos = ap ? ap->pos : 0;
-  v.kv = ap ? ap->kv : KvStore{};
-  v.rp = a.rp;
   v.trace = a.trace;
   static bool attr_set = false;
   if (!attr_set) {
@@ -747,8 +775,7 @@ cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const A
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_vote<<<dim3(a.nchunk_active, a.s.batch * a.s.hq), kVoteThreads, vote_smem_bytes(a.rho), st>>>(v);
-  return cudaGetLastError();
+  return launch_pdl(k_vote, dim3(a.nchunk_active, a.s.batch * a.s.hq), dim3(kVoteThreads), vote_smem_bytes(a.rho), st, v);
 }
 
 cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st) {
@@ -764,8 +791,7 @@ cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st) {
   c.hist = a.hist;
   c.cand_idx = a.cand_idx;
   c.trace = a.trace;
-  k_compact<<<dim3(a.nchunk_active, a.s.batch * a.s.hq), kCompactThreads, 0, st>>>(c);
-  return cudaGetLastError();
+  return launch_pdl(k_compact, dim3(a.nchunk_active, a.s.batch * a.s.hq), dim3(kCompactThreads), 0, st, c);
 }
 
 cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st) {
@@ -788,8 +814,7 @@ cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st) {
   r.out_idx = a.topk_idx;
   r.out_score = a.topk_score;
   r.trace = a.trace;
-  k_rerank<<<dim3(r.nblk, a.s.batch * a.s.hq), kRerankThreads, 0, st>>>(r);
-  return cudaGetLastError();
+  return launch_pdl(k_rerank, dim3(r.nblk, a.s.batch * a.s.hq), dim3(kRerankThreads), 0, st, r);
 }
 
 cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st) {
@@ -803,8 +828,14 @@ cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st) {
   t.out_idx = a.topk_idx;
   t.out_score = a.topk_score;
   t.trace = a.trace;
-  k_topk<<<a.s.batch * a.s.hq, kTopkThreads, 0, st>>>(t);
-  return cudaGetLastError();
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkStage * 8);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const size_t smem = a.C <= kTopkStage ? (size_t)((a.C + 3) / 4) * 4 * 8 : 0;
+  return launch_pdl(k_topk, dim3(a.s.batch * a.s.hq), dim3(kTopkThreads), smem, st, t);
 }
 
 }  // namespace paris

@@ -274,7 +274,8 @@ paris_status retrieve_launch(paris_ctx* c, const void* q, paris_dtype dtype, int
     return PARIS_OK;
   }
   const RetrieveArgs a = retrieve_args(c, topk_idx, topk_score);
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_VOTE, s, [&] { return launch_vote(q, dtype, a, fuse, s); }));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_QPREP, s, [&] { return launch_qprep(q, dtype, a, fuse, s); }));
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_VOTE, s, [&] { return launch_vote(a, s); }));
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_COMPACT, s, [&] { return launch_compact(a, s); }));
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_RERANK, s, [&] { return launch_rerank(a, s); }));
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_TOPK, s, [&] { return launch_topk(a, s); }));
@@ -325,6 +326,11 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   // rows of the candidate arrays start on 16-byte boundaries (staged by 16-byte copies)
   c->cmax = (std::max<int64_t>(1, candidate_count(c->rcap, f.cand_bp, f.topk)) + 3) / 4 * 4;
   c->nsplit_max = (int)((f.sink + f.local + f.update_buf + f.topk + kAttnSplit - 1) / kAttnSplit) + 1;
+  if (c->nsplit_max > kMaxSplits) {
+    delete c;
+    return fail(nullptr, PARIS_EINVAL, "sink + local + update_buf + topk must be at most %d rows",
+                (kMaxSplits - 1) * kAttnSplit);
+  }
   std::memset(&c->sm, 0, sizeof c->sm);
   for (int i = 0; i < kDim; ++i)
     if (srht_signs[i] < 0) c->sm.w[i >> 5] |= 1u << (i & 31);
@@ -382,14 +388,14 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   TRY(dalloc(c, &c->part, (size_t)bq * c->nsplit_max * kPartStride * sizeof(float), "attention partials"));
   TRY(dalloc(c, &c->status, sizeof(uint32_t), "status word"));
   TRY(dalloc(c, &c->counters, (size_t)2 * bq * sizeof(uint32_t), "block counters"));
-  TRY(dalloc(c, &c->trace, kTraceSlots * sizeof(uint64_t), "phase trace"));
   {
     const char* env = std::getenv("PARIS_TRACE");
     c->tracing = env != nullptr && env[0] == '1';
   }
+  TRY(dalloc(c, &c->trace, (c->tracing ? kTraceWords : kTraceSlots) * sizeof(uint64_t), "phase trace"));
   cudaError_t e = cudaMemset(c->status, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)2 * bq * sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMemset(c->trace, 0, kTraceSlots * sizeof(uint64_t));
+  if (e == cudaSuccess) e = cudaMemset(c->trace, 0, (c->tracing ? kTraceWords : kTraceSlots) * sizeof(uint64_t));
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "initialising the context"));
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "cudaDeviceSynchronize"));
@@ -616,10 +622,12 @@ paris_status paris_debug_dump(paris_ctx* c, int what, int seq, int head, void* d
       }
       return PARIS_OK;
     }
-    case PARIS_DUMP_TRACE:
-      if ((st = need(kTraceSlots * sizeof(uint64_t))) != PARIS_OK) return st;
-      PARIS_CUDA(c, cudaMemcpy(dst, c->trace, kTraceSlots * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+    case PARIS_DUMP_TRACE: {
+      const size_t n = (size_t)(c->tracing ? kTraceWords : kTraceSlots) * sizeof(uint64_t);
+      if ((st = need(std::min(n, bytes))) != PARIS_OK) return st;
+      PARIS_CUDA(c, cudaMemcpy(dst, c->trace, std::min(n, bytes), cudaMemcpyDeviceToHost));
       return PARIS_OK;
+    }
     default:
       return fail(c, PARIS_EINVAL, "unknown dump %d", what);
   }

@@ -11,6 +11,15 @@ constexpr unsigned kFull = 0xffffffffu;
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
+// Programmatic dependent launch.  pdl_wait(): wait until the preceding kernel
+// of the stream has completed and its writes are visible (returns at once
+// when the launch has no programmatic dependency).  pdl_trigger(): let the
+// next kernel of the stream be scheduled; every kernel here triggers only
+// after its own wait, so work a kernel does before its wait overlaps nothing
+// but its immediate predecessor.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // Phase trace: thread 0 of a chosen block stores the global nanosecond timer
 // into trace[slot] (trace == nullptr: tracing off).
 __device__ __forceinline__ void trace_mark(uint64_t* trace, int slot) {
@@ -18,6 +27,19 @@ __device__ __forceinline__ void trace_mark(uint64_t* trace, int slot) {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     trace[slot] = t;
+  }
+}
+
+// Per-block trace: thread 0 of every block stores the timer into
+// trace[kTraceSlots + ((kernel * kTraceBlocks + block) * 4 + phase)].
+__device__ __forceinline__ void trace_block(uint64_t* trace, int kernel, int phase) {
+  if (trace != nullptr && threadIdx.x == 0) {
+    const int64_t blk = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+    if (blk < kTraceBlocks) {
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      trace[kTraceSlots + ((int64_t)kernel * kTraceBlocks + blk) * 4 + phase] = t;
+    }
   }
 }
 

@@ -18,7 +18,8 @@ constexpr int kCentroids = 1 << kM;
 constexpr int kRecBytes = 128;         // 64 B packed codes + 16 x float w
 constexpr int kChunk = 16384;          // keys per inverted-index chunk
 constexpr int kOffStride = 264;        // 257 bucket offsets, padded
-constexpr int kAttnSplit = 128;        // attention rows per partial block
+constexpr int kAttnSplit = 64;         // attention rows per partial block
+constexpr int kMaxSplits = 512;        // partial blocks per query head: window + k <= 32768 rows
 constexpr int kPartStride = kDim + 4;  // m, l, pad, pad, o[128]
 constexpr int kMaxBins = 256;          // vote values 0..255
 constexpr int kMaxChunks = 256;        // chunks per (sequence, KV head): 4M Retrieval-zone keys
@@ -107,8 +108,27 @@ struct AppendFuse {
   KvStore kv;
 };
 
+// Launch `kern` so that it may start while the preceding kernel of the
+// stream finishes (the kernel itself waits with pdl_wait before it reads
+// anything that kernel writes).
+template <typename... P, typename... A>
+cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+}
+
+cudaError_t launch_qprep(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st);
 size_t vote_smem_bytes(int rho);
-cudaError_t launch_vote(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st);
+cudaError_t launch_vote(const RetrieveArgs& a, cudaStream_t st);
 cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st);
 cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st);
 cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st);
@@ -137,6 +157,10 @@ constexpr uint32_t kStatusBadIndex = 1u;
 // Phase-trace slots (block (0, 0) of each kernel, and the reducing block of
 // query head 0).
 constexpr int kTraceSlots = 64;
+constexpr int kTraceBlocks = 4096;   // per-block stamps (start, after wait, -, end) of up to 8 kernels
+constexpr int kTraceKernels = 8;
+constexpr int64_t kTraceWords = kTraceSlots + (int64_t)kTraceKernels * kTraceBlocks * 4;
+enum TraceKernel { kTkQprep = 0, kTkVote, kTkCompact, kTkRerank, kTkTopk, kTkAttend };
 enum TraceSlot {
   kTrVote0 = 0, kTrVote1, kTrVote2, kTrVote3, kTrVote4,
   kTrCompact0 = 8, kTrCompact1, kTrCompact2,

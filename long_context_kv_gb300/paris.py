@@ -49,7 +49,7 @@ _SIGNATURES = {
     "paris_profile_end": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
 }
 
-KERNELS = ["place_kv", "encode", "build_index", "append", "vote", "compact", "rerank", "topk", "attend", "fill"]
+KERNELS = ["place_kv", "encode", "build_index", "append", "qprep", "vote", "compact", "rerank", "topk", "attend", "fill"]
 
 
 class paris_config(ctypes.Structure):
@@ -225,7 +225,7 @@ class Context:
             DUMP_VOTES: ((N,), np.uint8), DUMP_CANDS: ((C,), np.int32), DUMP_CAND_EST: ((C,), np.float32),
             DUMP_QT: ((d,), np.float32), DUMP_QNORM: ((1,), np.float32), DUMP_HOT: ((B, rho), np.uint32),
             DUMP_LEVELS: ((15,), np.float32), DUMP_KV: ((2, T, d), np.uint16),
-            DUMP_TRACE: ((64,), np.uint64),
+            DUMP_TRACE: ((64 + 8 * 4096 * 4,), np.uint64),
         }
         shape, dt = shapes[what]
         out = np.zeros(shape, dtype=dt)

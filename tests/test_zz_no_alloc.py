@@ -40,7 +40,7 @@ def test_noalloc_attention_matches_the_context_scratch_version_twice():
 
 
 def test_noalloc_attention_rejects_shapes_beyond_its_area():
-    # 64 query heads x ceil((16 + 64 + 4096) / 128) = 33 splits = 2112 rows > 1024
+    # 64 query heads x ceil((16 + 64 + 4096) / 64) = 66 splits = 4224 rows > 1024
     c = g.make_case(16 + 5000 + 64, seed=32, n_kv_heads=8, n_q_heads=64, sink=16, local=64, update_buf=16,
                     topk=4096, cand_bp=10000)
     q = g.queries_from_zone(c)
