@@ -119,7 +119,7 @@ def traffic_record(kernel: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", "kernels_retrieve.cu"), "rb").read() + \
+    src = open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", "kernels_decode.cu"), "rb").read() + \
         open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", "kernels_attend.cu"), "rb").read()
     sha = hashlib.sha1(src).hexdigest()[:12]
     for line in open(path):
@@ -192,6 +192,12 @@ def run_ours(args, rank, world):
         j = L["step"]
         L["step"] = j + 1
         L["ctx"].paris_decode_step(L["kn"][j], L["vn"][j], L["qs"][j], L["idx"], L["sc"], L["out"])
+
+    if args.profile_case:
+        for i in range(args.warmup + args.steps):
+            step(i)
+        torch.cuda.synchronize()
+        return {"profile_case": DESCRIPTION[args.workload], "layers": nl, "steps": args.warmup + args.steps}
 
     dist = world > 1
     if dist:
@@ -280,9 +286,8 @@ def run_ours(args, rank, world):
             a[1] += n
     del g_prof
     kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
-    us_retrieve = sum(1e3 * prof[k][0] for k in ("qprep", "vote", "compact", "rerank", "topk", "fill")) / args.steps
-    us_attend = 1e3 * prof["attend"][0] / args.steps
-    us_append = sum(1e3 * prof[k][0] for k in ("append", "build_index")) / args.steps
+    us_decode = 1e3 * prof.get("decode", [0.0, 0])[0] / args.steps
+    us_append = sum(1e3 * prof.get(k, [0.0, 0])[0] for k in ("append", "build_index")) / args.steps
 
     # roofline of the dominant kernel (algorithmic bytes per launch)
     Nmean = sum(keys_per_step) / len(keys_per_step) / (b * hkv)
@@ -291,19 +296,13 @@ def run_ours(args, rank, world):
     keff = min(w["topk"], C)
     nwin = S + w["local"] + w["update_buf"] // 2
     alg = {
-        # votes read back (1 B per key and query head), candidate records
-        # (64 B codes + 64 B w) gathered, candidate index + estimate written,
-        # top-k index + estimate written
-        "rerank": b * hq * C * (4 + 128 + 4),
-        # estimates and positions read, top-k positions and estimates written
-        "topk": b * hq * (C * 8 + keff * 8),
-        # votes read (1 B per key and query head), candidate positions written
-        "compact": b * hq * (int(Nmean) + C * 4),
-        # hot bucket lists (2 B per entry; rho B of 256 buckets per subspace),
-        # bucket offsets of every chunk, votes (1 B per key) and histograms written
-        "vote": b * hq * (2 * w["rho"] * w["n_sub"] * Nmean / 256 + nch * (16 * 264 * 4 + 1024) + Nmean),
-        # retrieved K and V rows, plus the window rows once per KV head
-        "attend": b * hq * keff * 4 * d + b * hkv * nwin * 4 * d,
+        # one launch = one decode step of one layer.  Per query head: the
+        # hot buckets' list entries (2 B each; rho of 256 buckets in each of
+        # B subspaces), the candidates' 128-byte records, the retrieved K and
+        # V rows (2 x 256 B) and the top-k written (index + estimate).  Per
+        # KV head: the bucket offsets of every chunk and the window's K/V rows.
+        "decode": b * hq * (2 * w["rho"] * w["n_sub"] * Nmean / 256 + C * 128 + keff * 4 * d + keff * 8)
+                  + b * hkv * (nch * 16 * 264 * 4 + nwin * 4 * d),
     }
     dom = max(kernels, key=lambda k: kernels[k]["us_per_launch"] * kernels[k]["launches"])
     peak, peak_src = hbm_peak()
@@ -313,8 +312,6 @@ def run_ours(args, rank, world):
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom),
                 "algorithmic_bytes": alg[dom]}
-    retr_bytes = alg["rerank"] + b * hq * (w["rho"] * w["n_sub"]) * (Nmean / 256) * 2
-    retrieve_frac = retr_bytes / (us_retrieve * 1e-6) / 1e9 / peak
 
     # end to end through the public API with host buffers
     L0 = layers[0]
@@ -384,8 +381,7 @@ def run_ours(args, rank, world):
                          f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"},
         "us_per_decode_step": 1e3 * ms / args.steps,
         "us_per_decode_step_eager": 1e3 * ms_eager / args.steps,
-        "us_retrieve": us_retrieve, "us_attend": us_attend, "us_append": us_append,
-        "retrieve_hbm_frac": round(retrieve_frac, 4),
+        "us_decode_kernel": us_decode, "us_append": us_append,
         "recall_at_k": recall,
         "kernels": kernels,
         "roofline": roof,
@@ -477,6 +473,8 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=60)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="only set up the workload and run warmup + steps decode steps, untimed (for ncu)")
     args = ap.parse_args()
     if args.oracle_sample:
         oracle_sample(args)
@@ -507,11 +505,12 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl")
     cb = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.profile_case:
         cb = cpu_baseline(args)  # before any CUDA work in this process
     res = run_ours(args, rank, world)
     if rank == 0:
-        res["cpu_baseline"] = cb
+        if not args.profile_case:
+            res["cpu_baseline"] = cb
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as tdist

@@ -157,7 +157,7 @@ paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtyp
  * process exits) instead of in the context, and the call allocates nothing.
  * The pages have no counterpart; this is a property of this library.
  * Limit: batch x n_q_heads x splits <= 1024, with splits =
- * ceil((tokens in Sink, Local and Update Buffer + k_eff) / 128), and
+ * ceil((tokens in Sink, Local and Update Buffer + k_eff) / 64), and
  * batch x n_q_heads <= 1024; larger calls return PARIS_EINVAL.  The first call
  * on a device looks up the area's device address once (cudaGetSymbolAddress
  * with that device current); make that first call before any stream capture.
@@ -167,12 +167,17 @@ paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtyp
 paris_status paris_sparse_attend_noalloc(paris_ctx* ctx, const void* q, paris_dtype dtype,
                                          const int32_t* topk_idx, void* out_bf16, void* stream);
 
-/* One decode step: exactly paris_append_decode(k, v), then
- * paris_retrieve(q, ...), then paris_sparse_attend(q, topk_idx, out), with the
- * same arguments and results, in six kernels instead of seven: the append
- * rides in the query-preparation kernel unless it fills the Update Buffer (then the flush
- * and index rebuild run first).  k, v: device, kv_dtype, [batch][Hkv][d];
- * q: device, q_dtype, [batch][Hq][d]; outputs as in the two calls.          */
+/* One decode step: paris_append_decode(k, v), then paris_retrieve(q, ...),
+ * then paris_sparse_attend(q, topk_idx, out), with the same arguments.  The
+ * top-k positions, their estimates and k_eff are bit for bit those of the
+ * three calls; the attention output is the same sum in another float32
+ * order (here it runs inside the retrieval kernel, its rows split over the
+ * blocks that serve each query head).  One kernel launch when the append
+ * does not fill the Update Buffer: the step's own token is read from k/v
+ * where the attention needs it and written to the cache at the end of the
+ * kernel.  When it does, the append, flush and index rebuild run first.
+ * k, v: device, kv_dtype, [batch][Hkv][d]; q: device, q_dtype,
+ * [batch][Hq][d]; outputs as in the three calls.                           */
 paris_status paris_decode_step(paris_ctx* ctx, const void* k, const void* v, paris_dtype kv_dtype, const void* q,
                                paris_dtype q_dtype, int32_t* topk_idx, float* topk_score, void* out_bf16,
                                int64_t* k_eff, void* stream);
@@ -221,15 +226,12 @@ typedef enum {
   PARIS_KERNEL_ENCODE = 1,      /* prefill: SRHT, bucket ids, codes, w                   */
   PARIS_KERNEL_BUILD_INDEX = 2, /* per-chunk inverted bucket index                       */
   PARIS_KERNEL_APPEND = 3,      /* standalone decode append (store + encode one token)   */
-  PARIS_KERNEL_QPREP = 4,       /* query rotation, norms, top-rho centroids (and the fused
-                                   append of a decode step)                             */
-  PARIS_KERNEL_VOTE = 5,        /* collision votes over the inverted bucket index        */
-  PARIS_KERNEL_COMPACT = 6,     /* candidate selection (ordered compaction)              */
-  PARIS_KERNEL_RERANK = 7,      /* RSQ-IP estimates of the candidates                    */
-  PARIS_KERNEL_TOPK = 8,        /* top-k of the estimates                                */
-  PARIS_KERNEL_ATTEND = 9,      /* sparse attention and the merge of its splits          */
-  PARIS_KERNEL_FILL = 10,       /* empty-result fill                                     */
-  PARIS_KERNEL_COUNT = 11
+  PARIS_KERNEL_DECODE = 4,      /* fused retrieval: query preparation, votes, candidates,
+                                   rerank, top-k; in a decode step also the sparse
+                                   attention and the append of the step's token      */
+  PARIS_KERNEL_ATTEND = 5,      /* standalone sparse attention and the merge of its splits */
+  PARIS_KERNEL_FILL = 6,        /* empty-result fill                                     */
+  PARIS_KERNEL_COUNT = 7
 } paris_kernel;
 
 /* Cumulative kernel launches of this context since paris_create, per

@@ -206,7 +206,6 @@ RetrieveArgs retrieve_args(paris_ctx* c, int32_t* topk_idx, float* topk_score) {
   a.cand_idx = c->cand_idx;
   a.cand_est = c->cand_est;
   a.cmax = c->cmax;
-  a.counter_select = c->counters;
   a.trace = c->tracing ? c->trace : nullptr;
   a.topk_idx = topk_idx;
   a.topk_score = topk_score;
@@ -258,28 +257,52 @@ bool append_flushes(const paris_ctx* c) {
   return c->n_local + c->n_buf + 1 > c->s.local;
 }
 
+// The step's own token, when the decode kernel appends it.
+struct NewToken {
+  const void* k;
+  const void* v;
+  paris_dtype dtype;
+  int64_t pos;
+};
+
+// Retrieval (and, with out != nullptr, the sparse attention) of the current
+// zones.  With `tok`, the zone bookkeeping already counts the token and the
+// decode kernel writes it into the cache.  An empty Retrieval zone gives the
+// (-1, -inf) fill; the attention then runs as its own kernel.
 paris_status retrieve_launch(paris_ctx* c, const void* q, paris_dtype dtype, int32_t* topk_idx, float* topk_score,
-                             int64_t* k_eff, const AppendFuse* fuse, cudaStream_t s) {
+                             int64_t* k_eff, const NewToken* tok, void* out, cudaStream_t s) {
   const int64_t nq = (int64_t)c->s.batch * c->s.hq;
   if (c->N == 0) {
     *k_eff = 0;
-    if (fuse) {
-      const AppendFuse f = *fuse;
+    if (tok) {
+      const NewToken f = *tok;
       PARIS_CUDA(c, launch(c, PARIS_KERNEL_APPEND, s, [&] {
                    return launch_append(f.k, f.v, f.dtype, f.pos, c->s, c->kv, c->t, c->sm, c->rp, s);
                  }));
     }
     PARIS_CUDA(c, launch(c, PARIS_KERNEL_FILL, s,
                          [&] { return launch_fill_empty(topk_idx, topk_score, nq * c->cfg.topk, s); }));
+    if (out) {
+      const AttendArgs a = attend_args(c, topk_idx, out);
+      PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTEND, s, [&] { return launch_attend(q, dtype, a, s); }));
+    }
     return PARIS_OK;
   }
-  const RetrieveArgs a = retrieve_args(c, topk_idx, topk_score);
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_QPREP, s, [&] { return launch_qprep(q, dtype, a, fuse, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_VOTE, s, [&] { return launch_vote(a, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_COMPACT, s, [&] { return launch_compact(a, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_RERANK, s, [&] { return launch_rerank(a, s); }));
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_TOPK, s, [&] { return launch_topk(a, s); }));
-  *k_eff = a.k_eff;
+  DecodeLaunch L;
+  L.ra = retrieve_args(c, topk_idx, topk_score);
+  L.kv = c->kv;
+  L.nsink = std::min<int64_t>(c->s.sink, c->T);
+  L.nwin = L.nsink + c->n_local + c->n_buf;
+  L.q = q;
+  L.qdtype = dtype;
+  L.k_new = tok ? tok->k : nullptr;
+  L.v_new = tok ? tok->v : nullptr;
+  L.kvdtype = tok ? tok->dtype : PARIS_BF16;
+  L.new_pos = tok ? tok->pos : -1;
+  L.status = c->status;
+  L.out = static_cast<__nv_bfloat16*>(out);
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_DECODE, s, [&] { return launch_decode(L, s); }));
+  *k_eff = L.ra.k_eff;
   return PARIS_OK;
 }
 
@@ -467,7 +490,7 @@ paris_status paris_retrieve(paris_ctx* c, const void* q, paris_dtype dtype, int3
   paris_status st = check_dtype(c, dtype);
   if (st != PARIS_OK) return st;
   if (!q || !topk_idx || !k_eff) return fail(c, PARIS_EINVAL, "q, topk_idx and k_eff must not be NULL");
-  return retrieve_launch(c, q, dtype, topk_idx, topk_score, k_eff, nullptr, static_cast<cudaStream_t>(stream));
+  return retrieve_launch(c, q, dtype, topk_idx, topk_score, k_eff, nullptr, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 paris_status paris_sparse_attend(paris_ctx* c, const void* q, paris_dtype dtype, const int32_t* topk_idx,
@@ -494,24 +517,15 @@ paris_status paris_decode_step(paris_ctx* c, const void* k, const void* v, paris
   if (c->T + 1 > c->cfg.max_ctx) return fail(c, PARIS_ECAPACITY, "cache is full (max_ctx = %d)", c->cfg.max_ctx);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (append_flushes(c)) {
+    // the flush re-indexes chunks the retrieval reads: append first
     st = paris_append_decode(c, k, v, kv_dtype, stream);
     if (st != PARIS_OK) return st;
-    st = retrieve_launch(c, q, q_dtype, topk_idx, topk_score, k_eff, nullptr, s);
-  } else {
-    AppendFuse f;
-    f.k = k;
-    f.v = v;
-    f.dtype = kv_dtype;
-    f.pos = c->T;
-    f.kv = c->kv;
-    int64_t n_old;
-    zones_append(c, &n_old);
-    st = retrieve_launch(c, q, q_dtype, topk_idx, topk_score, k_eff, &f, s);
+    return retrieve_launch(c, q, q_dtype, topk_idx, topk_score, k_eff, nullptr, out_bf16, s);
   }
-  if (st != PARIS_OK) return st;
-  const AttendArgs a = attend_args(c, topk_idx, out_bf16);
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTEND, s, [&] { return launch_attend(q, q_dtype, a, s); }));
-  return PARIS_OK;
+  const NewToken tok{k, v, kv_dtype, c->T};
+  int64_t n_old;
+  zones_append(c, &n_old);
+  return retrieve_launch(c, q, q_dtype, topk_idx, topk_score, k_eff, &tok, out_bf16, s);
 }
 
 paris_status paris_get_state(const paris_ctx* c, paris_state* out) {

@@ -91,21 +91,28 @@ struct RetrieveArgs {
   int32_t* cand_idx;  // [batch*Hq][cmax]
   float* cand_est;
   int64_t cmax;
-  uint32_t* counter_select;  // [batch*Hq] rerank blocks finished, reset by the last one
   uint64_t* trace;           // phase timestamps (nullptr: off)
   // outputs
   int32_t* topk_idx;  // [batch*Hq][k]
   float* topk_score;  // may be null
 };
 
-// A decode-token append fused into the vote kernel (one warp per
-// (sequence, KV head), in the tiles of chunk 0).
-struct AppendFuse {
-  const void* k;
-  const void* v;
-  int dtype;
-  int64_t pos;
+// One launch of the fused decode kernel: retrieval for every (sequence,
+// query head), optionally the sparse attention (out != nullptr) and the
+// append of the step's own token (k_new != nullptr; the zone bookkeeping
+// already counts it).
+struct DecodeLaunch {
+  RetrieveArgs ra;
   KvStore kv;
+  int64_t nsink, nwin;  // attention window rows: Sink, then Local + Buffer
+  const void* q;
+  int qdtype;
+  const void* k_new;
+  const void* v_new;
+  int kvdtype;
+  int64_t new_pos;
+  uint32_t* status;
+  __nv_bfloat16* out;
 };
 
 // Launch `kern` so that it may start while the preceding kernel of the
@@ -126,12 +133,8 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
   return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
 }
 
-cudaError_t launch_qprep(const void* q, int dtype, const RetrieveArgs& a, const AppendFuse* ap, cudaStream_t st);
-size_t vote_smem_bytes(int rho);
-cudaError_t launch_vote(const RetrieveArgs& a, cudaStream_t st);
-cudaError_t launch_compact(const RetrieveArgs& a, cudaStream_t st);
-cudaError_t launch_rerank(const RetrieveArgs& a, cudaStream_t st);
-cudaError_t launch_topk(const RetrieveArgs& a, cudaStream_t st);
+int decode_cluster_size(int nchunk_active);
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st);
 cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_t st);
 
 // ---- sparse attention ---------------------------------------------------
@@ -157,15 +160,16 @@ constexpr uint32_t kStatusBadIndex = 1u;
 // Phase-trace slots (block (0, 0) of each kernel, and the reducing block of
 // query head 0).
 constexpr int kTraceSlots = 64;
-constexpr int kTraceBlocks = 4096;   // per-block stamps (start, after wait, -, end) of up to 8 kernels
+constexpr int kTraceBlocks = 4096;   // per-block stamps: 4 per block and trace row
 constexpr int kTraceKernels = 8;
 constexpr int64_t kTraceWords = kTraceSlots + (int64_t)kTraceKernels * kTraceBlocks * 4;
-enum TraceKernel { kTkQprep = 0, kTkVote, kTkCompact, kTkRerank, kTkTopk, kTkAttend };
+// trace rows: the fused decode kernel uses three (start, after wait,
+// prepared, voted | compacted, reranked, top-k out, after barrier |
+// attention tiles, merged, -, end); the standalone attention one
+enum TraceKernel { kTkDecode0 = 0, kTkDecode1, kTkDecode2, kTkAttend };
 enum TraceSlot {
-  kTrVote0 = 0, kTrVote1, kTrVote2, kTrVote3, kTrVote4,
-  kTrCompact0 = 8, kTrCompact1, kTrCompact2,
-  kTrRerank0 = 16, kTrRerank1, kTrRerank2, kTrRerank3,
-  kTrTopk0 = 20, kTrTopk1, kTrTopk2, kTrTopk3, kTrTopk4, kTrTopk5,
+  kTrDecode0 = 0, kTrDecode1, kTrDecode2, kTrDecode3, kTrDecode4, kTrDecode5, kTrDecode6,
+  kTrDecodeFine = 8,  // 8 .. 28: steps inside the vote and top-k phases
   kTrAttend0 = 32, kTrAttend1, kTrAttend2, kTrAttend3, kTrAttend4
 };
 

@@ -49,7 +49,7 @@ _SIGNATURES = {
     "paris_profile_end": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
 }
 
-KERNELS = ["place_kv", "encode", "build_index", "append", "qprep", "vote", "compact", "rerank", "topk", "attend", "fill"]
+KERNELS = ["place_kv", "encode", "build_index", "append", "decode", "attend", "fill"]
 
 
 class paris_config(ctypes.Structure):

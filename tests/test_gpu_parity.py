@@ -195,8 +195,10 @@ def test_retrieval_zone_in_host_memory_matches_hbm():
 
 
 def test_decode_step_equals_the_three_calls():
-    """paris_decode_step (append fused into the vote kernel) gives exactly
-    what append + retrieve + sparse_attend give, across flushes."""
+    """paris_decode_step (one fused kernel unless the append flushes) gives
+    the top-k and estimates of append + retrieve + sparse_attend bit for bit,
+    and their attention output up to float32 summation order, across
+    flushes."""
     kw = dict(seed=24, batch=2, n_kv_heads=2, n_q_heads=4, sink=16, local=64, update_buf=16, topk=64,
               cand_bp=500, rho=4)
     a = g.make_case(16 + 20000 + 64, **kw)
@@ -217,7 +219,8 @@ def test_decode_step_equals_the_three_calls():
         kb = b.ctx.paris_decode_step(kd, vd, qd, ib, sb, ob)
         torch.cuda.synchronize()
         assert ka == kb
-        assert torch.equal(ia, ib) and torch.equal(sa, sb) and torch.equal(oa, ob), t
+        assert torch.equal(ia, ib) and torch.equal(sa, sb), t
+        torch.testing.assert_close(ob.float(), oa.float(), rtol=0, atol=g.ATTN_ATOL)
         g.append(a, k, v, device=False)  # host-side mirror of what both contexts now hold
         if t % 20 == 19:
             g.check_state(a)
