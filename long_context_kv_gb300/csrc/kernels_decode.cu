@@ -8,26 +8,28 @@
 // Update Buffer and the retrieved tokens ("Problem definition",
 // "Sliding-window update mechanism").
 //
-// One thread-block cluster of CS <= 8 blocks per (sequence, query head);
-// block r of the cluster owns a contiguous range of index chunks of the
-// Retrieval zone, so block order is position order.  The steps that need
-// the whole query head exchange small tables through distributed shared
-// memory between cluster barriers (every block reaches every barrier):
+// One thread-block cluster of CS <= 4 blocks (1024 threads, one per SM) per
+// (sequence, query head); block r owns a contiguous range of index chunks
+// of the Retrieval zone, so block order is position order.  Cluster
+// barriers separate the steps that need the whole query head (every block
+// reaches every barrier):
 //   1. each block: q~, ||q|| and the hot centroids (redundantly), the votes
 //      of its chunks and their histogram;
-//   2. barrier; every block sums the cluster's histograms, finds the vote
-//      threshold and writes its candidates (positions ascending) at their
-//      place in the query head's candidate list;
-//   3. each block: estimates of its candidates;
-//   4. top-k: four 8-bit radix passes over the estimates' order keys, one
-//      barrier each; every block derives the same k-th key and, from every
-//      block's counts, its own output offset;
+//   2. barrier; every block sums the cluster's histograms (distributed
+//      shared memory), finds the vote threshold and writes its candidates
+//      (positions ascending) at their place in the query head's list;
+//   3. barrier; block r computes the estimates of the slice
+//      [C r / CS, C (r + 1) / CS) of that list;
+//   4. barrier; every block finds the k-th best estimate over all C (radix
+//      select in shared memory) and writes the selected entries of its
+//      slice at their place in the top-k;
 //   5. barrier; the rows (window + top-k) are split evenly over the blocks;
 //      each block stages its rows through a four-stage asynchronous-copy
-//      pipeline with an online softmax; barrier; block 0 merges.
+//      pipeline, every warp with its own online softmax; barrier; block 0
+//      merges the blocks.
 // A decode token appended in the same step is read from the caller's k/v
-// where the attention needs it, and written to the cache by one block at
-// the very end (nothing in this launch reads the slots it writes).
+// where the attention needs it, and written to the cache by one warp while
+// the query is prepared (nothing in this launch reads the slots it writes).
 #include <float.h>
 
 #include "paris_device.cuh"
@@ -35,34 +37,39 @@
 namespace paris {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kClusterMax = 8;
-constexpr int kListCap = 2048;      // candidates per block kept in shared memory; the rest re-read from global
-constexpr int kTile = 32;           // attention rows per pipeline stage
+constexpr int kClusterMax = 4;
+constexpr int kVoteSlots = 2;       // chunks per block whose votes stay in shared memory
+constexpr int kListCap = 4096;      // candidates of the block's slice kept in shared memory
+constexpr int kTile = 64;           // attention rows per pipeline stage
 constexpr int kStages = 4;
 constexpr int kKStride = kDim + 8;  // bf16 per staged row: 272 B keeps 16-byte reads conflict-free
-constexpr int kSelCap = 16384;      // candidates whose keys block 0 stages for the top-k
+constexpr int kSelCap = 16384;      // candidates whose keys the top-k stages in shared memory
 constexpr int kSelBins = 2048;      // 11-bit radix digits
-static_assert(kWarps == kSub, "warp b prepares subspace b");
 static_assert(kTile * 16 == kThreads, "16 threads per staged row");
+static_assert(2 * kWarps == kTile, "two rows of a tile per warp");
+static_assert(kChunk / kThreads == 16, "one 16-byte vote vector per thread and chunk");
+static_assert(2 * kThreads == kSelBins, "two radix digits per thread");
 
-// byte offsets inside the phase-shared region
-constexpr int kUKeys = 0;                                   // u32 [kSelCap]: top-k order keys (block 0)
-constexpr int kUVotes = 0;                                  // u8 [kChunk]: votes of the block's last chunk
-constexpr int kUOffs = kUVotes + kChunk;                    // u32 [kSub][kOffStride]
-constexpr int kUSelHist = kUKeys + kSelCap * 4;             // u32 [kSelBins]
-constexpr int kUListPos = kUSelHist + kSelBins * 4;         // i32 [kListCap]: the block's candidate slice
-constexpr int kUListEst = kUListPos + kListCap * 4;         // f32 [kListCap]: its estimates
-constexpr int kUVoteEnd = kUListEst + kListCap * 4;
-constexpr int kUStageK = 0;                                 // bf16 [kStages][kTile][kKStride]
+// byte offsets inside the phase-shared dynamic region
+constexpr int kUVotes = 0;                                    // u8 [kVoteSlots][kChunk]
+constexpr int kUOffs = kUVotes + kVoteSlots * kChunk;         // u32 [kVoteSlots][kSub][kOffStride]
+constexpr int kUHot = kUOffs + kVoteSlots * kSub * kOffStride * 4;  // hot lists: hv[nhot], then per list
+                                                              // (G x nhot) hbeg, hwt and hpre (+1)
+constexpr int kURecSlots = 0;                                 // 128 B per thread: a candidate record being gathered
+constexpr int kUKeys = 0;                                     // u32 [kSelCap]: top-k order keys
+constexpr int kUSelHist = kUKeys + kSelCap * 4;               // u32 [kSelBins]
+constexpr int kUStageK = 0;                                   // bf16 [kStages][kTile][kKStride]
 constexpr int kUStageV = kStages * kTile * kKStride * 2;
 constexpr int kUAttnEnd = 2 * kStages * kTile * kKStride * 2;
-constexpr int kUBytes = kUVoteEnd > kUAttnEnd ? kUVoteEnd : kUAttnEnd;
-static_assert(kUOffs + kSub * kOffStride * 4 <= kUSelHist, "vote tables inside the key area");
-static_assert(kUAttnEnd <= kUListPos, "attention stages below the candidate slice");
-
-__host__ __device__ constexpr int hot_bytes(int nhot) { return (16 * nhot + 4 + 15) & ~15; }
+constexpr int kUListPos = kUAttnEnd;                          // i32 [kListCap]: the block's candidate slice
+constexpr int kUListEst = kUListPos + kListCap * 4;           // f32 [kListCap]: its estimates
+constexpr int kUBytes = kUListEst + kListCap * 4;
+static_assert(kUHot + (4 * kSub * kCentroids + 1) * 4 <= kUListPos, "hot lists (G = 1) below the candidate slice");
+static_assert(kUHot + (7 * 1024 + 1) * 4 <= kUListPos, "hot lists (G = 2) below the candidate slice");
+static_assert(kUSelHist + kSelBins * 4 <= kUListPos, "top-k tables below the candidate slice");
+static_assert(kURecSlots + kThreads * kRecBytes <= kUListPos, "record slots below the candidate slice");
 
 struct DecodeArgs {
   Shape s;
@@ -103,6 +110,7 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 
 // Cluster barrier: every thread of every block of the cluster arrives; the
 // writes before it (shared and global) are visible to the cluster after it.
@@ -119,6 +127,23 @@ __device__ __forceinline__ uint32_t dsmem_u32(const void* p, uint32_t rank) {
   return v;
 }
 
+// Per byte of x: 0x80 where the byte is nonzero / equals the byte of c4 /
+// exceeds it (unsigned); 0 elsewhere.
+__device__ __forceinline__ uint32_t bytes_nonzero(uint32_t x) {
+  return (((x & 0x7f7f7f7fu) + 0x7f7f7f7fu) | x) & 0x80808080u;
+}
+__device__ __forceinline__ uint32_t bytes_eq(uint32_t x, uint32_t c4) { return ~bytes_nonzero(x ^ c4) & 0x80808080u; }
+__device__ __forceinline__ uint32_t bytes_gt(uint32_t x, uint32_t c4) {
+  // per byte (x | 0x80) - (c & 0x7f) never borrows; its high bit is [x_low7 >= c_low7]
+  const uint32_t d = (x | 0x80808080u) - (c4 & 0x7f7f7f7fu);
+  const uint32_t ge = ((x & ~c4) | (~(x ^ c4) & d)) & 0x80808080u;
+  return ge & ~bytes_eq(x, c4);
+}
+// 0x80 in each of the first n (clamped to 0..4) bytes.
+__device__ __forceinline__ uint32_t first_bytes(int n) {
+  return n >= 4 ? 0x80808080u : n <= 0 ? 0u : (0x80808080u >> (8 * (4 - n)));
+}
+
 // Estimate of one candidate from its 128-byte record, float32 in this order:
 //   acc = 0; for b: dot = 0; for j: dot = dot + v_{b,j} q~_{b,j};
 //   acc = acc + w_b dot;   est = ||q|| acc,
@@ -132,60 +157,45 @@ __device__ __forceinline__ float estimate(const uint4 (&x)[8], const float* tq, 
     const uint32_t cw = (b & 3) == 0 ? cq.x : (b & 3) == 1 ? cq.y : (b & 3) == 2 ? cq.z : cq.w;
     const uint4 wq = x[4 + (b >> 2)];
     const float w = __uint_as_float((b & 3) == 0 ? wq.x : (b & 3) == 1 ? wq.y : (b & 3) == 2 ? wq.z : wq.w);
+    // nibble j times 4 (a byte offset into its 16-entry row): even j in the
+    // bytes of lo4, odd j in the bytes of hi4
+    const uint32_t lo4 = (cw << 2) & 0x3c3c3c3cu, hi4 = (cw >> 2) & 0x3c3c3c3cu;
+    const char* row = reinterpret_cast<const char*>(tq + b * kM * 16);
     float dot = 0.f;
 #pragma unroll
-    for (int j = 0; j < kM; ++j) dot = __fadd_rn(dot, tq[(b * kM + j) * 16 + ((cw >> (4 * j)) & 15u)]);
+    for (int j = 0; j < kM; ++j) {
+      const uint32_t off = __byte_perm((j & 1) ? hi4 : lo4, 0u, 0x4440u + (j >> 1));
+      dot = __fadd_rn(dot, *reinterpret_cast<const float*>(row + j * 64 + off));
+    }
     acc = __fadd_rn(acc, __fmul_rn(w, dot));
   }
   return __fmul_rn(qn, acc);
 }
 
-// Per byte of x: 0x80 where the byte equals the byte of c4 / exceeds it
-// (unsigned), 0 elsewhere.
-__device__ __forceinline__ uint32_t bytes_eq(uint32_t x, uint32_t c4) {
-  const uint32_t y = x ^ c4;
-  const uint32_t t = ((y & 0x7f7f7f7fu) + 0x7f7f7f7fu) | y;  // high bit set in every nonzero byte
-  return ~t & 0x80808080u;
-}
-__device__ __forceinline__ uint32_t bytes_gt(uint32_t x, uint32_t c4) {
-  // per byte (x | 0x80) - (c & 0x7f) never borrows; its high bit is [x_low7 >= c_low7]
-  const uint32_t d = (x | 0x80808080u) - (c4 & 0x7f7f7f7fu);
-  const uint32_t ge = ((x & ~c4) | (~(x ^ c4) & d)) & 0x80808080u;
-  return ge & ~bytes_eq(x, c4);
-}
-
-// Block 0 of a query head's cluster: the k_eff-th largest order key over all
-// C estimates (radix select, 11-bit digits below the bits all keys share),
-// then, for every block's slice [C r / cs, C (r + 1) / cs), where its
-// selected entries start in the output and how many of its keys equal to
-// the k-th key it keeps (those equal keys go to the lowest positions, which
-// are the lowest candidate indices).  Writes sel[r] = (offset, kept) and
-// sel[kClusterMax][0] = the k-th key.  All threads of the block call it.
-__device__ __noinline__ void select_kth(const int64_t C, const int64_t k_eff, const float* est, int cs,
-                                        uint8_t* U, uint32_t* tmp, uint32_t (*sel)[2]) {
+// The k_eff-th largest order key over the C estimates of a query head
+// (radix select, 11-bit digits below the bits all keys share; keys staged
+// in shared memory when C <= kSelCap).  Returns the key; *remaining_out
+// receives how many keys equal to it belong to the top k_eff.  All threads
+// of the block call it and get the same results.
+__device__ __noinline__ uint32_t select_kth(const int64_t C, const int64_t k_eff, const float* est, uint8_t* U,
+                                            uint32_t* tmp, uint32_t* remaining_out) {
   __shared__ uint32_t s_digit, s_skip;
-  __shared__ uint32_t cnt_gt[kClusterMax], cnt_eq[kClusterMax];
-  __shared__ int64_t bounds[kClusterMax + 1];
+  __shared__ uint32_t s_and[kWarps], s_or[kWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* keys = reinterpret_cast<uint32_t*>(U + kUKeys);
   uint32_t* hist = reinterpret_cast<uint32_t*>(U + kUSelHist);
   const bool staged = C <= kSelCap;
-  auto key_at = [&](int64_t i) { return staged ? keys[i] : order_key(__ldcg(est + i)); };
-  if (tid < kClusterMax) {
-    cnt_gt[tid] = 0;
-    cnt_eq[tid] = 0;
-  }
-  if (tid <= cs) bounds[tid] = C * tid / cs;
+  const int n = (int)C;  // at most the Retrieval-zone capacity
   // keys (8 loads in flight per thread), and the bits every key shares
   uint32_t kand = 0xffffffffu, kor = 0u;
-  for (int64_t i0 = tid; i0 < C; i0 += 8 * kThreads) {
+  for (int i0 = tid; i0 < n; i0 += 8 * kThreads) {
     float v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < C ? __ldcg(est + i0 + u * kThreads) : 0.f;
+    for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < n ? __ldcg(est + i0 + u * kThreads) : 0.f;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int64_t i = i0 + u * kThreads;
-      if (i < C) {
+      const int i = i0 + u * kThreads;
+      if (i < n) {
         const uint32_t k = order_key(v[u]);
         if (staged) keys[i] = k;
         kand &= k;
@@ -196,18 +206,17 @@ __device__ __noinline__ void select_kth(const int64_t C, const int64_t k_eff, co
   kand = __reduce_and_sync(kFull, kand);
   kor = __reduce_or_sync(kFull, kor);
   if (lane == 0) {
-    tmp[warp] = kand;
-    tmp[16 + warp] = kor;
+    s_and[warp] = kand;
+    s_or[warp] = kor;
   }
   __syncthreads();
   kand = 0xffffffffu;
   kor = 0u;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    kand &= tmp[w];
-    kor |= tmp[16 + w];
+    kand &= s_and[w];
+    kor |= s_or[w];
   }
-  __syncthreads();
   const uint32_t diff = kand ^ kor;
   uint32_t prefix = kand, remaining = (uint32_t)k_eff;
   if (diff != 0) {
@@ -219,31 +228,21 @@ __device__ __noinline__ void select_kth(const int64_t C, const int64_t k_eff, co
       const uint32_t dmask = (1u << nb) - 1u;
       for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
       __syncthreads();
-      for (int64_t i = tid; i < C; i += kThreads) {
-        const uint32_t k = key_at(i);
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t k = staged ? keys[i] : order_key(__ldcg(est + i));
         if ((k & mask) == prefix) atomicAdd(&hist[(k >> lo) & dmask], 1u);
       }
       __syncthreads();
-      // thread t owns digits kSelBins-1-4t .. kSelBins-4-4t, scanned from the top
-      uint32_t c4[4], sum4 = 0;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        c4[u] = hist[kSelBins - 1 - 4 * tid - u];
-        sum4 += c4[u];
-      }
+      // thread t owns digits kSelBins-1-2t and kSelBins-2-2t, scanned from the top
+      const uint32_t c0 = hist[kSelBins - 1 - 2 * tid], c1 = hist[kSelBins - 2 - 2 * tid];
       uint32_t tot;
-      const uint32_t exc = block_excl_scan(sum4, tmp, &tot);
-      if (exc < remaining && exc + sum4 >= remaining) {
-        uint32_t run = exc;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (run + c4[u] >= remaining) {
-            s_digit = (uint32_t)(kSelBins - 1 - 4 * tid - u);
-            s_skip = run;
-            break;
-          }
-          run += c4[u];
-        }
+      const uint32_t exc = block_excl_scan(c0 + c1, tmp, &tot);
+      if (exc < remaining && exc + c0 >= remaining) {
+        s_digit = (uint32_t)(kSelBins - 1 - 2 * tid);
+        s_skip = exc;
+      } else if (exc + c0 < remaining && exc + c0 + c1 >= remaining) {
+        s_digit = (uint32_t)(kSelBins - 2 - 2 * tid);
+        s_skip = exc + c0;
       }
       __syncthreads();
       prefix |= s_digit << lo;
@@ -253,65 +252,30 @@ __device__ __noinline__ void select_kth(const int64_t C, const int64_t k_eff, co
       __syncthreads();
     }
   }
-  // per slice: keys above / equal to the k-th key
-  for (int64_t i0 = 0; i0 < C; i0 += kThreads) {
-    const int64_t i = i0 + tid;
-    int owner = 0;
-    uint32_t g = 0, e = 0;
-    if (i < C) {
-#pragma unroll
-      for (int q = 1; q < kClusterMax; ++q) owner += (q < cs && i >= bounds[q]) ? 1 : 0;
-      const uint32_t k = key_at(i);
-      g = k > prefix ? 1u : 0u;
-      e = k == prefix ? 1u : 0u;
-    }
-    if (__all_sync(kFull, owner == __shfl_sync(kFull, owner, 0))) {
-      const uint32_t gs = __reduce_add_sync(kFull, g), es = __reduce_add_sync(kFull, e);
-      if (lane == 0) {
-        if (gs) atomicAdd(&cnt_gt[owner], gs);
-        if (es) atomicAdd(&cnt_eq[owner], es);
-      }
-    } else {
-      if (g) atomicAdd(&cnt_gt[owner], 1u);
-      if (e) atomicAdd(&cnt_eq[owner], 1u);
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t rem = remaining, off = 0;
-    for (int q = 0; q < cs; ++q) {
-      const uint32_t et = min(cnt_eq[q], rem);
-      rem -= et;
-      sel[q][0] = off;
-      sel[q][1] = et;
-      off += cnt_gt[q] + et;
-    }
-    sel[kClusterMax][0] = prefix;
-  }
+  *remaining_out = remaining;
+  return prefix;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ float qs[kDim], zs[kDim], qts[kDim];
   __shared__ float tq[kDim * 16];
-  __shared__ uint32_t hist[kMaxBins];                  // read by the cluster
-  __shared__ __align__(16) float part[kPartStride];    // read by block 0
+  __shared__ uint32_t hist[kMaxBins];                // read by the cluster
+  __shared__ __align__(16) float part[kPartStride];  // read by block 0
   __shared__ uint32_t tot[kMaxBins];
   __shared__ uint32_t tmp[33];
-  __shared__ uint32_t red[64];
-  __shared__ uint32_t sel_info[kClusterMax + 1][2];      // block 0: per block (output offset, equal keys kept); k-th key
+  __shared__ uint32_t red[2 * kWarps];
   __shared__ uint8_t rvalid[kStages][kTile];
   __shared__ float s_qn;
   __shared__ int s_T;
   __shared__ int64_t s_quota;
-  extern __shared__ __align__(16) uint8_t dyn[];
+  extern __shared__ __align__(16) uint8_t U[];
 
   const int nhot = kSub * a.rho;
-  uint32_t* hv = reinterpret_cast<uint32_t*>(dyn);  // hot entries: id | weight << 16 | subspace << 24
+  const int nlist = (nhot <= 1024 ? kVoteSlots : 1) * nhot;  // hot lists of a group of chunks
+  uint32_t* hv = reinterpret_cast<uint32_t*>(U + kUHot);  // hot entries: id | weight << 16 | subspace << 24
   uint32_t* hbeg = hv + nhot;
-  uint32_t* hwt = hbeg + nhot;
-  uint32_t* hpre = hwt + nhot;                       // nhot + 1
-  uint8_t* U = dyn + hot_bytes(nhot);
-  uint8_t* votes = U + kUVotes;
+  uint32_t* hwt = hbeg + nlist;
+  uint32_t* hpre = hwt + nlist;                            // nlist + 1
   uint32_t* offs = reinterpret_cast<uint32_t*>(U + kUOffs);
   int32_t* lpos = reinterpret_cast<int32_t*>(U + kUListPos);
   float* lest = reinterpret_cast<float*>(U + kUListEst);
@@ -327,18 +291,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
   trace_block(a.trace, kTkDecode0, 0);
 
   // ---- before the wait: cleared counters ---------------------------------
-  for (int i = tid; i < kChunk / 16; i += kThreads) reinterpret_cast<uint4*>(votes)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < kVoteSlots * kChunk / 16; i += kThreads)
+    reinterpret_cast<uint4*>(U + kUVotes)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < kMaxBins; i += kThreads) hist[i] = 0;
   pdl_wait();
   pdl_trigger();
   trace_block(a.trace, kTkDecode0, 1);
   trace_mark(tr, kTrDecode0);
 
-  auto prefetch_offsets = [&](int c) {
+  // offset tables of chunks c .. c + n - 1 (consecutive in memory)
+  auto prefetch_offsets = [&](int c, int n) {
     const uint32_t* og = a.t.off + ((sh * a.t.nchunk + c) * kSub) * kOffStride;
-    for (int i = tid; i < kSub * kOffStride / 4; i += kThreads) cp_async16(offs + 4 * i, og + 4 * i);
+    for (int i = tid; i < n * kSub * kOffStride / 4; i += kThreads) cp_async16(offs + 4 * i, og + 4 * i);
   };
-  if (c_lo < c_hi) prefetch_offsets(c_lo);
+  if (c_lo < c_hi) prefetch_offsets(c_lo, min(nhot <= 1024 ? kVoteSlots : 1, c_hi - c_lo));
 
   // ---- 1. query preparation ------------------------------------------------
   //   ||q|| = sqrt(sequential sum over the d inputs of q_j q_j);
@@ -357,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
     for (int i = 0; i < 4; ++i) zs[4 * lane + i] = y[i];
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kSub) {
     // the two sequential norm chains side by side in lanes 0 (q) and 1 (z)
     float acc = 0.f;
     if (lane < 2) {
@@ -384,8 +350,34 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
       s_qn = nq;
       if (r == 0) a.qnorm[sq] = nq;
     }
-  }
-  {
+  } else if (warp == kSub + 1) {
+    // the step's own token into the cache (nothing in this launch reads the
+    // ring slot or table row it writes: the attention takes it from k/v)
+    if (a.new_pos >= 0 && r == 0 && qh % a.s.g == 0)
+      append_token_warp(a.k_new, a.v_new, a.kvdtype, a.new_pos, sh, lane, a.s, a.kv, a.t, a.sm, a.rp);
+  } else if (warp > kSub + 1) {
+    // warm L2 with the window rows this block's attention will read
+    if (a.out != nullptr) {
+      const int64_t R = a.nwin + a.k_eff;
+      const int64_t w_lo = R * r / cs, w_hi = min64(R * (r + 1) / cs, a.nwin);
+      const int ring = a.s.local + a.s.ubuf;
+      const uint32_t nmod = ring > 0 ? (uint32_t)(a.N % ring) : 0u;
+      for (int64_t row = w_lo + (tid - (kSub + 2) * 32); row < w_hi; row += kThreads - (kSub + 2) * 32) {
+        int64_t slot = row;
+        if (row >= a.nsink) {
+          uint32_t x = nmod + (uint32_t)(row - a.nsink);
+          if (x >= (uint32_t)ring) x -= (uint32_t)ring;
+          slot = a.s.sink + x;
+        }
+        const __nv_bfloat16* kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
+        const __nv_bfloat16* vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
+        prefetch_l2(kp);
+        prefetch_l2(kp + 64);
+        prefetch_l2(vp);
+        prefetch_l2(vp + 64);
+      }
+    }
+  } else if (warp < kSub) {
     const int b = warp;
     // the lane's centroids are lane + 32 i: bits 0-4 of the id are the lane's,
     // so the first five terms of the sequential sum are shared, then the
@@ -445,31 +437,40 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
   // ---- 1b. collision votes of the block's chunks ---------------------------
   // Each key of a chunk sits in exactly one bucket per subspace, so walking
   // the lists of the hot buckets and adding their weights gives every key
-  // sum_b weight_b(id_{i,b}) (one byte per key, at most 255).
-  uint32_t nz_mine = 0;
+  // sum_b weight_b(id_{i,b}) (one byte per key, at most 255).  The block
+  // takes its chunks G at a time as one span of G x kChunk keys (G = 2, or
+  // 1 when the hot lists are long).
+  const int G = nhot <= 1024 ? kVoteSlots : 1;
+  uint8_t* span = U + kUVotes;
+  uint32_t c1 = 0, c2 = 0, c3 = 0, c4 = 0, nz_mine = 0;
   int64_t own_len = 0;
-  for (int c = c_lo; c < c_hi; ++c) {
-    const int64_t base = (int64_t)c * kChunk;
-    const int len = (int)min64(kChunk, a.N - base);
-    own_len += len;
+  for (int g0 = c_lo; g0 < c_hi; g0 += G) {
+    const int ng = min(G, c_hi - g0), nl = ng * nhot;
+    const int64_t gbase = (int64_t)g0 * kChunk;
+    const int glen = (int)min64((int64_t)ng * kChunk, a.N - gbase);
+    own_len += glen;
     cp_async_wait_all();
-    __syncthreads();  // the chunk's offsets (and, first time, the hot list) are in place
+    __syncthreads();  // the group's offsets (and, first time, the hot list) are in place
     {
-      constexpr int kHotPer = (kSub * kCentroids + kThreads - 1) / kThreads;
-      const int per = (nhot + kThreads - 1) / kThreads;
+      // list e2 = g * nhot + e: chunk g0 + g, hot entry e; its entries start
+      // at (g * B + b) * kChunk + offset in the group's entry lists
+      constexpr int kHotPer = (kSub * kCentroids + kThreads - 1) / kThreads;  // lists per thread: G nhot <= 4096
+      const int per = (nl + kThreads - 1) / kThreads;
       uint32_t lens[kHotPer];
       uint32_t my = 0;
 #pragma unroll
       for (int i = 0; i < kHotPer; ++i) {
-        const int e = tid * per + i;
+        const int e2 = tid * per + i;
         lens[i] = 0;
-        if (i < per && e < nhot) {
-          const uint32_t h = hv[e];
+        if (i < per && e2 < nl) {
+          const int g = e2 >= nhot ? 1 : 0;
+          const uint32_t h = hv[e2 - g * nhot];
           const uint32_t b = h >> 24, id = h & 0xffu;
-          const uint32_t beg = offs[b * kOffStride + id];
-          lens[i] = offs[b * kOffStride + id + 1] - beg;
-          hbeg[e] = b * kChunk + beg;
-          hwt[e] = (h >> 16) & 0xffu;
+          const uint32_t* og = offs + g * (kSub * kOffStride);
+          const uint32_t beg = og[b * kOffStride + id];
+          lens[i] = og[b * kOffStride + id + 1] - beg;
+          hbeg[e2] = ((uint32_t)g * kSub + b) * kChunk + beg;
+          hwt[e2] = ((h >> 16) & 0xffu) | ((uint32_t)g << 16);
         }
         my += lens[i];
       }
@@ -477,22 +478,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
       uint32_t run = block_excl_scan(my, tmp, &total);
 #pragma unroll
       for (int i = 0; i < kHotPer; ++i) {
-        const int e = tid * per + i;
-        if (i < per && e < nhot) hpre[e] = run;
+        const int e2 = tid * per + i;
+        if (i < per && e2 < nl) hpre[e2] = run;
         run += lens[i];
       }
-      if (tid == 0) hpre[nhot] = total;
+      if (tid == 0) hpre[nl] = total;
     }
     __syncthreads();
-    if (c == c_lo) trace_mark(tr, kTrDecodeFine + 0);
-    if (c + 1 < c_hi) prefetch_offsets(c + 1);  // the offsets are not read again for this chunk
-    const uint32_t total = hpre[nhot];
-    const uint16_t* ent = a.t.ent + ((sh * a.t.nchunk + c) * kSub) * (int64_t)kChunk;
+    if (g0 == c_lo) trace_mark(tr, kTrDecodeFine + 0);
+    if (g0 + G < c_hi) prefetch_offsets(g0 + G, min(G, c_hi - g0 - G));  // offsets not read again
+    const uint32_t total = hpre[nl];
+    const uint16_t* ent = a.t.ent + ((sh * a.t.nchunk + g0) * kSub) * (int64_t)kChunk;
     // thread t takes kWalk consecutive list entries: one search, then linear
     // steps; all kWalk loads in flight together
     constexpr int kWalk = 8;
     for (uint32_t f0 = kWalk * tid; f0 < total; f0 += kWalk * kThreads) {
-      int e = 0, hi = nhot - 1;  // last e with hpre[e] <= f0 (a non-empty list)
+      int e = 0, hi = nl - 1;  // last e with hpre[e] <= f0 (a non-empty list)
       while (e < hi) {
         const int mid = (e + hi + 1) >> 1;
         if (hpre[mid] <= f0) e = mid; else hi = mid - 1;
@@ -505,42 +506,55 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
         key[u] = 0;
         if (f < total) {
           while (hpre[e + 1] <= f) ++e;
-          key[u] = __ldg(ent + hbeg[e] + (f - hpre[e]));
-          wt[u] = hwt[e];
+          const uint32_t hw = hwt[e];
+          key[u] = __ldg(ent + hbeg[e] + (f - hpre[e])) + ((hw >> 16) << 14);  // key within the span
+          wt[u] = hw & 0xffu;
         }
       }
 #pragma unroll
       for (int u = 0; u < kWalk; ++u)
-        if (wt[u]) atomicAdd(reinterpret_cast<uint32_t*>(votes) + (key[u] >> 2), wt[u] << ((key[u] & 3) * 8));
+        if (wt[u]) atomicAdd(reinterpret_cast<uint32_t*>(span) + (key[u] >> 2), wt[u] << ((key[u] & 3) * 8));
     }
     __syncthreads();
-    if (c == c_lo) trace_mark(tr, kTrDecodeFine + 1);
-    // histogram of the chunk's votes; votes out (and cleared for the next chunk)
-    uint8_t* vout = a.votes + (int64_t)sq * a.t.nchunk * kChunk + base;
-    const bool last = c + 1 == c_hi;
-    uint32_t small = 0;
-    for (int i = tid; i < kChunk / 16; i += kThreads) {
-      uint4* vp = reinterpret_cast<uint4*>(votes) + i;
+    if (g0 == c_lo) trace_mark(tr, kTrDecodeFine + 1);
+    // votes out; histogram: counts of votes 1..4 by bit planes (bytes below 8),
+    // larger votes one by one (thread t: 16 keys of each chunk of the group)
+    for (int g = 0; g < ng; ++g) {
+      const int vi = g * kThreads + tid;
+      uint4* vp = reinterpret_cast<uint4*>(span) + vi;
       const uint4 w4 = *vp;
-      reinterpret_cast<uint4*>(vout)[i] = w4;
-      if (!last) *vp = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(a.votes + (int64_t)sq * a.t.nchunk * kChunk + gbase)[vi] = w4;
+      if (g0 + G < c_hi) *vp = make_uint4(0, 0, 0, 0);  // the span is reused by the next group
       const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t v = (ws[k >> 2] >> (8 * (k & 3))) & 0xffu;
-        const bool in = v != 0 && 16 * i + k < len;
-        if (in && v <= 4) small += 1u << (8 * (v - 1));  // per-thread counts <= 32 fit a byte
-        else if (in) atomicAdd(&hist[v], 1u);
-        nz_mine += in ? 1u : 0u;
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t x = ws[k];
+        const uint32_t v80 = first_bytes(glen - (16 * vi + 4 * k));
+        const uint32_t v01 = v80 >> 7;
+        const uint32_t big8 = (bytes_nonzero(x & 0xf8f8f8f8u) >> 7) & v01;  // valid bytes >= 8
+        const uint32_t lo = v01 & ~big8;
+        const uint32_t p0 = x & lo, p1 = (x >> 1) & lo, p2 = (x >> 2) & lo;
+        c1 += __popc(p0 & ~p1 & ~p2);
+        c2 += __popc(p1 & ~p0 & ~p2);
+        c3 += __popc(p0 & p1 & ~p2);
+        c4 += __popc(p2 & ~p0 & ~p1);
+        nz_mine += __popc(bytes_nonzero(x) & v80);
+        uint32_t big = big8 | (p2 & (p0 | p1));  // valid bytes >= 5
+        while (big) {
+          const int j = (31 - __clz(big & (0u - big))) >> 3;
+          big &= big - 1;
+          atomicAdd(&hist[(x >> (8 * j)) & 0xffu], 1u);
+        }
       }
-    }
-#pragma unroll
-    for (int v = 1; v <= 4; ++v) {
-      const uint32_t cnt = __reduce_add_sync(kFull, (small >> (8 * (v - 1))) & 0xffu);
-      if (lane == 0 && cnt) atomicAdd(&hist[v], cnt);
     }
   }
   {
+    const uint32_t cv[4] = {c1, c2, c3, c4};
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t cnt = __reduce_add_sync(kFull, cv[v]);
+      if (lane == 0 && cnt) atomicAdd(&hist[v + 1], cnt);
+    }
     uint32_t nz_all;
     block_excl_scan(nz_mine, tmp, &nz_all);
     if (tid == 0) hist[0] = (uint32_t)own_len - nz_all;
@@ -602,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
     eqb = __reduce_add_sync(kFull, eqb);
     if (lane == 0) {
       red[warp] = gtb;
-      red[32 + warp] = eqb;
+      red[kWarps + warp] = eqb;
     }
     __syncthreads();
     gtb = 0;
@@ -610,47 +624,41 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       gtb += red[w];
-      eqb += red[32 + w];
+      eqb += red[kWarps + w];
     }
     sel_before = gtb + min64(eqb, quota);
     eq_allow = max64(0, quota - (int64_t)eqb);
   }
   trace_mark(tr, kTrDecode2);
 
-  // ordered compaction: thread t owns keys [32t, 32t + 32) of each chunk,
-  // compared four at a time (bytes of a word)
+  // ordered compaction: thread t owns keys [16 G t, 16 G (t + 1)) of each
+  // group's span, compared four at a time (bytes of a word)
   const int64_t cq = (int64_t)sq * a.cmax;
   {
-    int64_t nsel = 0;
+    uint32_t nsel = 0;
     const uint32_t T4 = (uint32_t)T * 0x01010101u;
-    for (int c = c_lo; c < c_hi; ++c) {
-      const int64_t base = (int64_t)c * kChunk;
-      const int len = (int)min64(kChunk, a.N - base);
-      constexpr int kPer = kChunk / kThreads;
-      const int k0 = tid * kPer;
-      uint32_t vw[kPer / 4];
-      if (c + 1 == c_hi) {
-        const uint4* vin = reinterpret_cast<const uint4*>(votes + k0);
+    int32_t* out = a.cand_idx + cq + sel_before;
+    for (int g0 = c_lo; g0 < c_hi; g0 += G) {
+      const int ng = min(G, c_hi - g0);
+      const int64_t gbase = (int64_t)g0 * kChunk;
+      const int glen = (int)min64((int64_t)ng * kChunk, a.N - gbase);
+      const int k0 = 16 * G * tid;
+      const bool in_smem = g0 + G >= c_hi;  // the last group's votes are still in shared memory
+      uint32_t vw[4 * kVoteSlots];
 #pragma unroll
-        for (int i = 0; i < kPer / 16; ++i) {
-          const uint4 x = vin[i];
-          vw[4 * i] = x.x; vw[4 * i + 1] = x.y; vw[4 * i + 2] = x.z; vw[4 * i + 3] = x.w;
-        }
-      } else {
-        const uint4* vin = reinterpret_cast<const uint4*>(a.votes + (int64_t)sq * a.t.nchunk * kChunk + base + k0);
-#pragma unroll
-        for (int i = 0; i < kPer / 16; ++i) {
-          const uint4 x = __ldcg(vin + i);
-          vw[4 * i] = x.x; vw[4 * i + 1] = x.y; vw[4 * i + 2] = x.z; vw[4 * i + 3] = x.w;
-        }
+      for (int i = 0; i < kVoteSlots; ++i) {
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (i < G && k0 + 16 * i < glen)
+          x = in_smem ? reinterpret_cast<const uint4*>(span)[G * tid + i]
+                      : __ldcg(reinterpret_cast<const uint4*>(a.votes + (int64_t)sq * a.t.nchunk * kChunk + gbase) + G * tid + i);
+        vw[4 * i] = x.x; vw[4 * i + 1] = x.y; vw[4 * i + 2] = x.z; vw[4 * i + 3] = x.w;
       }
-      // per byte: 0x80 where the vote is above T / equal to T (keys past len: neither)
-      uint32_t gtm[kPer / 4], eqm[kPer / 4];
+      // per byte: 0x80 where the vote is above T / equal to T (keys past the span: neither)
+      uint32_t gtm[4 * kVoteSlots], eqm[4 * kVoteSlots];
       uint32_t n_eq = 0, n_gt = 0;
 #pragma unroll
-      for (int w = 0; w < kPer / 4; ++w) {
-        const int rest = len - (k0 + 4 * w);
-        const uint32_t valid = rest >= 4 ? 0x80808080u : rest <= 0 ? 0u : (0x80808080u >> (8 * (4 - rest)));
+      for (int w = 0; w < 4 * kVoteSlots; ++w) {
+        const uint32_t valid = w < 4 * G ? first_bytes(glen - (k0 + 4 * w)) : 0u;
         gtm[w] = bytes_gt(vw[w], T4) & valid;
         eqm[w] = bytes_eq(vw[w], T4) & valid;
         n_gt += __popc(gtm[w]);
@@ -660,10 +668,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
       const uint32_t eq_rank0 = block_excl_scan(n_eq, tmp, &eq_tot);
       uint32_t eq_left = (uint32_t)max64(0, min64((int64_t)n_eq, eq_allow - (int64_t)eq_rank0));
       uint32_t csel;
-      int64_t pos = nsel + block_excl_scan(n_gt + eq_left, tmp, &csel);
-      int32_t* out = a.cand_idx + cq + sel_before;
+      uint32_t pos = nsel + block_excl_scan(n_gt + eq_left, tmp, &csel);
+      const int32_t pbase = (int32_t)(a.s.sink + gbase + k0);
 #pragma unroll
-      for (int w = 0; w < kPer / 4; ++w) {
+      for (int w = 0; w < 4 * kVoteSlots; ++w) {
         uint32_t e = eqm[w];
         // the lowest-position keys equal to T, up to this thread's share
         while (__popc(e) > (int)eq_left) e &= ~(0x80000000u >> __clz(e));
@@ -672,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
         while (m) {
           const int j = (31 - __clz(m & (0u - m))) >> 3;  // lowest flagged byte
           m &= m - 1;
-          out[pos++] = (int32_t)(a.s.sink + base + k0 + 4 * w + j);
+          out[pos++] = pbase + 4 * w + j;
         }
       }
       eq_allow = max64(0, eq_allow - (int64_t)eq_tot);
@@ -684,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
   cluster_sync();
 
   // ---- 3. estimates: block r takes the slice [C r / cs, C (r + 1) / cs) ------
+  trace_block(a.trace, kTkDecode3, 0);
   const int64_t s_lo = a.C * r / cs, s_hi = a.C * (r + 1) / cs;
   const uint32_t nown = (uint32_t)(s_hi - s_lo);
   {
@@ -693,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
     // conflicts), so both gathers are in flight together
     const uint8_t* rec = a.t.rec + sh * a.t.rcap * kRecBytes;
     const float qn = s_qn;
-    uint4* slot = reinterpret_cast<uint4*>(U + kUKeys) + tid * 8;
+    uint4* slot = reinterpret_cast<uint4*>(U + kURecSlots) + tid * 8;
     for (uint32_t i0 = 0; i0 < nown; i0 += 2 * kThreads) {
       const uint32_t ia = i0 + tid, ib = i0 + kThreads + tid;
       const int32_t pa = ia < nown ? __ldcg(a.cand_idx + cq + s_lo + ia) : -1;
@@ -735,21 +744,45 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
   trace_mark(tr, kTrDecode3);
 
   // ---- 4. top-k ------------------------------------------------------------
-  // The k_eff-th best candidate by (estimate desc, position asc): block 0
-  // runs a radix select over the order keys of all C estimates, then tells
-  // every block where its slice's selected entries go and how many of its
-  // keys equal to the k-th key it keeps (the lowest positions first).
+  // The k_eff-th best candidate by (estimate desc, position asc): every
+  // block finds the k-th key over all C estimates, counts the keys above it
+  // and equal to it in the slices before its own, and so knows where its
+  // slice's selected entries go and how many of its keys equal to the k-th
+  // key it keeps (equal keys go to the lowest positions first).
   const bool select_all = a.k_eff >= a.C;  // the same in every block
   uint32_t prefix = 0, my_eq_take = 0;
   int64_t out_off = s_lo;
   if (!select_all) {
     cluster_sync();  // every estimate is written
-    if (r == 0) select_kth(a.C, a.k_eff, a.cand_est + cq, cs, U, tmp, sel_info);
-    cluster_sync();
-    prefix = dsmem_u32(&sel_info[kClusterMax][0], 0);
-    out_off = dsmem_u32(&sel_info[r][0], 0);
-    my_eq_take = dsmem_u32(&sel_info[r][1], 0);
+    trace_block(a.trace, kTkDecode3, 1);
+    uint32_t remaining;
+    prefix = select_kth(a.C, a.k_eff, a.cand_est + cq, U, tmp, &remaining);
+    trace_block(a.trace, kTkDecode3, 2);
+    const uint32_t* keys = reinterpret_cast<const uint32_t*>(U + kUKeys);
+    uint32_t gtb = 0, eqb = 0;
+    for (int i = tid; i < (int)s_lo; i += kThreads) {
+      const uint32_t k = a.C <= kSelCap ? keys[i] : order_key(__ldcg(a.cand_est + cq + i));
+      gtb += k > prefix ? 1u : 0u;
+      eqb += k == prefix ? 1u : 0u;
+    }
+    gtb = __reduce_add_sync(kFull, gtb);
+    eqb = __reduce_add_sync(kFull, eqb);
+    if (lane == 0) {
+      red[warp] = gtb;
+      red[kWarps + warp] = eqb;
+    }
+    __syncthreads();
+    gtb = 0;
+    eqb = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      gtb += red[w];
+      eqb += red[kWarps + w];
+    }
+    out_off = gtb + min(eqb, remaining);
+    my_eq_take = remaining > eqb ? remaining - eqb : 0u;
   }
+  trace_block(a.trace, kTkDecode3, 3);
   trace_mark(tr, kTrDecodeFine + 20);
   {
     // ordered output: thread t owns entries [t * per, t * per + per) of the slice
@@ -808,56 +841,55 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
     const int64_t row_lo = R * r / cs, row_hi = R * (r + 1) / cs;
     const int ntiles = (int)((row_hi - row_lo + kTile - 1) / kTile);
     const int ring = a.s.local + a.s.ubuf;
+    // where each of the block's rows comes from, resolved once (all loads in
+    // flight): element offset into the window arrays (kSrcWindow set) or the
+    // Retrieval-zone store; kSrcFresh: the step's own token; -1: no row
+    constexpr int64_t kSrcWindow = int64_t(1) << 62, kSrcFresh = int64_t(1) << 61;
+    const uint32_t nmod = ring > 0 ? (uint32_t)(a.N % ring) : 0u;  // ring slot of the first Local token
+    auto row_source = [&](int64_t row) -> int64_t {
+      if (row < a.nwin) {
+        int64_t slot = row, pos = row;
+        if (row >= a.nsink) {
+          uint32_t x = nmod + (uint32_t)(row - a.nsink);  // < 2 ring: the window holds at most ring tokens
+          if (x >= (uint32_t)ring) x -= (uint32_t)ring;
+          slot = a.s.sink + x;
+          pos = a.s.sink + a.N + (row - a.nsink);
+        }
+        if (pos == a.new_pos) return kSrcFresh;
+        return kSrcWindow | ((sh * a.kv.win + slot) * kDim);
+      }
+      const int64_t pos = __ldcg(a.topk_idx + (int64_t)sq * a.k + (row - a.nwin));
+      if (pos >= a.s.sink && pos < a.s.sink + a.N) return (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
+      if (pos >= 0) atomicOr(a.status, kStatusBadIndex);
+      return -1;
+    };
+    constexpr int kRowTab = kListCap / 2;
+    int64_t* rsrc = reinterpret_cast<int64_t*>(lpos);
+    const int nrows = (int)(row_hi - row_lo);
+    for (int t = tid; t < min(nrows, kRowTab); t += kThreads) rsrc[t] = row_source(row_lo + t);
+    __syncthreads();
     const int srow = tid >> 4, ch = tid & 15;  // staged row of the tile, 16-byte chunk of it
     // stage tile j into buffer j % kStages (one commit group per tile, empty past the end)
-    // top-k positions of the block's retrieved rows, loaded once (all in flight)
-    const int64_t ret0 = max64(row_lo, a.nwin);
-    const int ntab = (int)min64(max64(0, row_hi - ret0), kListCap);
-    int32_t* ptab = lpos;
-    __syncthreads();  // the candidate slice in lpos is no longer read
-    for (int t = tid; t < ntab; t += kThreads) ptab[t] = __ldcg(a.topk_idx + (int64_t)sq * a.k + (ret0 - a.nwin) + t);
-    const uint32_t nmod = ring > 0 ? (uint32_t)(a.N % ring) : 0u;  // ring slot of the first Local token
-    __syncthreads();
     auto stage = [&](int j) {
       const int buf = j % kStages;
       uint16_t* kd = stK + (buf * kTile + srow) * kKStride + 8 * ch;
       uint16_t* vd = stV + (buf * kTile + srow) * kKStride + 8 * ch;
-      const int64_t row = row_lo + (int64_t)j * kTile + srow;
-      bool have = false;
-      if (j < ntiles && row < row_hi) {
-        if (row < a.nwin) {
-          int64_t slot = row, pos = row;
-          if (row >= a.nsink) {
-            uint32_t x = nmod + (uint32_t)(row - a.nsink);  // < 2 ring: the window holds at most ring tokens
-            if (x >= (uint32_t)ring) x -= (uint32_t)ring;
-            slot = a.s.sink + x;
-            pos = a.s.sink + a.N + (row - a.nsink);
-          }
-          if (pos == a.new_pos) {
-            // the step's own token: from the caller's k/v, converted as the append stores it
-            *reinterpret_cast<uint4*>(kd) = load8_as_bf16(a.k_new, a.kvdtype, sh * kDim + 8 * ch);
-            *reinterpret_cast<uint4*>(vd) = load8_as_bf16(a.v_new, a.kvdtype, sh * kDim + 8 * ch);
-          } else {
-            const int64_t e = (sh * a.kv.win + slot) * kDim + 8 * ch;
-            cp_async16(kd, a.kv.win_k + e);
-            cp_async16(vd, a.kv.win_v + e);
-          }
-          have = true;
-        } else {
-          const int64_t t = row - ret0;
-          const int64_t pos = t < kListCap ? ptab[t] : __ldcg(a.topk_idx + (int64_t)sq * a.k + (row - a.nwin));
-          if (pos >= a.s.sink && pos < a.s.sink + a.N) {
-            const int64_t e = (sh * a.kv.rcap + (pos - a.s.sink)) * kDim + 8 * ch;
-            cp_async16(kd, a.kv.st_k + e);
-            cp_async16(vd, a.kv.st_v + e);
-            have = true;
-          } else if (pos >= 0 && ch == 0) {
-            atomicOr(a.status, kStatusBadIndex);
-          }
-        }
+      const int rl = j * kTile + srow;
+      int64_t src = -1;
+      if (j < ntiles && rl < nrows) src = rl < kRowTab ? rsrc[rl] : row_source(row_lo + rl);
+      if (src == kSrcFresh) {
+        // the step's own token: from the caller's k/v, converted as the append stores it
+        *reinterpret_cast<uint4*>(kd) = load8_as_bf16(a.k_new, a.kvdtype, sh * kDim + 8 * ch);
+        *reinterpret_cast<uint4*>(vd) = load8_as_bf16(a.v_new, a.kvdtype, sh * kDim + 8 * ch);
+      } else if (src >= 0) {
+        const bool win = (src & kSrcWindow) != 0;
+        const int64_t e = (src & (kSrcFresh - 1)) + 8 * ch;
+        cp_async16(kd, (win ? a.kv.win_k : a.kv.st_k) + e);
+        cp_async16(vd, (win ? a.kv.win_v : a.kv.st_v) + e);
+      } else {
+        *reinterpret_cast<uint4*>(vd) = make_uint4(0, 0, 0, 0);  // finite zeros for the V sum
       }
-      if (!have) *reinterpret_cast<uint4*>(vd) = make_uint4(0, 0, 0, 0);  // finite zeros for the V sum
-      if (ch == 0) rvalid[buf][srow] = have ? 1 : 0;
+      if (ch == 0) rvalid[buf][srow] = src != -1 ? 1 : 0;
       cp_async_commit();
     };
 #pragma unroll
@@ -920,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
       for (int w2 = 0; w2 < kWarps; ++w2)
         if (wml[2 * w2 + 1] > 0.f) Mb = fmaxf(Mb, wml[2 * w2]);
       float ob = 0.f, lb = 0.f;
-#pragma unroll
+#pragma unroll 8
       for (int w2 = 0; w2 < kWarps; ++w2) {
         const float lw = wml[2 * w2 + 1];
         if (lw > 0.f) {
@@ -965,9 +997,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode(DecodeArgs a) {
     trace_block(a.trace, kTkDecode2, 1);
   }
 
-  // ---- the step's own token into the cache ---------------------------------
-  if (a.new_pos >= 0 && r == 0 && qh % a.s.g == 0 && warp == 0)
-    append_token_warp(a.k_new, a.v_new, a.kvdtype, a.new_pos, sh, lane, a.s, a.kv, a.t, a.sm, a.rp);
   trace_mark(tr, kTrDecode6);
   trace_block(a.trace, kTkDecode2, 3);
 }
@@ -1030,18 +1059,16 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.topk_idx = ra.topk_idx;
   a.topk_score = ra.topk_score;
   a.out = L.out;
-  const size_t smem = (size_t)hot_bytes(kSub * ra.rho) + kUBytes;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               hot_bytes(kSub * kCentroids) + kUBytes);
+    const cudaError_t e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kUBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, ra.s.batch * ra.s.hq);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = kUBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -163,10 +163,11 @@ constexpr int kTraceSlots = 64;
 constexpr int kTraceBlocks = 4096;   // per-block stamps: 4 per block and trace row
 constexpr int kTraceKernels = 8;
 constexpr int64_t kTraceWords = kTraceSlots + (int64_t)kTraceKernels * kTraceBlocks * 4;
-// trace rows: the fused decode kernel uses three (start, after wait,
+// trace rows: the fused decode kernel uses four (start, after wait,
 // prepared, voted | compacted, reranked, top-k out, after barrier |
-// attention tiles, merged, -, end); the standalone attention one
-enum TraceKernel { kTkDecode0 = 0, kTkDecode1, kTkDecode2, kTkAttend };
+// attention tiles, merged, -, end | rerank start, top-k start, k-th key
+// found, output offsets known); the standalone attention one
+enum TraceKernel { kTkDecode0 = 0, kTkDecode1, kTkDecode2, kTkAttend, kTkDecode3 };
 enum TraceSlot {
   kTrDecode0 = 0, kTrDecode1, kTrDecode2, kTrDecode3, kTrDecode4, kTrDecode5, kTrDecode6,
   kTrDecodeFine = 8,  // 8 .. 28: steps inside the vote and top-k phases
