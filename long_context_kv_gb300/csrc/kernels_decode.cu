@@ -55,8 +55,10 @@ static_assert(2 * kThreads == kSelBins, "two radix digits per thread");
 // byte offsets inside the phase-shared dynamic region
 constexpr int kUVotes = 0;                                    // u8 [kVoteSlots][kChunk]
 constexpr int kUOffs = kUVotes + kVoteSlots * kChunk;         // u32 [kVoteSlots][kSub][kOffStride]
-constexpr int kUHot = kUOffs + kVoteSlots * kSub * kOffStride * 4;  // hot lists: hv[nhot], then per list
-                                                              // (G x nhot) hbeg, hwt and hpre (+1)
+constexpr int kWarpBins = 64;                                 // per-warp counts of votes 8 .. 71
+constexpr int kUWarpHist = kUOffs + kVoteSlots * kSub * kOffStride * 4;  // u32 [kWarps][kWarpBins]
+constexpr int kUHot = kUWarpHist + kWarps * kWarpBins * 4;    // hot lists: hv[nhot], then per list
+                                                              // (G x nhot) hbeg, hwt, hpre (+1), hsm
 constexpr int kURecSlots = 0;                                 // 128 B per thread: a candidate record being gathered
 constexpr int kUKeys = 0;                                     // u32 [kSelCap]: top-k order keys
 constexpr int kUSelHist = kUKeys + kSelCap * 4;               // u32 [kSelBins]
@@ -66,8 +68,9 @@ constexpr int kUAttnEnd = 2 * kStages * kTile * kKStride * 2;
 constexpr int kUListPos = kUAttnEnd;                          // i32 [kListCap]: the block's candidate slice
 constexpr int kUListEst = kUListPos + kListCap * 4;           // f32 [kListCap]: its estimates
 constexpr int kUBytes = kUListEst + kListCap * 4;
-static_assert(kUHot + (4 * kSub * kCentroids + 1) * 4 <= kUListPos, "hot lists (G = 1) below the candidate slice");
-static_assert(kUHot + (7 * 1024 + 1) * 4 <= kUListPos, "hot lists (G = 2) below the candidate slice");
+static_assert(kUHot + (5 * kSub * kCentroids + 1) * 4 + 16 <= kUBytes, "hot lists (G = 1) inside the region");
+static_assert(kUWarpHist + kWarps * kWarpBins * 4 <= kUHot, "per-warp vote counts before the hot lists");
+static_assert(kUHot + (9 * 1024 + 1) * 4 + 16 <= kUBytes, "hot lists (G = 2) inside the region");
 static_assert(kUSelHist + kSelBins * 4 <= kUListPos, "top-k tables below the candidate slice");
 static_assert(kURecSlots + kThreads * kRecBytes <= kUListPos, "record slots below the candidate slice");
 
@@ -276,6 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   uint32_t* hbeg = hv + nhot;
   uint32_t* hwt = hbeg + nlist;
   uint32_t* hpre = hwt + nlist;                            // nlist + 1
+  int32_t* hsm = reinterpret_cast<int32_t*>(hpre + nlist + 1);  // list entry f is lists[hsm[e] + f]
+  // the group's lists, copied into shared memory when they fit
+  const int lists_at = (kUHot + (nhot + 4 * nlist + 1) * 4 + 15) & ~15;
+  uint16_t* lists = reinterpret_cast<uint16_t*>(U + lists_at);
+  const int lists_cap = (kUBytes - lists_at) / 2;
   uint32_t* offs = reinterpret_cast<uint32_t*>(U + kUOffs);
   int32_t* lpos = reinterpret_cast<int32_t*>(U + kUListPos);
   float* lest = reinterpret_cast<float*>(U + kUListEst);
@@ -294,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   for (int i = tid; i < kVoteSlots * kChunk / 16; i += kThreads)
     reinterpret_cast<uint4*>(U + kUVotes)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < kMaxBins; i += kThreads) hist[i] = 0;
+  uint32_t* whist = reinterpret_cast<uint32_t*>(U + kUWarpHist);
+  for (int i = tid; i < kWarps * kWarpBins; i += kThreads) whist[i] = 0;
   pdl_wait();
   pdl_trigger();
   trace_block(a.trace, kTkDecode0, 1);
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   // 1 when the hot lists are long).
   const int G = nhot <= 1024 ? kVoteSlots : 1;
   uint8_t* span = U + kUVotes;
-  uint32_t c1 = 0, c2 = 0, c3 = 0, c4 = 0, nz_mine = 0;
+  uint32_t cnt[7] = {0, 0, 0, 0, 0, 0, 0}, nz_mine = 0;  // votes 1..7 counted by bit planes
   int64_t own_len = 0;
   for (int g0 = c_lo; g0 < c_hi; g0 += G) {
     const int ng = min(G, c_hi - g0), nl = ng * nhot;
@@ -489,36 +499,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     if (g0 + G < c_hi) prefetch_offsets(g0 + G, min(G, c_hi - g0 - G));  // offsets not read again
     const uint32_t total = hpre[nl];
     const uint16_t* ent = a.t.ent + ((sh * a.t.nchunk + g0) * kSub) * (int64_t)kChunk;
-    // thread t takes kWalk consecutive list entries: one search, then linear
-    // steps; all kWalk loads in flight together
-    constexpr int kWalk = 8;
-    for (uint32_t f0 = kWalk * tid; f0 < total; f0 += kWalk * kThreads) {
-      int e = 0, hi = nl - 1;  // last e with hpre[e] <= f0 (a non-empty list)
-      while (e < hi) {
-        const int mid = (e + hi + 1) >> 1;
-        if (hpre[mid] <= f0) e = mid; else hi = mid - 1;
+    // list e2 goes to lists[S, S + pad) with S = 8-aligned(hpre + 24 e2): its
+    // aligned 16-byte pieces (the list plus up to 14 neighbouring bytes)
+    const bool staged = (int64_t)total + 24 * nl + 8 <= lists_cap;  // the same in the whole block
+    if (staged) {
+      for (int e2 = warp; e2 < nl; e2 += kWarps) {
+        const uint32_t hb = hbeg[e2], len = hpre[e2 + 1] - hpre[e2];
+        const uint32_t S = (hpre[e2] + 24u * e2 + 7u) & ~7u;
+        const uint32_t n16 = ((hb & 7u) + len + 7u) >> 3;
+        for (uint32_t k = lane; k < n16; k += 32) cp_async16(lists + S + 8 * k, ent + (hb & ~7u) + 8 * k);
+        if (lane == 0) hsm[e2] = (int32_t)(S + (hb & 7u)) - (int32_t)hpre[e2];
       }
-      uint32_t key[kWalk], wt[kWalk];
+      cp_async_wait_all();
+      __syncthreads();
+    }
+    // warp w walks lists w, w + 32, ...; lane l takes entries l, l + 32, ...
+    uint32_t* votes32 = reinterpret_cast<uint32_t*>(span);
+    for (int e2 = warp; e2 < nl; e2 += kWarps) {
+      const uint32_t p0 = hpre[e2], len = hpre[e2 + 1] - p0, hw = hwt[e2];
+      const uint32_t wt = hw & 0xffu, koff = (hw >> 16) << 14;  // weight; the chunk's place in the span
+      if (staged) {
+        const uint16_t* src = lists + hsm[e2] + (int32_t)p0;
+        for (uint32_t i = lane; i < len; i += 32) {
+          const uint32_t key = src[i] + koff;
+          atomicAdd(votes32 + (key >> 2), wt << ((key & 3) * 8));
+        }
+      } else {
+        const uint16_t* src = ent + hbeg[e2];
+        for (uint32_t i0 = 0; i0 < len; i0 += 128) {
+          uint32_t kk[4];
 #pragma unroll
-      for (int u = 0; u < kWalk; ++u) {
-        const uint32_t f = f0 + u;
-        wt[u] = 0;
-        key[u] = 0;
-        if (f < total) {
-          while (hpre[e + 1] <= f) ++e;
-          const uint32_t hw = hwt[e];
-          key[u] = __ldg(ent + hbeg[e] + (f - hpre[e])) + ((hw >> 16) << 14);  // key within the span
-          wt[u] = hw & 0xffu;
+          for (int u = 0; u < 4; ++u) kk[u] = i0 + 32 * u + lane < len ? __ldg(src + i0 + 32 * u + lane) : 0xffffffffu;
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (kk[u] != 0xffffffffu) {
+              const uint32_t key = kk[u] + koff;
+              atomicAdd(votes32 + (key >> 2), wt << ((key & 3) * 8));
+            }
         }
       }
-#pragma unroll
-      for (int u = 0; u < kWalk; ++u)
-        if (wt[u]) atomicAdd(reinterpret_cast<uint32_t*>(span) + (key[u] >> 2), wt[u] << ((key[u] & 3) * 8));
     }
     __syncthreads();
     if (g0 == c_lo) trace_mark(tr, kTrDecodeFine + 1);
-    // votes out; histogram: counts of votes 1..4 by bit planes (bytes below 8),
-    // larger votes one by one (thread t: 16 keys of each chunk of the group)
+    // votes out; histogram: counts of votes 1..7 by bit planes (the bytes
+    // below 8), larger votes one by one (thread t: 16 keys of each chunk of
+    // the group)
     for (int g = 0; g < ng; ++g) {
       const int vi = g * kThreads + tid;
       uint4* vp = reinterpret_cast<uint4*>(span) + vi;
@@ -531,32 +556,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         const uint32_t x = ws[k];
         const uint32_t v80 = first_bytes(glen - (16 * vi + 4 * k));
         const uint32_t v01 = v80 >> 7;
-        const uint32_t big8 = (bytes_nonzero(x & 0xf8f8f8f8u) >> 7) & v01;  // valid bytes >= 8
-        const uint32_t lo = v01 & ~big8;
+        uint32_t big = (bytes_nonzero(x & 0xf8f8f8f8u) >> 7) & v01;  // valid bytes >= 8
+        const uint32_t lo = v01 & ~big;
         const uint32_t p0 = x & lo, p1 = (x >> 1) & lo, p2 = (x >> 2) & lo;
-        c1 += __popc(p0 & ~p1 & ~p2);
-        c2 += __popc(p1 & ~p0 & ~p2);
-        c3 += __popc(p0 & p1 & ~p2);
-        c4 += __popc(p2 & ~p0 & ~p1);
+        cnt[0] += __popc(p0 & ~p1 & ~p2);
+        cnt[1] += __popc(~p0 & p1 & ~p2);
+        cnt[2] += __popc(p0 & p1 & ~p2);
+        cnt[3] += __popc(~p0 & ~p1 & p2);
+        cnt[4] += __popc(p0 & ~p1 & p2);
+        cnt[5] += __popc(~p0 & p1 & p2);
+        cnt[6] += __popc(p0 & p1 & p2);
         nz_mine += __popc(bytes_nonzero(x) & v80);
-        uint32_t big = big8 | (p2 & (p0 | p1));  // valid bytes >= 5
         while (big) {
           const int j = (31 - __clz(big & (0u - big))) >> 3;
           big &= big - 1;
-          atomicAdd(&hist[(x >> (8 * j)) & 0xffu], 1u);
+          const uint32_t v = (x >> (8 * j)) & 0xffu;
+          if (v < 8 + kWarpBins) atomicAdd(&whist[warp * kWarpBins + (v - 8)], 1u);
+          else atomicAdd(&hist[v], 1u);
         }
       }
     }
   }
   {
-    const uint32_t cv[4] = {c1, c2, c3, c4};
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint32_t cnt = __reduce_add_sync(kFull, cv[v]);
-      if (lane == 0 && cnt) atomicAdd(&hist[v + 1], cnt);
+    for (int v = 0; v < 7; ++v) {
+      const uint32_t n = __reduce_add_sync(kFull, cnt[v]);
+      if (lane == 0 && n) atomicAdd(&hist[v + 1], n);
     }
     uint32_t nz_all;
-    block_excl_scan(nz_mine, tmp, &nz_all);
+    block_excl_scan(nz_mine, tmp, &nz_all);  // (its barriers also order the per-warp counts)
+    if (tid < kWarpBins) {
+      uint32_t n = 0;
+#pragma unroll 8
+      for (int w = 0; w < kWarps; ++w) n += whist[w * kWarpBins + tid];
+      if (n) atomicAdd(&hist[8 + tid], n);
+    }
     if (tid == 0) hist[0] = (uint32_t)own_len - nz_all;
   }
   trace_block(a.trace, kTkDecode0, 3);
@@ -946,26 +980,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       wml[2 * warp + 1] = l;
     }
     __syncthreads();
-    if (tid < kDim) {
-      float Mb = -FLT_MAX;
+    if (warp == 0) {
+      // lane w: warp w's weight exp2(m_w - max) (0 for a warp without rows)
+      const float mw = wml[2 * lane], lw = wml[2 * lane + 1];
+      float mx = lw > 0.f ? mw : -FLT_MAX;
 #pragma unroll
-      for (int w2 = 0; w2 < kWarps; ++w2)
-        if (wml[2 * w2 + 1] > 0.f) Mb = fmaxf(Mb, wml[2 * w2]);
-      float ob = 0.f, lb = 0.f;
-#pragma unroll 8
-      for (int w2 = 0; w2 < kWarps; ++w2) {
-        const float lw = wml[2 * w2 + 1];
-        if (lw > 0.f) {
-          const float f = exp2f(wml[2 * w2] - Mb);
-          ob += wo[w2 * kDim + tid] * f;
-          lb += lw * f;
-        }
-      }
-      part[4 + tid] = ob;
-      if (tid == 0) {
-        part[0] = Mb;
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      const float f = lw > 0.f ? exp2f(mw - mx) : 0.f;
+      wml[2 * lane + 1] = f;  // weights replace the sums (read below)
+      float lb = lw * f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lb += __shfl_xor_sync(kFull, lb, o);
+      if (lane == 0) {
+        part[0] = mx;
         part[1] = lb;
       }
+    }
+    __syncthreads();
+    if (tid < kDim) {
+      float ob = 0.f;
+#pragma unroll 8
+      for (int w2 = 0; w2 < kWarps; ++w2) ob += wo[w2 * kDim + tid] * wml[2 * w2 + 1];
+      part[4 + tid] = ob;
     }
     cluster_sync();
     trace_mark(tr, kTrDecode5);

@@ -399,7 +399,8 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   }
   TRY(dalloc(c, &c->t.ids, (size_t)bh * c->rcap * kSub, "bucket ids"));
   TRY(dalloc(c, &c->t.rec, (size_t)bh * c->rcap * kRecBytes, "codes and w"));
-  TRY(dalloc(c, &c->t.ent, (size_t)bh * c->nchunk * kSub * kChunk * sizeof(uint16_t), "bucket lists"));
+  // 16 spare bytes: list copies round their last 16-byte piece up
+  TRY(dalloc(c, &c->t.ent, (size_t)bh * c->nchunk * kSub * kChunk * sizeof(uint16_t) + 16, "bucket lists"));
   TRY(dalloc(c, &c->t.off, (size_t)bh * c->nchunk * kSub * kOffStride * sizeof(uint32_t), "bucket offsets"));
   TRY(dalloc(c, &c->qt, (size_t)bq * kDim * sizeof(float), "q~"));
   TRY(dalloc(c, &c->qnorm, (size_t)bq * sizeof(float), "||q||"));
