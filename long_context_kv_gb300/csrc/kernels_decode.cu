@@ -730,47 +730,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   const int64_t s_lo = a.C * r / cs, s_hi = a.C * (r + 1) / cs;
   const uint32_t nown = (uint32_t)(s_hi - s_lo);
   {
-    // two candidates per thread and round: the first one's record straight
-    // into registers, the second one's by asynchronous copy into the
-    // thread's own 128-byte slot (16-byte chunks swizzled against bank
-    // conflicts), so both gathers are in flight together
+    // Warp w takes candidates 32 w + 1024 k + lane.  Its 32 records of a
+    // round are copied into the warp's own 4 KB of shared memory with each
+    // copy instruction covering four whole 128-byte records (lane l: piece
+    // l % 8 of record l / 8 + 4 u), then every lane estimates its own.
     const uint8_t* rec = a.t.rec + sh * a.t.rcap * kRecBytes;
     const float qn = s_qn;
-    uint4* slot = reinterpret_cast<uint4*>(U + kURecSlots) + tid * 8;
-    for (uint32_t i0 = 0; i0 < nown; i0 += 2 * kThreads) {
-      const uint32_t ia = i0 + tid, ib = i0 + kThreads + tid;
-      const int32_t pa = ia < nown ? __ldcg(a.cand_idx + cq + s_lo + ia) : -1;
-      const int32_t pb = ib < nown ? __ldcg(a.cand_idx + cq + s_lo + ib) : -1;
-      if (pb >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(rec + (int64_t)(pb - a.s.sink) * kRecBytes);
+    uint4* wslot = reinterpret_cast<uint4*>(U + kURecSlots) + warp * 32 * 8;
+    for (uint32_t c0 = 32 * warp; c0 < nown; c0 += kThreads) {
+      const uint32_t i = c0 + lane;
+      const int32_t pm = i < nown ? __ldcg(a.cand_idx + cq + s_lo + i) : -1;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) cp_async16(slot + (u ^ (tid & 7)), src + u);
+      for (int u = 0; u < 8; ++u) {
+        const int rc = 4 * u + (lane >> 3), piece = lane & 7;
+        const int32_t p = __shfl_sync(kFull, pm, rc);
+        if (p >= 0)
+          cp_async16(wslot + rc * 8 + (piece ^ (rc & 7)),
+                     rec + (int64_t)(p - a.s.sink) * kRecBytes + 16 * piece);
       }
-      cp_async_commit();
-      if (pa >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(rec + (int64_t)(pa - a.s.sink) * kRecBytes);
+      cp_async_wait_all();
+      __syncwarp();
+      if (pm >= 0) {
         uint4 x[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = __ldg(src + u);
+        for (int u = 0; u < 8; ++u) x[u] = wslot[lane * 8 + (u ^ (lane & 7))];
         const float e = estimate(x, tq, qn);
-        a.cand_est[cq + s_lo + ia] = e;
-        if (ia < kListCap) {
-          lpos[ia] = pa;
-          lest[ia] = e;
+        a.cand_est[cq + s_lo + i] = e;
+        if (i < kListCap) {
+          lpos[i] = pm;
+          lest[i] = e;
         }
       }
-      cp_async_wait_all();  // this thread's own slot
-      if (pb >= 0) {
-        uint4 x[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = slot[u ^ (tid & 7)];
-        const float e = estimate(x, tq, qn);
-        a.cand_est[cq + s_lo + ib] = e;
-        if (ib < kListCap) {
-          lpos[ib] = pb;
-          lest[ib] = e;
-        }
-      }
+      __syncwarp();  // the slots are reused by the next round
     }
   }
   __syncthreads();
