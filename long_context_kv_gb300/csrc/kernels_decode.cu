@@ -23,10 +23,10 @@
 //   4. barrier; every block finds the k-th best estimate over all C (radix
 //      select in shared memory) and writes the selected entries of its
 //      slice at their place in the top-k;
-//   5. barrier; the rows (window + top-k) are split evenly over the blocks;
-//      each block stages its rows through a four-stage asynchronous-copy
-//      pipeline, every warp with its own online softmax; barrier; block 0
-//      merges the blocks.
+//   5. barrier; the window rows and the top-k rows are split evenly over the
+//      blocks; each block stages them in rounds of 128 rows, two rounds in
+//      flight, every warp scoring 4 rows of a round with its own online
+//      softmax; barrier; block 0 merges the blocks.
 // A decode token appended in the same step is read from the caller's k/v
 // where the attention needs it, and written to the cache by one warp while
 // the query is prepared (nothing in this launch reads the slots it writes).
@@ -107,12 +107,12 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 
 // Cluster barrier: every thread of every block of the cluster arrives; the
@@ -260,7 +260,9 @@ __device__ __noinline__ uint32_t select_kth(const int64_t C, const int64_t k_eff
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
-  __shared__ float qs[kDim], zs[kDim], qts[kDim];
+  __shared__ __align__(16) float qs[kDim];
+  __shared__ __align__(16) float zs[kDim];
+  __shared__ __align__(16) float qts[kDim];
   __shared__ float tq[kDim * 16];
   __shared__ uint32_t hist[kMaxBins];                // read by the cluster
   __shared__ __align__(16) float part[kPartStride];  // read by block 0
@@ -368,8 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   } else if (warp > kSub + 1) {
     // warm L2 with the window rows this block's attention will read
     if (a.out != nullptr) {
-      const int64_t R = a.nwin + a.k_eff;
-      const int64_t w_lo = R * r / cs, w_hi = min64(R * (r + 1) / cs, a.nwin);
+      const int64_t w_lo = a.nwin * r / cs, w_hi = a.nwin * (r + 1) / cs;
       const int ring = a.s.local + a.s.ubuf;
       const uint32_t nmod = ring > 0 ? (uint32_t)(a.N % ring) : 0u;
       for (int64_t row = w_lo + (tid - (kSub + 2) * 32); row < w_hi; row += kThreads - (kSub + 2) * 32) {
@@ -740,6 +741,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     for (uint32_t c0 = 32 * warp; c0 < nown; c0 += kThreads) {
       const uint32_t i = c0 + lane;
       const int32_t pm = i < nown ? __ldcg(a.cand_idx + cq + s_lo + i) : -1;
+      // the next round's records start on their way to L2 now
+      const uint32_t inx = i + kThreads;
+      if (inx < nown) prefetch_l2(rec + (int64_t)(__ldcg(a.cand_idx + cq + s_lo + inx) - a.s.sink) * kRecBytes);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int rc = 4 * u + (lane >> 3), piece = lane & 7;
@@ -862,9 +866,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 
   // ---- 5. sparse attention ---------------------------------------------------
   if (a.out != nullptr) {
-    const int64_t R = a.nwin + a.k_eff;
-    const int64_t row_lo = R * r / cs, row_hi = R * (r + 1) / cs;
-    const int ntiles = (int)((row_hi - row_lo + kTile - 1) / kTile);
+    // block r: an even share of the window rows and of the retrieved rows
+    const int64_t wl = a.nwin * r / cs, wh = a.nwin * (r + 1) / cs;
+    const int64_t kl = a.k_eff * r / cs, kh = a.k_eff * (r + 1) / cs;
+    const int nwb = (int)(wh - wl);
+    const int nrows = nwb + (int)(kh - kl);
+    auto grow = [&](int t) -> int64_t { return t < nwb ? wl + t : a.nwin + kl + (t - nwb); };
     const int ring = a.s.local + a.s.ubuf;
     // where each of the block's rows comes from, resolved once (all loads in
     // flight): element offset into the window arrays (kSrcWindow set) or the
@@ -890,74 +897,97 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     };
     constexpr int kRowTab = kListCap / 2;
     int64_t* rsrc = reinterpret_cast<int64_t*>(lpos);
-    const int nrows = (int)(row_hi - row_lo);
-    for (int t = tid; t < min(nrows, kRowTab); t += kThreads) rsrc[t] = row_source(row_lo + t);
+    for (int t = tid; t < min(nrows, kRowTab); t += kThreads) rsrc[t] = row_source(grow(t));
     __syncthreads();
-    const int srow = tid >> 4, ch = tid & 15;  // staged row of the tile, 16-byte chunk of it
-    // stage tile j into buffer j % kStages (one commit group per tile, empty past the end)
-    auto stage = [&](int j) {
-      const int buf = j % kStages;
-      uint16_t* kd = stK + (buf * kTile + srow) * kKStride + 8 * ch;
-      uint16_t* vd = stV + (buf * kTile + srow) * kKStride + 8 * ch;
-      const int rl = j * kTile + srow;
-      int64_t src = -1;
-      if (j < ntiles && rl < nrows) src = rl < kRowTab ? rsrc[rl] : row_source(row_lo + rl);
-      if (src == kSrcFresh) {
-        // the step's own token: from the caller's k/v, converted as the append stores it
-        *reinterpret_cast<uint4*>(kd) = load8_as_bf16(a.k_new, a.kvdtype, sh * kDim + 8 * ch);
-        *reinterpret_cast<uint4*>(vd) = load8_as_bf16(a.v_new, a.kvdtype, sh * kDim + 8 * ch);
-      } else if (src >= 0) {
-        const bool win = (src & kSrcWindow) != 0;
-        const int64_t e = (src & (kSrcFresh - 1)) + 8 * ch;
-        cp_async16(kd, (win ? a.kv.win_k : a.kv.st_k) + e);
-        cp_async16(vd, (win ? a.kv.win_v : a.kv.st_v) + e);
-      } else {
-        *reinterpret_cast<uint4*>(vd) = make_uint4(0, 0, 0, 0);  // finite zeros for the V sum
+    // Rounds of kRound rows through two halves of the stage area: round
+    // rd + 2 loads into the half that round rd has just used, so two rounds
+    // are in flight.  A round's copies: 16 threads per row, one 16-byte piece
+    // each.  Warp w scores rows 4 w .. 4 w + 3 of a round (8 lanes per row,
+    // 16 dimensions each) with its own online softmax; lane l accumulates
+    // output dimensions 4 l .. 4 l + 3 over the warp's rows.
+    constexpr int kRound = kStages * kTile / 2;
+    static_assert(kRound == 4 * kWarps && 16 * kRound == 2 * kThreads, "4 rows per warp, 2 copied rows per thread");
+    const int nrounds = (nrows + kRound - 1) / kRound;
+    auto issue = [&](int rd) {
+      const int half = rd & 1;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int rr = (tid >> 4) + 64 * u, ch = tid & 15;  // round row, 16-byte piece
+        uint16_t* kd = stK + (half * kRound + rr) * kKStride + 8 * ch;
+        uint16_t* vd = stV + (half * kRound + rr) * kKStride + 8 * ch;
+        const int rl = rd * kRound + rr;
+        int64_t src = -1;
+        if (rd < nrounds && rl < nrows) src = rl < kRowTab ? rsrc[rl] : row_source(grow(rl));
+        if (src == kSrcFresh) {
+          // the step's own token: from the caller's k/v, converted as the append stores it
+          *reinterpret_cast<uint4*>(kd) = load8_as_bf16(a.k_new, a.kvdtype, sh * kDim + 8 * ch);
+          *reinterpret_cast<uint4*>(vd) = load8_as_bf16(a.v_new, a.kvdtype, sh * kDim + 8 * ch);
+        } else if (src >= 0) {
+          const bool win = (src & kSrcWindow) != 0;
+          const int64_t e = (src & (kSrcFresh - 1)) + 8 * ch;
+          cp_async16(kd, (win ? a.kv.win_k : a.kv.st_k) + e);
+          cp_async16(vd, (win ? a.kv.win_v : a.kv.st_v) + e);
+        } else {
+          *reinterpret_cast<uint4*>(vd) = make_uint4(0, 0, 0, 0);  // finite zeros for the V sum
+        }
+        if (ch == 0) rvalid[half * 2 + (rr >> 6)][rr & 63] = src != -1 ? 1 : 0;
       }
-      if (ch == 0) rvalid[buf][srow] = src != -1 ? 1 : 0;
       cp_async_commit();
     };
+    trace_mark(tr, kTrDecodeRound - 1);
+    issue(0);
+    issue(1);
+    const int hrow = 4 * warp + (lane >> 3), oct = lane & 7;  // scored row of the round, eighth of it
+    float qv[16];  // the lane's 16 dimensions of the scaled q, loaded once
 #pragma unroll
-    for (int j = 0; j < kStages; ++j) stage(j);
-    // Each warp keeps its own online softmax over rows 2w and 2w + 1 of
-    // every tile: lanes 0-15 score row 2w and lanes 16-31 row 2w + 1
-    // (8 dimensions each, q in registers); every lane accumulates output
-    // dimensions 4 lane .. 4 lane + 3.  The warps merge once at the end.
-    const int hrow = 2 * warp + (lane >> 4), sub = lane & 15;
-    float qr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qr[i] = zs[8 * sub + i];
+    for (int i = 0; i < 16; ++i) qv[i] = zs[16 * oct + i];
     float M = -FLT_MAX, l = 0.f, o4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < ntiles; ++j) {
-      const int buf = j % kStages;
-      cp_async_wait_group<kStages - 1>();
+    for (int rd = 0; rd < nrounds; ++rd) {
+      const int half = rd & 1;
+      cp_async_wait_group<1>();  // all but the newest group: round rd has landed
       __syncthreads();
-      const uint4 kv8 = *reinterpret_cast<const uint4*>(stK + (buf * kTile + hrow) * kKStride + 8 * sub);
-      const uint32_t w[4] = {kv8.x, kv8.y, kv8.z, kv8.w};
+      if (rd < 8) trace_mark(tr, kTrDecodeRound + 2 * rd);
+      const uint16_t* kh = stK + half * kRound * kKStride;
+      const uint16_t* vh = stV + half * kRound * kKStride;
       float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s += qr[2 * i] * bf16_bits_to_float(w[i] & 0xffffu);
-        s += qr[2 * i + 1] * __uint_as_float(w[i] & 0xffff0000u);
+      for (int u = 0; u < 2; ++u) {
+        const uint4 kv8 = *reinterpret_cast<const uint4*>(kh + hrow * kKStride + 16 * oct + 8 * u);
+        const float* q8 = qv + 8 * u;
+        s += q8[0] * bf16_bits_to_float(kv8.x & 0xffffu) + q8[1] * __uint_as_float(kv8.x & 0xffff0000u);
+        s += q8[2] * bf16_bits_to_float(kv8.y & 0xffffu) + q8[3] * __uint_as_float(kv8.y & 0xffff0000u);
+        s += q8[4] * bf16_bits_to_float(kv8.z & 0xffffu) + q8[5] * __uint_as_float(kv8.z & 0xffff0000u);
+        s += q8[6] * bf16_bits_to_float(kv8.w & 0xffffu) + q8[7] * __uint_as_float(kv8.w & 0xffff0000u);
       }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-      const bool valid = rvalid[buf][hrow] != 0;
+      s += __shfl_xor_sync(kFull, s, 1);
+      s += __shfl_xor_sync(kFull, s, 2);
+      s += __shfl_xor_sync(kFull, s, 4);
+      const bool valid = rvalid[half * 2 + (hrow >> 6)][hrow & 63] != 0;
       if (!valid) s = -FLT_MAX;
-      const float Mn = fmaxf(M, fmaxf(s, __shfl_xor_sync(kFull, s, 16)));
+      float mx = fmaxf(s, __shfl_xor_sync(kFull, s, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+      const float Mn = fmaxf(M, mx);
       const float sc = exp2f(M - Mn);
       const float pm = valid ? exp2f(s - Mn) : 0.f;
-      const float p0 = __shfl_sync(kFull, pm, 0), p1 = __shfl_sync(kFull, pm, 16);
-      l = l * sc + p0 + p1;
-      const uint2 v0 = *reinterpret_cast<const uint2*>(stV + (buf * kTile + 2 * warp) * kKStride + 4 * lane);
-      const uint2 v1 = *reinterpret_cast<const uint2*>(stV + (buf * kTile + 2 * warp + 1) * kKStride + 4 * lane);
-      o4[0] = o4[0] * sc + p0 * bf16_bits_to_float(v0.x & 0xffffu) + p1 * bf16_bits_to_float(v1.x & 0xffffu);
-      o4[1] = o4[1] * sc + p0 * __uint_as_float(v0.x & 0xffff0000u) + p1 * __uint_as_float(v1.x & 0xffff0000u);
-      o4[2] = o4[2] * sc + p0 * bf16_bits_to_float(v0.y & 0xffffu) + p1 * bf16_bits_to_float(v1.y & 0xffffu);
-      o4[3] = o4[3] * sc + p0 * __uint_as_float(v0.y & 0xffff0000u) + p1 * __uint_as_float(v1.y & 0xffff0000u);
+      float ps = oct == 0 ? pm : 0.f;
+      ps += __shfl_xor_sync(kFull, ps, 8);
+      ps += __shfl_xor_sync(kFull, ps, 16);
+      l = l * sc + ps;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o4[k] *= sc;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = __shfl_sync(kFull, pm, 8 * i);
+        const uint2 v = *reinterpret_cast<const uint2*>(vh + (4 * warp + i) * kKStride + 4 * lane);
+        o4[0] += p * bf16_bits_to_float(v.x & 0xffffu);
+        o4[1] += p * __uint_as_float(v.x & 0xffff0000u);
+        o4[2] += p * bf16_bits_to_float(v.y & 0xffffu);
+        o4[3] += p * __uint_as_float(v.y & 0xffff0000u);
+      }
       M = Mn;
-      __syncthreads();  // buffer `buf` is free
-      stage(j + kStages);
+      __syncthreads();  // this half is refilled next
+      if (rd < 8) trace_mark(tr, kTrDecodeRound + 2 * rd + 1);
+      issue(rd + 2);
     }
     cp_async_wait_all();
     __syncthreads();

@@ -171,6 +171,7 @@ enum TraceKernel { kTkDecode0 = 0, kTkDecode1, kTkDecode2, kTkAttend, kTkDecode3
 enum TraceSlot {
   kTrDecode0 = 0, kTrDecode1, kTrDecode2, kTrDecode3, kTrDecode4, kTrDecode5, kTrDecode6,
   kTrDecodeFine = 8,  // 8 .. 28: steps inside the vote and top-k phases
+  kTrDecodeRound = 41,  // 40: attention rounds start; 41 + 2 rd: round rd landed, + 1: computed
   kTrAttend0 = 32, kTrAttend1, kTrAttend2, kTrAttend3, kTrAttend4
 };
 
