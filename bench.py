@@ -289,7 +289,7 @@ def run_ours(args, rank, world):
     us_decode = 1e3 * prof.get("decode", [0.0, 0])[0] / args.steps
     us_append = sum(1e3 * prof.get(k, [0.0, 0])[0] for k in ("append", "build_index")) / args.steps
 
-    # roofline of the dominant kernel (algorithmic bytes per launch, see DESIGN.md)
+    # roofline of the dominant kernel (algorithmic bytes per launch)
     Nmean = sum(keys_per_step) / len(keys_per_step) / (b * hkv)
     nch = -(-int(Nmean) // 16384)
     C = max((w["cand_bp"] * int(Nmean) + 9999) // 10000, min(w["topk"], int(Nmean)))

@@ -21,7 +21,7 @@ Two arithmetic modes
   agrees bit for bit.  The order of every sum is stated in the docstring of
   the function that computes it.
 
-Readings of points the pages leave open (each is also listed in the design doc):
+Readings of points the pages leave open:
 R1 SRHT = H_d diag(D) / sqrt(d), no subsampling (d is a power of two), one D
    shared by keys and queries of a layer; D is an input.
 R2 normalise-then-rotate equals rotate-then-divide-by-norm; ids and codes
