@@ -130,6 +130,37 @@ def traffic_record(kernel: str):
 
 
 # ---------------------------------------------------------------------------
+# ranks (one process per GPU; every rank runs its own replica of the workload)
+# ---------------------------------------------------------------------------
+def rank_seed(rank: int, layer: int) -> int:
+    """Seed of a rank's layer context: ranks draw disjoint synthetic inputs."""
+    return 20260202 + 1 + 1000 * rank + layer
+
+
+def rank_barrier(dist: bool) -> None:
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+
+
+def max_over_ranks_of(x: float, dist: bool, device: str) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
+    if not dist:
+        return x
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(keys_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job keys per second: every rank scans its own keys_per_rank in
+    the timed region, and the job takes the slowest rank's ms_max."""
+    return keys_per_rank * world / (ms_max / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 def run_ours(args, rank, world):
@@ -151,13 +182,12 @@ def run_ours(args, rank, world):
     per_layer_steps = (args.warmup + 4 * args.steps + nl - 1) // nl + 2
     max_ctx = ctxlen + per_layer_steps + 8
     fdt = torch.bfloat16 if args.workload != "tiny-4k" else torch.float32
-    seed0 = 20260202 + 1 + 1000 * rank
     gen = torch.Generator(device="cuda")
     layers = []
     keep_keys = None
     t_setup = time.time()
     for li in range(nl):
-        seed = seed0 + li
+        seed = rank_seed(rank, li)
         cfg = P.make_config(batch=b, n_kv_heads=hkv, n_q_heads=hq, head_dim=d, n_sub=w["n_sub"], rho=w["rho"],
                             sink=S, local=w["local"], update_buf=w["update_buf"], topk=w["topk"],
                             cand_bp=w["cand_bp"], max_ctx=max_ctx, retrieval_on_host=0)
@@ -200,20 +230,13 @@ def run_ours(args, rank, world):
         return {"profile_case": DESCRIPTION[args.workload], "layers": nl, "steps": args.warmup + args.steps}
 
     dist = world > 1
-    if dist:
-        import torch.distributed as tdist
 
     def barrier():
         torch.cuda.synchronize()
-        if dist:
-            tdist.barrier()
+        rank_barrier(dist)
 
     def max_over_ranks(x):
-        if not dist:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(x, dist, "cuda")
 
     i = 0
     for _ in range(args.warmup):
@@ -271,8 +294,7 @@ def run_ours(args, rank, world):
         for _ in range(3):
             g_main.replay()
         torch.cuda.synchronize()
-    keys_total = sum(keys_per_step) * world
-    value = keys_total / (ms / 1e3)
+    value = job_throughput(sum(keys_per_step), world, ms)
 
     # per-kernel device time: a second capture with events around every kernel
     g_prof, _, _ = capture(profile=True)
@@ -385,7 +407,7 @@ def run_ours(args, rank, world):
         "recall_at_k": recall,
         "kernels": kernels,
         "roofline": roof,
-        "e2e": {"value": keys_e2e * world / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(keys_e2e, world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk.summary(),
