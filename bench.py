@@ -179,7 +179,7 @@ def run_ours(args, rank, world):
     nl = args.layers or w["layers"]
     ctxlen, d = w["context"], w["head_dim"]
     b, hkv, hq, S = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["sink"]
-    per_layer_steps = (args.warmup + 4 * args.steps + nl - 1) // nl + 2
+    per_layer_steps = (args.warmup + 8 * args.steps + 64 + nl - 1) // nl + 2
     max_ctx = ctxlen + per_layer_steps + 8
     fdt = torch.bfloat16 if args.workload != "tiny-4k" else torch.float32
     gen = torch.Generator(device="cuda")
@@ -296,6 +296,48 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
     value = job_throughput(sum(keys_per_step), world, ms)
 
+    # the calls of the path one by one (paris_retrieve, paris_sparse_attend,
+    # paris_append_decode), each as K captured calls replayed like the step
+    def timed_calls(call):
+        nonlocal i
+        cs = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(args.steps):
+                call(layers[i % nl], i)
+                i += 1
+        g.replay()
+        torch.cuda.synchronize()
+        return timed(g.replay) / args.steps
+
+    def call_retrieve(L, _):
+        L["ctx"].paris_retrieve(L["qs"][L["step"]], L["idx"], L["sc"])
+
+    def call_attend(L, _):
+        L["ctx"].paris_sparse_attend(L["qs"][L["step"]], L["idx"], L["out"])
+
+    def call_append(L, _):
+        j = L["step"]
+        L["step"] = j + 1
+        L["ctx"].paris_append_decode(L["kn"][j], L["vn"][j])
+
+    keys_retrieve = sum(L["ctx"].paris_get_state()["N"] * b * hkv for L in layers) / nl
+    ms_retrieve = timed_calls(call_retrieve)
+    ms_attend = timed_calls(call_attend)
+    ms_append = timed_calls(call_append)
+
+    # per-step device time distribution: events around each eager step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(64)]
+    barrier()
+    for e0, e1 in ev:
+        e0.record(stream)
+        step(i)
+        i += 1
+        e1.record(stream)
+    torch.cuda.synchronize()
+    step_us = sorted(1e3 * e0.elapsed_time(e1) for e0, e1 in ev)
+    pct = lambda p_: step_us[min(len(step_us) - 1, int(p_ * len(step_us)))]
+
     # per-kernel device time: a second capture with events around every kernel
     g_prof, _, _ = capture(profile=True)
     g_prof.replay()
@@ -309,7 +351,6 @@ def run_ours(args, rank, world):
     del g_prof
     kernels = {k: {"us_per_launch": 1e3 * v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1]}
     us_decode = 1e3 * prof.get("decode", [0.0, 0])[0] / args.steps
-    us_append = sum(1e3 * prof.get(k, [0.0, 0])[0] for k in ("append", "build_index")) / args.steps
 
     # roofline of the dominant kernel (algorithmic bytes per launch)
     Nmean = sum(keys_per_step) / len(keys_per_step) / (b * hkv)
@@ -317,12 +358,18 @@ def run_ours(args, rank, world):
     C = max((w["cand_bp"] * int(Nmean) + 9999) // 10000, min(w["topk"], int(Nmean)))
     keff = min(w["topk"], C)
     nwin = S + w["local"] + w["update_buf"] // 2
+    # Algorithmic bytes of one decode-step launch (one layer), per unit of
+    # work: 16 B of bucket ids per Retrieval key and (sequence, KV head) --
+    # the full scan a flat layout streams; 128 B of codes and w per candidate
+    # and (sequence, query head); 8 B per top-k output; the top-k K and V
+    # rows (2 x 256 B) per query head, and the window's rows (Sink, Local,
+    # Buffer) once per KV head.  The kernel itself reads only the rho hot
+    # bucket lists of each subspace (2 B per entry), so it moves fewer bytes
+    # than this for the ids; "design_bytes" counts what it does read.
     alg = {
-        # one launch = one decode step of one layer.  Per query head: the
-        # hot buckets' list entries (2 B each; rho of 256 buckets in each of
-        # B subspaces), the candidates' 128-byte records, the retrieved K and
-        # V rows (2 x 256 B) and the top-k written (index + estimate).  Per
-        # KV head: the bucket offsets of every chunk and the window's K/V rows.
+        "decode": b * hkv * 16 * Nmean + b * hq * (C * 128 + keff * 8 + keff * 4 * d) + b * hkv * nwin * 4 * d,
+    }
+    design = {
         "decode": b * hq * (2 * w["rho"] * w["n_sub"] * Nmean / 256 + C * 128 + keff * 4 * d + keff * 8)
                   + b * hkv * (nch * 16 * 264 * 4 + nwin * 4 * d),
     }
@@ -333,7 +380,7 @@ def run_ours(args, rank, world):
         ach = alg[dom] / (kernels[dom]["us_per_launch"] * 1e-6) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom),
-                "algorithmic_bytes": alg[dom]}
+                "algorithmic_bytes": alg[dom], "design_bytes": design[dom]}
 
     # end to end through the public API with host buffers
     L0 = layers[0]
@@ -403,7 +450,10 @@ def run_ours(args, rank, world):
                          f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"},
         "us_per_decode_step": 1e3 * ms / args.steps,
         "us_per_decode_step_eager": 1e3 * ms_eager / args.steps,
-        "us_decode_kernel": us_decode, "us_append": us_append,
+        "us_decode_kernel": us_decode,
+        "us_per_decode_step_eager_p10_p50_p90": [round(pct(0.1), 2), round(pct(0.5), 2), round(pct(0.9), 2)],
+        "us_retrieve": 1e3 * ms_retrieve, "keys_per_s_retrieve": job_throughput(keys_retrieve, world, ms_retrieve),
+        "us_sparse_attend": 1e3 * ms_attend, "us_append": 1e3 * ms_append,
         "recall_at_k": recall,
         "kernels": kernels,
         "roofline": roof,

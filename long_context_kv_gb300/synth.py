@@ -57,8 +57,7 @@ def keys(seed: int, batch: int, n_kv_heads: int, t0: int, t1: int, d: int,
     out = np.empty((batch, n_kv_heads, t1 - t0, d), dtype=np.float32)
     for b in range(batch):
         for h in range(n_kv_heads):
-            out[b, h] = _blocked_normal(seed, _S_KEYS, b, h, t0, t1, d)
-            out[b, h] *= scale[h][None, :]
+            out[b, h] = key_rows(seed, b, h, t0, t1, d, scale)
     return out
 
 
@@ -67,8 +66,19 @@ def values(seed: int, batch: int, n_kv_heads: int, t0: int, t1: int, d: int) -> 
     out = np.empty((batch, n_kv_heads, t1 - t0, d), dtype=np.float32)
     for b in range(batch):
         for h in range(n_kv_heads):
-            out[b, h] = _blocked_normal(seed, _S_VALUES, b, h, t0, t1, d)
+            out[b, h] = value_rows(seed, b, h, t0, t1, d)
     return out
+
+
+def key_rows(seed: int, b: int, h: int, t0: int, t1: int, d: int, scale: np.ndarray) -> np.ndarray:
+    """keys(...)[b, h] alone, float32 [t1 - t0, d]: the same bits, without
+    drawing the other (sequence, head) pairs (long contexts, one head at a time)."""
+    return _blocked_normal(seed, _S_KEYS, b, h, t0, t1, d) * scale[h][None, :]
+
+
+def value_rows(seed: int, b: int, h: int, t0: int, t1: int, d: int) -> np.ndarray:
+    """values(...)[b, h] alone, float32 [t1 - t0, d]."""
+    return _blocked_normal(seed, _S_VALUES, b, h, t0, t1, d)
 
 
 _BLOCK = 4096
