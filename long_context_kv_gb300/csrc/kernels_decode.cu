@@ -10,23 +10,25 @@
 //
 // One thread-block cluster of CS <= 4 blocks (1024 threads, one per SM) per
 // (sequence, query head); block r owns a contiguous range of index chunks
-// of the Retrieval zone, so block order is position order.  Cluster
-// barriers separate the steps that need the whole query head (every block
-// reaches every barrier):
+// of the Retrieval zone, so block order is position order.  What a block
+// hands to the others it stores straight into their shared memory before a
+// cluster barrier.  Four barriers separate the steps:
 //   1. each block: q~, ||q|| and the hot centroids (redundantly), the votes
-//      of its chunks and their histogram;
-//   2. barrier; every block sums the cluster's histograms (distributed
-//      shared memory), finds the vote threshold and writes its candidates
-//      (positions ascending) at their place in the query head's list;
-//   3. barrier; block r computes the estimates of the slice
-//      [C r / CS, C (r + 1) / CS) of that list;
-//   4. barrier; every block finds the k-th best estimate over all C (radix
-//      select in shared memory) and writes the selected entries of its
-//      slice at their place in the top-k;
-//   5. barrier; the window rows and the top-k rows are split evenly over the
-//      blocks; each block stages them in rounds of 128 rows, two rounds in
-//      flight, every warp scoring 4 rows of a round with its own online
-//      softmax; barrier; block 0 merges the blocks.
+//      of its chunks and their histogram, pushed to every block;
+//   2. barrier; every block sums the histograms, finds the vote threshold
+//      and writes its candidates (positions ascending) at their place in the
+//      query head's list;
+//   3. barrier; block r estimates its slice [C r / CS, C (r + 1) / CS) of
+//      the list and pushes the order keys of the
+//      estimates (and their range) to every block;
+//   4. barrier; every block finds the k-th best key over all C (a counting
+//      pass in shared memory), counts the entries taken before its slice and
+//      writes the ones its slice takes at their place in the top-k; those
+//      rows and its share of the window rows are its attention rows, staged
+//      in rounds of 128 rows, two rounds in flight, every warp scoring 4 rows
+//      of a round with its own online softmax; the block's partial goes to
+//      block 0;
+//   5. barrier; block 0 merges the partials.
 // A decode token appended in the same step is read from the caller's k/v
 // where the attention needs it, and written to the cache by one warp while
 // the query is prepared (nothing in this launch reads the slots it writes).
@@ -45,8 +47,10 @@ constexpr int kListCap = 4096;      // candidates of the block's slice kept in s
 constexpr int kTile = 64;           // attention rows per pipeline stage
 constexpr int kStages = 4;
 constexpr int kKStride = kDim + 8;  // bf16 per staged row: 272 B keeps 16-byte reads conflict-free
-constexpr int kSelCap = 16384;      // candidates whose keys the top-k stages in shared memory
+constexpr int kSelCap = 12288;      // candidates whose order keys every block of the cluster holds
 constexpr int kSelBins = 2048;      // 11-bit radix digits
+constexpr int kBinRank = 64;        // keys left in the k-th digit that are ranked directly
+constexpr int kRowTab = kSelCap / 2;  // attention rows whose sources are resolved into a table
 static_assert(kTile * 16 == kThreads, "16 threads per staged row");
 static_assert(2 * kWarps == kTile, "two rows of a tile per warp");
 static_assert(kChunk / kThreads == 16, "one 16-byte vote vector per thread and chunk");
@@ -60,19 +64,21 @@ constexpr int kUWarpHist = kUOffs + kVoteSlots * kSub * kOffStride * 4;  // u32 
 constexpr int kUHot = kUWarpHist + kWarps * kWarpBins * 4;    // hot lists: hv[nhot], then per list
                                                               // (G x nhot) hbeg, hwt, hpre (+1), hsm
 constexpr int kURecSlots = 0;                                 // 128 B per thread: a candidate record being gathered
-constexpr int kUKeys = 0;                                     // u32 [kSelCap]: top-k order keys
-constexpr int kUSelHist = kUKeys + kSelCap * 4;               // u32 [kSelBins]
 constexpr int kUStageK = 0;                                   // bf16 [kStages][kTile][kKStride]
 constexpr int kUStageV = kStages * kTile * kKStride * 2;
 constexpr int kUAttnEnd = 2 * kStages * kTile * kKStride * 2;
-constexpr int kUListPos = kUAttnEnd;                          // i32 [kListCap]: the block's candidate slice
-constexpr int kUListEst = kUListPos + kListCap * 4;           // f32 [kListCap]: its estimates
-constexpr int kUBytes = kUListEst + kListCap * 4;
+constexpr int kUSelHist = kUStageK + kStages / 2 * kTile * kKStride * 2;  // u32 [kSelBins], then u32 [kBinRank]:
+                                                              // in the K rows of the second attention round
+constexpr int kUSelPos = kUSelHist + (kSelBins + kBinRank) * 4;  // i32 [kListCap]: positions the block's slice takes
+constexpr int kUKeys = kUAttnEnd;                             // u32 [kSelCap]: order keys of all C estimates,
+                                                              // then i64 [kRowTab]: attention row sources
+constexpr int kUListPos = kUKeys + kSelCap * 4;               // i32 [kListCap]: the block's rerank slice
+constexpr int kUBytes = kUListPos + kListCap * 4;
 static_assert(kUHot + (5 * kSub * kCentroids + 1) * 4 + 16 <= kUBytes, "hot lists (G = 1) inside the region");
 static_assert(kUWarpHist + kWarps * kWarpBins * 4 <= kUHot, "per-warp vote counts before the hot lists");
 static_assert(kUHot + (9 * 1024 + 1) * 4 + 16 <= kUBytes, "hot lists (G = 2) inside the region");
-static_assert(kUSelHist + kSelBins * 4 <= kUListPos, "top-k tables below the candidate slice");
-static_assert(kURecSlots + kThreads * kRecBytes <= kUListPos, "record slots below the candidate slice");
+static_assert(kUSelPos + kListCap * 4 <= kUStageV, "top-k tables inside the second round's K rows");
+static_assert(kURecSlots + kThreads * kRecBytes <= kUKeys, "record slots below the order keys");
 
 struct DecodeArgs {
   Shape s;
@@ -83,6 +89,11 @@ struct DecodeArgs {
   int rho, flat, nbins, cpb, nchunk_active;
   int64_t N, C, k, k_eff, cmax;
   int64_t nsink, nwin;  // attention window rows
+  // cut points q = 0 .. kClusterMax (C q / CS and nwin q / CS, clamped at
+  // q = CS): the rerank slices of the candidate list and the blocks' shares
+  // of the window rows
+  int64_t ccut[kClusterMax + 1], wcut[kClusterMax + 1];
+  uint32_t nmod;        // ring slot of the first Local token
   const void* q;
   int qdtype;
   float qscale;
@@ -121,12 +132,72 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// 32-bit load from the same shared-memory variable of block `rank` of the cluster.
-__device__ __forceinline__ uint32_t dsmem_u32(const void* p, uint32_t rank) {
+// Address of the same shared-memory variable in block `rank` of the cluster,
+// and a 32-bit store there.  Stores to other blocks are made visible by the
+// next cluster barrier.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
   const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-  uint32_t ra, v;
+  uint32_t ra;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(a), "r"(rank));
-  asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(ra) : "memory");
+  return ra;
+}
+__device__ __forceinline__ void dsmem_st_u32(uint32_t ra, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(ra), "r"(v) : "memory");
+}
+
+// Exclusive block scan of two unsigned values per thread at once (tmp: 66
+// words of shared memory); x and y are replaced by their prefixes, tx and ty
+// receive the block sums.
+__device__ __forceinline__ void block_excl_scan2(uint32_t& x, uint32_t& y, uint32_t* tmp, uint32_t& tx,
+                                                 uint32_t& ty) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t ix = x, iy = y;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t tx = __shfl_up_sync(kFull, ix, o), ty = __shfl_up_sync(kFull, iy, o);
+    if (lane >= o) {
+      ix += tx;
+      iy += ty;
+    }
+  }
+  if (lane == 31) {
+    tmp[warp] = ix;
+    tmp[33 + warp] = iy;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t vx = tmp[lane], vy = tmp[33 + lane];
+    uint32_t sx = vx, sy = vy;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t tx = __shfl_up_sync(kFull, sx, o), ty = __shfl_up_sync(kFull, sy, o);
+      if (lane >= o) {
+        sx += tx;
+        sy += ty;
+      }
+    }
+    tmp[lane] = sx - vx;
+    tmp[33 + lane] = sy - vy;
+    if (lane == 31) {
+      tmp[32] = sx;
+      tmp[65] = sy;
+    }
+  }
+  __syncthreads();
+  x = tmp[warp] + ix - x;
+  y = tmp[33 + warp] + iy - y;
+  tx = tmp[32];
+  ty = tmp[65];
+  __syncthreads();
+}
+
+// c[q] for a q known only at run time, by constant-index selects (a
+// run-time index into a kernel parameter array would copy it to local memory).
+__device__ __forceinline__ int64_t cut_at(const int64_t (&c)[kClusterMax + 1], int q) {
+  int64_t v = c[0];
+#pragma unroll
+  for (int i = 1; i <= kClusterMax; ++i)
+    if (q == i) v = c[i];
   return v;
 }
 
@@ -175,84 +246,129 @@ __device__ __forceinline__ float estimate(const uint4 (&x)[8], const float* tq, 
   return __fmul_rn(qn, acc);
 }
 
-// The k_eff-th largest order key over the C estimates of a query head
-// (radix select, 11-bit digits below the bits all keys share; keys staged
-// in shared memory when C <= kSelCap).  Returns the key; *remaining_out
-// receives how many keys equal to it belong to the top k_eff.  All threads
-// of the block call it and get the same results.
-__device__ __noinline__ uint32_t select_kth(const int64_t C, const int64_t k_eff, const float* est, uint8_t* U,
-                                            uint32_t* tmp, uint32_t* remaining_out) {
-  __shared__ uint32_t s_digit, s_skip;
-  __shared__ uint32_t s_and[kWarps], s_or[kWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t* keys = reinterpret_cast<uint32_t*>(U + kUKeys);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(U + kUSelHist);
-  const bool staged = C <= kSelCap;
-  const int n = (int)C;  // at most the Retrieval-zone capacity
-  // keys (8 loads in flight per thread), and the bits every key shares
-  uint32_t kand = 0xffffffffu, kor = 0u;
-  for (int i0 = tid; i0 < n; i0 += 8 * kThreads) {
-    float v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = i0 + u * kThreads < n ? __ldcg(est + i0 + u * kThreads) : 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = i0 + u * kThreads;
-      if (i < n) {
-        const uint32_t k = order_key(v[u]);
-        if (staged) keys[i] = k;
-        kand &= k;
-        kor |= k;
-      }
-    }
-  }
-  kand = __reduce_and_sync(kFull, kand);
-  kor = __reduce_or_sync(kFull, kor);
-  if (lane == 0) {
-    s_and[warp] = kand;
-    s_or[warp] = kor;
+// One counting pass of the k-th key search: keys are counted by bin_of(key)
+// (a bin in 0 .. kSelBins-1, or -1 for a key not in play), and the bin
+// holding the `remaining`-th largest key in play is found by scanning from
+// the top bin (bin order must follow key order).  `remaining` loses the keys
+// of the bins above it; *held receives how many keys the bin holds.
+// key_of(i) gives the i-th of n keys.  All threads of the block call it.
+template <class KeyOf, class BinOf>
+__device__ __forceinline__ uint32_t count_pass(KeyOf key_of, int n, BinOf bin_of, uint32_t* hist, uint32_t* tmp,
+                                               uint32_t& remaining, uint32_t* held) {
+  __shared__ uint32_t s_bin, s_skip;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    const int bn = bin_of(key_of(i));
+    if (bn >= 0) atomicAdd(&hist[bn], 1u);
   }
   __syncthreads();
-  kand = 0xffffffffu;
-  kor = 0u;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    kand &= s_and[w];
-    kor |= s_or[w];
+  // thread t owns bins kSelBins-1-2t and kSelBins-2-2t, scanned from the top
+  const uint32_t c0 = hist[kSelBins - 1 - 2 * tid], c1 = hist[kSelBins - 2 - 2 * tid];
+  uint32_t tot;
+  const uint32_t exc = block_excl_scan(c0 + c1, tmp, &tot);
+  if (exc < remaining && exc + c0 >= remaining) {
+    s_bin = (uint32_t)(kSelBins - 1 - 2 * tid);
+    s_skip = exc;
+  } else if (exc + c0 < remaining && exc + c0 + c1 >= remaining) {
+    s_bin = (uint32_t)(kSelBins - 2 - 2 * tid);
+    s_skip = exc + c0;
   }
-  const uint32_t diff = kand ^ kor;
-  uint32_t prefix = kand, remaining = (uint32_t)k_eff;
-  if (diff != 0) {
-    const int top = 31 - __clz(diff);  // highest bit where keys differ
-    uint32_t mask = top == 31 ? 0u : (0xffffffffu << (top + 1));
-    prefix = kand & mask;
-    for (int hi = top; hi >= 0;) {
-      const int nb = min(11, hi + 1), lo = hi + 1 - nb;
-      const uint32_t dmask = (1u << nb) - 1u;
-      for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
-      __syncthreads();
-      for (int i = tid; i < n; i += kThreads) {
-        const uint32_t k = staged ? keys[i] : order_key(__ldcg(est + i));
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> lo) & dmask], 1u);
-      }
-      __syncthreads();
-      // thread t owns digits kSelBins-1-2t and kSelBins-2-2t, scanned from the top
-      const uint32_t c0 = hist[kSelBins - 1 - 2 * tid], c1 = hist[kSelBins - 2 - 2 * tid];
-      uint32_t tot;
-      const uint32_t exc = block_excl_scan(c0 + c1, tmp, &tot);
-      if (exc < remaining && exc + c0 >= remaining) {
-        s_digit = (uint32_t)(kSelBins - 1 - 2 * tid);
-        s_skip = exc;
-      } else if (exc + c0 < remaining && exc + c0 + c1 >= remaining) {
-        s_digit = (uint32_t)(kSelBins - 2 - 2 * tid);
-        s_skip = exc + c0;
-      }
-      __syncthreads();
-      prefix |= s_digit << lo;
-      mask |= dmask << lo;
-      remaining -= s_skip;
-      hi = lo - 1;
-      __syncthreads();
+  __syncthreads();
+  const uint32_t bn = s_bin;
+  remaining -= s_skip;
+  *held = hist[bn];
+  __syncthreads();
+  return bn;
+}
+
+// The `remaining`-th largest of the few keys (at most kBinRank) for which
+// in_bin(key) holds: the key with fewer than `remaining` of them above it and
+// at least `remaining` at or above it.  Returns it; `remaining` becomes the
+// number of keys equal to it that are taken.
+template <class KeyOf, class InBin>
+__device__ __forceinline__ uint32_t rank_in_bin(KeyOf key_of, int n, InBin in_bin, uint32_t* bin,
+                                                uint32_t& remaining) {
+  __shared__ uint32_t s_nbin, s_key, s_rem;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_nbin = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kThreads) {
+    const uint32_t k = key_of(i);
+    if (in_bin(k)) bin[atomicAdd(&s_nbin, 1u)] = k;
+  }
+  __syncthreads();
+  const int nbin = (int)s_nbin;
+  if (tid < nbin) {
+    const uint32_t mine = bin[tid];
+    uint32_t above = 0, at = 0;
+    for (int j = 0; j < nbin; ++j) {
+      const uint32_t o = bin[j];
+      above += o > mine ? 1u : 0u;
+      at += o >= mine ? 1u : 0u;
+    }
+    if (above < remaining && at >= remaining) {  // every such thread holds the same key
+      s_key = mine;
+      s_rem = remaining - above;
+    }
+  }
+  __syncthreads();
+  const uint32_t key = s_key;
+  remaining = s_rem;
+  __syncthreads();
+  return key;
+}
+
+// The k_eff-th largest of the C order keys of a query head, and how many
+// keys equal to it belong to the top k_eff (*remaining_out).  kmin and kmax
+// are the smallest and largest key.  First pass: kSelBins bins linear in the
+// estimate between the two (a monotone map, so bin order is key order); if
+// the chosen bin holds at most kBinRank keys they are ranked directly.
+// Otherwise (a crowded bin, or a range the linear map cannot represent):
+// 11-bit radix digits below the bits kmin and kmax share, with the same
+// direct ranking once a digit is small.  key_of(i) gives key i.  All threads
+// of the block call it and get the same results.
+template <class KeyOf>
+__device__ __forceinline__ uint32_t select_kth(KeyOf key_of, const int64_t C, const int64_t k_eff, uint32_t kmin,
+                                               uint32_t kmax, uint8_t* U, uint32_t* tmp, uint32_t* remaining_out) {
+  uint32_t* hist = reinterpret_cast<uint32_t*>(U + kUSelHist);
+  uint32_t* bin = hist + kSelBins;
+  const int n = (int)C;
+  uint32_t remaining = (uint32_t)k_eff;
+  if (kmin == kmax) {
+    *remaining_out = remaining;
+    return kmin;
+  }
+  const float fmin = key_to_float(kmin), fmax = key_to_float(kmax);
+  const float sc = (float)kSelBins / (fmax - fmin);
+  if (isfinite(sc) && sc > 0.f) {
+    auto lin = [&](uint32_t k) -> int { return min(kSelBins - 1, (int)((key_to_float(k) - fmin) * sc)); };
+    uint32_t held;
+    const int bsel = (int)count_pass(key_of, n, lin, hist, tmp, remaining, &held);
+    if (held <= (uint32_t)kBinRank) {
+      const uint32_t key = rank_in_bin(key_of, n, [&](uint32_t k) { return lin(k) == bsel; }, bin, remaining);
+      *remaining_out = remaining;
+      return key;
+    }
+    remaining = (uint32_t)k_eff;
+  }
+  const int top = 31 - __clz(kmin ^ kmax);  // highest bit where keys differ
+  uint32_t mask = top == 31 ? 0u : (0xffffffffu << (top + 1));
+  uint32_t prefix = kmin & mask;
+  for (int hi = top; hi >= 0;) {
+    const int nb = min(11, hi + 1), lo = hi + 1 - nb;
+    const uint32_t dmask = (1u << nb) - 1u;
+    uint32_t held;
+    const uint32_t digit = count_pass(
+        key_of, n, [&](uint32_t k) { return (k & mask) == prefix ? (int)((k >> lo) & dmask) : -1; }, hist, tmp,
+        remaining, &held);
+    prefix |= digit << lo;
+    mask |= dmask << lo;
+    hi = lo - 1;
+    if (hi >= 0 && held <= (uint32_t)kBinRank) {
+      prefix = rank_in_bin(key_of, n, [&](uint32_t k) { return (k & mask) == prefix; }, bin, remaining);
+      break;
     }
   }
   *remaining_out = remaining;
@@ -265,10 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ __align__(16) float qts[kDim];
   __shared__ float tq[kDim * 16];
   __shared__ uint32_t hist[kMaxBins];                // read by the cluster
-  __shared__ __align__(16) float part[kPartStride];  // read by block 0
   __shared__ uint32_t tot[kMaxBins];
+  __shared__ uint32_t hall[kClusterMax][kMaxBins];           // every block's histogram, pushed by its owner
+  __shared__ uint32_t skey_mm[kClusterMax][2];               // smallest and largest order key of every block
+  __shared__ __align__(16) float pall[kClusterMax][kPartStride];  // attention partials, pushed to block 0
   __shared__ uint32_t tmp[33];
-  __shared__ uint32_t red[2 * kWarps];
+  __shared__ uint32_t red[2 * kWarps + 2];
   __shared__ uint8_t rvalid[kStages][kTile];
   __shared__ float s_qn;
   __shared__ int s_T;
@@ -288,7 +406,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   const int lists_cap = (kUBytes - lists_at) / 2;
   uint32_t* offs = reinterpret_cast<uint32_t*>(U + kUOffs);
   int32_t* lpos = reinterpret_cast<int32_t*>(U + kUListPos);
-  float* lest = reinterpret_cast<float*>(U + kUListEst);
   uint16_t* stK = reinterpret_cast<uint16_t*>(U + kUStageK);
   uint16_t* stV = reinterpret_cast<uint16_t*>(U + kUStageV);
 
@@ -370,9 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   } else if (warp > kSub + 1) {
     // warm L2 with the window rows this block's attention will read
     if (a.out != nullptr) {
-      const int64_t w_lo = a.nwin * r / cs, w_hi = a.nwin * (r + 1) / cs;
+      const int64_t w_lo = cut_at(a.wcut, r), w_hi = cut_at(a.wcut, r + 1);
       const int ring = a.s.local + a.s.ubuf;
-      const uint32_t nmod = ring > 0 ? (uint32_t)(a.N % ring) : 0u;
+      const uint32_t nmod = a.nmod;
       for (int64_t row = w_lo + (tid - (kSub + 2) * 32); row < w_hi; row += kThreads - (kSub + 2) * 32) {
         int64_t slot = row;
         if (row >= a.nsink) {
@@ -601,12 +718,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   // The candidates are the first C keys by (votes desc, index asc): with T
   // the largest vote value whose suffix count reaches C, every key above T
   // and the lowest-index keys equal to T, up to C.
+  __syncthreads();
+  if (tid < kMaxBins) {
+    const uint32_t mine = hist[tid];
+    for (int q = 0; q < cs; ++q) dsmem_st_u32(dsmem_addr(&hall[r][tid], q), mine);
+  }
   cluster_sync();
   uint32_t bef = 0;
   if (tid < kMaxBins) {
     uint32_t v[kClusterMax];
 #pragma unroll
-    for (int q = 0; q < kClusterMax; ++q) v[q] = q < cs ? dsmem_u32(hist + tid, q) : 0u;
+    for (int q = 0; q < kClusterMax; ++q) v[q] = q < cs ? hall[q][tid] : 0u;
     uint32_t all = 0;
 #pragma unroll
     for (int q = 0; q < kClusterMax; ++q) {
@@ -715,7 +837,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         while (m) {
           const int j = (31 - __clz(m & (0u - m))) >> 3;  // lowest flagged byte
           m &= m - 1;
-          out[pos++] = pbase + 4 * w + j;
+          const int32_t p = pbase + 4 * w + j;
+          out[pos++] = p;
         }
       }
       eq_allow = max64(0, eq_allow - (int64_t)eq_tot);
@@ -728,8 +851,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 
   // ---- 3. estimates: block r takes the slice [C r / cs, C (r + 1) / cs) ------
   trace_block(a.trace, kTkDecode3, 0);
-  const int64_t s_lo = a.C * r / cs, s_hi = a.C * (r + 1) / cs;
+  const int64_t s_lo = cut_at(a.ccut, r), s_hi = cut_at(a.ccut, r + 1);
   const uint32_t nown = (uint32_t)(s_hi - s_lo);
+  const bool keys_staged = a.C <= kSelCap;  // every block holds all C order keys
+  uint32_t keys_at[kClusterMax];
+#pragma unroll
+  for (int q = 0; q < kClusterMax; ++q) keys_at[q] = q < cs ? dsmem_addr(U + kUKeys, q) : 0u;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
   {
     // Warp w takes candidates 32 w + 1024 k + lane.  Its 32 records of a
     // round are copied into the warp's own 4 KB of shared memory with each
@@ -738,12 +866,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     const uint8_t* rec = a.t.rec + sh * a.t.rcap * kRecBytes;
     const float qn = s_qn;
     uint4* wslot = reinterpret_cast<uint4*>(U + kURecSlots) + warp * 32 * 8;
+    auto cand_pos = [&](uint32_t j) { return __ldcg(a.cand_idx + cq + s_lo + j); };
     for (uint32_t c0 = 32 * warp; c0 < nown; c0 += kThreads) {
       const uint32_t i = c0 + lane;
-      const int32_t pm = i < nown ? __ldcg(a.cand_idx + cq + s_lo + i) : -1;
+      const int32_t pm = i < nown ? cand_pos(i) : -1;
       // the next round's records start on their way to L2 now
       const uint32_t inx = i + kThreads;
-      if (inx < nown) prefetch_l2(rec + (int64_t)(__ldcg(a.cand_idx + cq + s_lo + inx) - a.s.sink) * kRecBytes);
+      if (inx < nown) prefetch_l2(rec + (int64_t)(cand_pos(inx) - a.s.sink) * kRecBytes);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int rc = 4 * u + (lane >> 3), piece = lane & 7;
@@ -760,39 +889,77 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         for (int u = 0; u < 8; ++u) x[u] = wslot[lane * 8 + (u ^ (lane & 7))];
         const float e = estimate(x, tq, qn);
         a.cand_est[cq + s_lo + i] = e;
-        if (i < kListCap) {
-          lpos[i] = pm;
-          lest[i] = e;
+        if (i < kListCap) lpos[i] = pm;
+        const uint32_t key = order_key(e);
+        kmn = min(kmn, key);
+        kmx = max(kmx, key);
+        if (keys_staged) {
+#pragma unroll
+          for (int q = 0; q < kClusterMax; ++q)
+            if (q < cs) dsmem_st_u32(keys_at[q] + 4u * (uint32_t)(s_lo + i), key);
         }
       }
       __syncwarp();  // the slots are reused by the next round
     }
   }
+  kmn = __reduce_min_sync(kFull, kmn);
+  kmx = __reduce_max_sync(kFull, kmx);
+  if (lane == 0) {
+    red[warp] = kmn;
+    red[kWarps + warp] = kmx;
+  }
   __syncthreads();
+  if (tid < cs) {
+    // the block's smallest and largest key, to every block
+    uint32_t x = 0xffffffffu, y = 0u;
+#pragma unroll 8
+    for (int w = 0; w < kWarps; ++w) {
+      x = min(x, red[w]);
+      y = max(y, red[kWarps + w]);
+    }
+    dsmem_st_u32(dsmem_addr(&skey_mm[r][0], tid), x);
+    dsmem_st_u32(dsmem_addr(&skey_mm[r][1], tid), y);
+  }
   trace_block(a.trace, kTkDecode1, 1);
   trace_mark(tr, kTrDecode3);
 
+  trace_block(a.trace, kTkDecode1, 2);
+  cluster_sync();  // every estimate and order key of the cluster, and their range, is in place
+  trace_block(a.trace, kTkDecode3, 1);
+
   // ---- 4. top-k ------------------------------------------------------------
   // The k_eff-th best candidate by (estimate desc, position asc): every
-  // block finds the k-th key over all C estimates, counts the keys above it
-  // and equal to it in the slices before its own, and so knows where its
-  // slice's selected entries go and how many of its keys equal to the k-th
-  // key it keeps (equal keys go to the lowest positions first).
+  // block finds the k_eff-th largest order key P over all C estimates and
+  // how many keys equal to P are taken (the lowest positions first).  The
+  // taken entries in list (position) order are the top-k.  Block r counts
+  // the entries taken before its slice, so knows where its slice's taken
+  // entries go, writes them, and attends over them (with its share of the
+  // window rows).
   const bool select_all = a.k_eff >= a.C;  // the same in every block
-  uint32_t prefix = 0, my_eq_take = 0;
-  int64_t out_off = s_lo;
+  const uint32_t* keys = reinterpret_cast<const uint32_t*>(U + kUKeys);
+  auto key_of = [&](int64_t i) -> uint32_t {
+    return keys_staged ? keys[i] : order_key(__ldcg(a.cand_est + cq + i));
+  };
+  uint32_t P = 0, remaining = 0;
   if (!select_all) {
-    cluster_sync();  // every estimate is written
-    trace_block(a.trace, kTkDecode3, 1);
-    uint32_t remaining;
-    prefix = select_kth(a.C, a.k_eff, a.cand_est + cq, U, tmp, &remaining);
-    trace_block(a.trace, kTkDecode3, 2);
-    const uint32_t* keys = reinterpret_cast<const uint32_t*>(U + kUKeys);
+    uint32_t x = 0xffffffffu, y = 0u;
+#pragma unroll
+    for (int q = 0; q < kClusterMax; ++q)
+      if (q < cs) {
+        x = min(x, skey_mm[q][0]);
+        y = max(y, skey_mm[q][1]);
+      }
+    P = select_kth(key_of, a.C, a.k_eff, x, y, U, tmp, &remaining);
+  }
+  trace_block(a.trace, kTkDecode3, 2);
+  int64_t out_off = s_lo;  // place of the slice's first taken entry
+  uint32_t eq_take = 0;    // keys equal to P that the slice takes
+  if (!select_all) {
     uint32_t gtb = 0, eqb = 0;
-    for (int i = tid; i < (int)s_lo; i += kThreads) {
-      const uint32_t k = a.C <= kSelCap ? keys[i] : order_key(__ldcg(a.cand_est + cq + i));
-      gtb += k > prefix ? 1u : 0u;
-      eqb += k == prefix ? 1u : 0u;
+    for (int64_t i = tid; i < s_lo; i += kThreads) {
+      const uint32_t k = key_of(i);
+      gtb += k > P ? 1u : 0u;
+      eqb += k == P ? 1u : 0u;
     }
     gtb = __reduce_add_sync(kFull, gtb);
     eqb = __reduce_add_sync(kFull, eqb);
@@ -803,50 +970,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     __syncthreads();
     gtb = 0;
     eqb = 0;
-#pragma unroll
+#pragma unroll 8
     for (int w = 0; w < kWarps; ++w) {
       gtb += red[w];
       eqb += red[kWarps + w];
     }
     out_off = gtb + min(eqb, remaining);
-    my_eq_take = remaining > eqb ? remaining - eqb : 0u;
+    eq_take = remaining > eqb ? remaining - eqb : 0u;
+    __syncthreads();  // red is reused below
   }
-  trace_block(a.trace, kTkDecode3, 3);
-  trace_mark(tr, kTrDecodeFine + 20);
+  // the slice in order: thread t owns entries [t per, t per + per) of it
+  int32_t* selpos = reinterpret_cast<int32_t*>(U + kUSelPos);
+  uint32_t nsel;  // entries the slice takes
   {
-    // ordered output: thread t owns entries [t * per, t * per + per) of the slice
-    auto est_of = [&](uint32_t i) { return i < kListCap ? lest[i] : __ldcg(a.cand_est + cq + s_lo + i); };
     const uint32_t per = (nown + kThreads - 1) / kThreads;
     const uint32_t i0 = min(nown, tid * per), i1 = min(nown, i0 + per);
-    uint32_t n_eq = 0, n_gt = 0;
+    uint32_t n_gt = 0, n_eq = 0;
     for (uint32_t i = i0; i < i1; ++i) {
-      const uint32_t key = order_key(est_of(i));
-      n_eq += key == prefix ? 1u : 0u;
-      n_gt += key > prefix ? 1u : 0u;
+      const uint32_t k = key_of(s_lo + i);
+      n_gt += select_all || k > P ? 1u : 0u;
+      n_eq += !select_all && k == P ? 1u : 0u;
     }
-    uint32_t tot_eq;
-    const uint32_t eq_rank0 = select_all ? 0u : block_excl_scan(n_eq, tmp, &tot_eq);
-    const uint32_t eq_take = select_all ? 0u : (uint32_t)max64(0, min64(n_eq, (int64_t)my_eq_take - eq_rank0));
-    const uint32_t cnt = select_all ? i1 - i0 : n_gt + eq_take;
-    uint32_t tot_sel;
-    uint32_t opos = block_excl_scan(cnt, tmp, &tot_sel);
-    int32_t* oi = a.topk_idx + (int64_t)sq * a.k + out_off;
-    float* os = a.topk_score ? a.topk_score + (int64_t)sq * a.k + out_off : nullptr;
-    uint32_t eq_seen = 0;
+    uint32_t gt_b = n_gt, eq_b = n_eq, gt_tot, eq_tot;
+    block_excl_scan2(gt_b, eq_b, red, gt_tot, eq_tot);
+    nsel = gt_tot + min(eq_tot, eq_take);
+    uint32_t j = gt_b + min(eq_b, eq_take), eq_seen = eq_b;
     for (uint32_t i = i0; i < i1; ++i) {
-      const float e = est_of(i);
-      const uint32_t key = order_key(e);
-      bool take = select_all || key > prefix;
-      if (!select_all && key == prefix) {
-        take = eq_seen < eq_take;
-        ++eq_seen;
-      }
+      const uint32_t k = key_of(s_lo + i);
+      bool take = select_all || k > P;
+      if (!select_all && k == P) take = eq_seen++ < eq_take;
       if (take) {
-        if (out_off + opos < a.k_eff) {  // always, unless the counts above disagree
-          oi[opos] = i < kListCap ? lpos[i] : __ldcg(a.cand_idx + cq + s_lo + i);
-          if (os) os[opos] = e;
+        const int32_t pos = i < kListCap ? lpos[i] : __ldcg(a.cand_idx + cq + s_lo + i);
+        // the estimate from its key, except for the one key +0 and -0 share
+        const float e = keys_staged && k != order_key(0.f) ? key_to_float(k) : __ldcg(a.cand_est + cq + s_lo + i);
+        if (out_off + j < a.k_eff) {  // always, unless the counts above disagree
+          a.topk_idx[(int64_t)sq * a.k + out_off + j] = pos;
+          if (a.topk_score) a.topk_score[(int64_t)sq * a.k + out_off + j] = e;
         }
-        ++opos;
+        if (j < kListCap) selpos[j] = pos;
+        ++j;
       }
     }
     if (r == 0) {
@@ -856,49 +1018,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       }
     }
   }
-  if (a.out != nullptr && tid < kDim) zs[tid] = qs[tid] * a.qscale;  // scaled q for the attention
-  trace_block(a.trace, kTkDecode1, 2);
+  trace_block(a.trace, kTkDecode3, 3);
   trace_mark(tr, kTrDecode4);
-  // the top-k of the whole cluster is written; no block reads another's
-  // shared memory after this point until the attention merge
-  cluster_sync();
-  trace_block(a.trace, kTkDecode1, 3);
 
   // ---- 5. sparse attention ---------------------------------------------------
   if (a.out != nullptr) {
-    // block r: an even share of the window rows and of the retrieved rows
-    const int64_t wl = a.nwin * r / cs, wh = a.nwin * (r + 1) / cs;
-    const int64_t kl = a.k_eff * r / cs, kh = a.k_eff * (r + 1) / cs;
+    // the block's rows: its share of the window rows, then the entries its slice took
+    const int64_t wl = cut_at(a.wcut, r), wh = cut_at(a.wcut, r + 1);
     const int nwb = (int)(wh - wl);
-    const int nrows = nwb + (int)(kh - kl);
-    auto grow = [&](int t) -> int64_t { return t < nwb ? wl + t : a.nwin + kl + (t - nwb); };
+    const int nrows = nwb + (int)min64(nsel, a.k_eff - out_off);
     const int ring = a.s.local + a.s.ubuf;
-    // where each of the block's rows comes from, resolved once (all loads in
-    // flight): element offset into the window arrays (kSrcWindow set) or the
-    // Retrieval-zone store; kSrcFresh: the step's own token; -1: no row
+    // where each row comes from: element offset into the window arrays
+    // (kSrcWindow set) or the Retrieval-zone store; kSrcFresh: the step's
+    // own token; -1: no row
     constexpr int64_t kSrcWindow = int64_t(1) << 62, kSrcFresh = int64_t(1) << 61;
-    const uint32_t nmod = ring > 0 ? (uint32_t)(a.N % ring) : 0u;  // ring slot of the first Local token
-    auto row_source = [&](int64_t row) -> int64_t {
-      if (row < a.nwin) {
-        int64_t slot = row, pos = row;
-        if (row >= a.nsink) {
-          uint32_t x = nmod + (uint32_t)(row - a.nsink);  // < 2 ring: the window holds at most ring tokens
-          if (x >= (uint32_t)ring) x -= (uint32_t)ring;
-          slot = a.s.sink + x;
-          pos = a.s.sink + a.N + (row - a.nsink);
-        }
-        if (pos == a.new_pos) return kSrcFresh;
-        return kSrcWindow | ((sh * a.kv.win + slot) * kDim);
+    const uint32_t nmod = a.nmod;
+    auto window_source = [&](int64_t row) -> int64_t {
+      int64_t slot = row, pos = row;
+      if (row >= a.nsink) {
+        uint32_t x = nmod + (uint32_t)(row - a.nsink);  // < 2 ring: the window holds at most ring tokens
+        if (x >= (uint32_t)ring) x -= (uint32_t)ring;
+        slot = a.s.sink + x;
+        pos = a.s.sink + a.N + (row - a.nsink);
       }
-      const int64_t pos = __ldcg(a.topk_idx + (int64_t)sq * a.k + (row - a.nwin));
+      if (pos == a.new_pos) return kSrcFresh;
+      return kSrcWindow | ((sh * a.kv.win + slot) * kDim);
+    };
+    auto retrieved_source = [&](int64_t pos) -> int64_t {
       if (pos >= a.s.sink && pos < a.s.sink + a.N) return (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
       if (pos >= 0) atomicOr(a.status, kStatusBadIndex);
       return -1;
     };
-    constexpr int kRowTab = kListCap / 2;
-    int64_t* rsrc = reinterpret_cast<int64_t*>(lpos);
-    for (int t = tid; t < min(nrows, kRowTab); t += kThreads) rsrc[t] = row_source(grow(t));
+    // rows past the table: resolved when they are loaded (the slice's top-k
+    // entries are in global memory by then)
+    auto row_source = [&](int t) -> int64_t {
+      return t < nwb ? window_source(wl + t)
+                     : retrieved_source(__ldcg(a.topk_idx + (int64_t)sq * a.k + out_off + (t - nwb)));
+    };
+    int64_t* rsrc = reinterpret_cast<int64_t*>(U + kUKeys);  // the order keys are no longer read
+    __syncthreads();  // the slice's taken positions are in place; every key read is done
+    for (int t = tid; t < min(nrows, kRowTab); t += kThreads) {
+      const int j = t - nwb;
+      rsrc[t] = t < nwb ? window_source(wl + t)
+                        : retrieved_source(j < kListCap ? selpos[j]
+                                                        : __ldcg(a.topk_idx + (int64_t)sq * a.k + out_off + j));
+    }
+    if (tid < kDim) zs[tid] = qs[tid] * a.qscale;  // scaled q for the attention
     __syncthreads();
+    trace_block(a.trace, kTkDecode1, 3);
     // Rounds of kRound rows through two halves of the stage area: round
     // rd + 2 loads into the half that round rd has just used, so two rounds
     // are in flight.  A round's copies: 16 threads per row, one 16-byte piece
@@ -917,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         uint16_t* vd = stV + (half * kRound + rr) * kKStride + 8 * ch;
         const int rl = rd * kRound + rr;
         int64_t src = -1;
-        if (rd < nrounds && rl < nrows) src = rl < kRowTab ? rsrc[rl] : row_source(grow(rl));
+        if (rd < nrounds && rl < nrows) src = rl < kRowTab ? rsrc[rl] : row_source(rl);
         if (src == kSrcFresh) {
           // the step's own token: from the caller's k/v, converted as the append stores it
           *reinterpret_cast<uint4*>(kd) = load8_as_bf16(a.k_new, a.kvdtype, sh * kDim + 8 * ch);
@@ -1013,8 +1180,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) lb += __shfl_xor_sync(kFull, lb, o);
       if (lane == 0) {
-        part[0] = mx;
-        part[1] = lb;
+        // the block's (max, sum), to block 0
+        dsmem_st_u32(dsmem_addr(&pall[r][0], 0), __float_as_uint(mx));
+        dsmem_st_u32(dsmem_addr(&pall[r][1], 0), __float_as_uint(lb));
       }
     }
     __syncthreads();
@@ -1022,17 +1190,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       float ob = 0.f;
 #pragma unroll 8
       for (int w2 = 0; w2 < kWarps; ++w2) ob += wo[w2 * kDim + tid] * wml[2 * w2 + 1];
-      part[4 + tid] = ob;
+      dsmem_st_u32(dsmem_addr(&pall[r][4 + tid], 0), __float_as_uint(ob));
     }
+    // every block's partial is in block 0; only block 0 reads shared memory after this
     cluster_sync();
     trace_mark(tr, kTrDecode5);
     if (r == 0 && tid < kDim) {
       float mm[kClusterMax], ll[kClusterMax], oo[kClusterMax];
 #pragma unroll
       for (int q = 0; q < kClusterMax; ++q) {
-        mm[q] = q < cs ? __uint_as_float(dsmem_u32(part, q)) : 0.f;
-        ll[q] = q < cs ? __uint_as_float(dsmem_u32(part + 1, q)) : 0.f;
-        oo[q] = q < cs ? __uint_as_float(dsmem_u32(part + 4 + tid, q)) : 0.f;
+        mm[q] = q < cs ? pall[q][0] : 0.f;
+        ll[q] = q < cs ? pall[q][1] : 0.f;
+        oo[q] = q < cs ? pall[q][4 + tid] : 0.f;
       }
       float Mx = -FLT_MAX;
 #pragma unroll
@@ -1049,8 +1218,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       }
       a.out[(int64_t)sq * kDim + tid] = __float2bfloat16_rn(Lt > 0.f ? ot / Lt : 0.f);
     }
-    // every block's shared memory stays until block 0 has read it
-    cluster_sync();
     trace_block(a.trace, kTkDecode2, 1);
   }
 
@@ -1098,6 +1265,15 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.cmax = ra.cmax;
   a.nsink = L.nsink;
   a.nwin = L.nwin;
+  for (int q = 0; q <= kClusterMax; ++q) {
+    const int qq = q < cs ? q : cs;
+    a.ccut[q] = ra.C * qq / cs;
+    a.wcut[q] = L.nwin * qq / cs;
+  }
+  {
+    const int ring = ra.s.local + ra.s.ubuf;
+    a.nmod = ring > 0 ? (uint32_t)(ra.N % ring) : 0u;
+  }
   a.q = L.q;
   a.qdtype = L.qdtype;
   a.qscale = 1.4426950408889634f / sqrtf((float)kDim);
