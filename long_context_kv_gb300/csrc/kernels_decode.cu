@@ -55,6 +55,7 @@ static_assert(kTile * 16 == kThreads, "16 threads per staged row");
 static_assert(2 * kWarps == kTile, "two rows of a tile per warp");
 static_assert(kChunk / kThreads == 16, "one 16-byte vote vector per thread and chunk");
 static_assert(2 * kThreads == kSelBins, "two radix digits per thread");
+static_assert(kMaxBins % 32 == 0 && kMaxBins <= kThreads, "one thread per vote value, whole warps");
 
 // byte offsets inside the phase-shared dynamic region
 constexpr int kUVotes = 0;                                    // u8 [kVoteSlots][kChunk]
@@ -659,9 +660,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     }
     __syncthreads();
     if (g0 == c_lo) trace_mark(tr, kTrDecodeFine + 1);
-    // votes out; histogram: counts of votes 1..7 by bit planes (the bytes
-    // below 8), larger votes one by one (thread t: 16 keys of each chunk of
-    // the group)
+    // votes out; histogram: votes 1..7 (the bytes below 8) by bit planes,
+    // larger votes one by one.  Thread t: 16 keys of each chunk of the group,
+    // as 4 G words; the planes of word w sit at bits 8 j + w (byte j), so one
+    // population count covers all of the thread's keys.
+    uint32_t P0 = 0, P1 = 0, P2 = 0;
     for (int g = 0; g < ng; ++g) {
       const int vi = g * kThreads + tid;
       uint4* vp = reinterpret_cast<uint4*>(span) + vi;
@@ -672,19 +675,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t x = ws[k];
-        const uint32_t v80 = first_bytes(glen - (16 * vi + 4 * k));
-        const uint32_t v01 = v80 >> 7;
+        const uint32_t v01 = first_bytes(glen - (16 * vi + 4 * k)) >> 7;
         uint32_t big = (bytes_nonzero(x & 0xf8f8f8f8u) >> 7) & v01;  // valid bytes >= 8
         const uint32_t lo = v01 & ~big;
-        const uint32_t p0 = x & lo, p1 = (x >> 1) & lo, p2 = (x >> 2) & lo;
-        cnt[0] += __popc(p0 & ~p1 & ~p2);
-        cnt[1] += __popc(~p0 & p1 & ~p2);
-        cnt[2] += __popc(p0 & p1 & ~p2);
-        cnt[3] += __popc(~p0 & ~p1 & p2);
-        cnt[4] += __popc(p0 & ~p1 & p2);
-        cnt[5] += __popc(~p0 & p1 & p2);
-        cnt[6] += __popc(p0 & p1 & p2);
-        nz_mine += __popc(bytes_nonzero(x) & v80);
+        const int w = 4 * g + k;
+        P0 |= (x & lo) << w;
+        P1 |= ((x >> 1) & lo) << w;
+        P2 |= ((x >> 2) & lo) << w;
+        nz_mine += __popc(big);
         while (big) {
           const int j = (31 - __clz(big & (0u - big))) >> 3;
           big &= big - 1;
@@ -694,6 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         }
       }
     }
+    cnt[0] += __popc(P0 & ~P1 & ~P2);
+    cnt[1] += __popc(~P0 & P1 & ~P2);
+    cnt[2] += __popc(P0 & P1 & ~P2);
+    cnt[3] += __popc(~P0 & ~P1 & P2);
+    cnt[4] += __popc(P0 & ~P1 & P2);
+    cnt[5] += __popc(~P0 & P1 & P2);
+    cnt[6] += __popc(P0 & P1 & P2);
+    nz_mine += __popc(P0 | P1 | P2);
   }
   {
 #pragma unroll
@@ -779,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     gtb = 0;
     eqb = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kMaxBins / 32; ++w) {  // the warps holding vote values
       gtb += red[w];
       eqb += red[kWarps + w];
     }
@@ -968,13 +974,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       red[kWarps + warp] = eqb;
     }
     __syncthreads();
-    gtb = 0;
-    eqb = 0;
-#pragma unroll 8
-    for (int w = 0; w < kWarps; ++w) {
-      gtb += red[w];
-      eqb += red[kWarps + w];
+    if (warp == 0) {
+      const uint32_t g = __reduce_add_sync(kFull, red[lane]), e = __reduce_add_sync(kFull, red[kWarps + lane]);
+      __syncwarp();
+      if (lane == 0) {
+        red[0] = g;
+        red[kWarps] = e;
+      }
     }
+    __syncthreads();
+    gtb = red[0];
+    eqb = red[kWarps];
     out_off = gtb + min(eqb, remaining);
     eq_take = remaining > eqb ? remaining - eqb : 0u;
     __syncthreads();  // red is reused below
