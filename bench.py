@@ -224,8 +224,12 @@ def run_ours(args, rank, world):
         L["ctx"].paris_decode_step(L["kn"][j], L["vn"][j], L["qs"][j], L["idx"], L["sc"], L["out"])
 
     if args.profile_case:
+        # the decode steps, then as many dense-attention calls on the same caches
         for i in range(args.warmup + args.steps):
             step(i)
+        for i in range(args.warmup + args.steps):
+            L = layers[i % nl]
+            L["ctx"].paris_dense_attend(L["qs"][0], L["out"])
         torch.cuda.synchronize()
         return {"profile_case": DESCRIPTION[args.workload], "layers": nl, "steps": args.warmup + args.steps}
 
@@ -321,9 +325,14 @@ def run_ours(args, rank, world):
         L["step"] = j + 1
         L["ctx"].paris_append_decode(L["kn"][j], L["vn"][j])
 
+    def call_dense(L, _):
+        L["ctx"].paris_dense_attend(L["qs"][L["step"]], L["out"])
+
     keys_retrieve = sum(L["ctx"].paris_get_state()["N"] * b * hkv for L in layers) / nl
     ms_retrieve = timed_calls(call_retrieve)
     ms_attend = timed_calls(call_attend)
+    ms_dense = timed_calls(call_dense)
+    tokens_dense = sum(L["ctx"].paris_get_state()["T"] for L in layers) / nl
     ms_append = timed_calls(call_append)
 
     # per-step device time distribution: events around each eager step
@@ -454,6 +463,13 @@ def run_ours(args, rank, world):
         "us_per_decode_step_eager_p10_p50_p90": [round(pct(0.1), 2), round(pct(0.5), 2), round(pct(0.9), 2)],
         "us_retrieve": 1e3 * ms_retrieve, "keys_per_s_retrieve": job_throughput(keys_retrieve, world, ms_retrieve),
         "us_sparse_attend": 1e3 * ms_attend, "us_append": 1e3 * ms_append,
+        # the full-attention comparator on the same cache: every K/V row once per step
+        "dense_attention": {
+            "us_per_step": 1e3 * ms_dense,
+            "decode_step_speedup": ms_dense / (ms / args.steps),
+            "hbm_gbs": b * hkv * tokens_dense * 4 * d / (ms_dense * 1e-3) / 1e9,
+            "hbm_frac": round(b * hkv * tokens_dense * 4 * d / (ms_dense * 1e-3) / 1e9 / peak, 4),
+        },
         "recall_at_k": recall,
         "kernels": kernels,
         "roofline": roof,

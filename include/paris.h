@@ -167,6 +167,22 @@ paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtyp
 paris_status paris_sparse_attend_noalloc(paris_ctx* ctx, const void* q, paris_dtype dtype,
                                          const int32_t* topk_idx, void* out_bf16, void* stream);
 
+/* Dense decode attention over every cached token -- Sink, Retrieval zone,
+ * Local and Update Buffer -- for each query head: the full-attention
+ * baseline ParisKV's decode throughput is compared against (ParisKV,
+ * Experiments, "Efficiency": throughput over full attention).  Same
+ * arithmetic as paris_sparse_attend (o = softmax(K q / sqrt(d)) V, float32
+ * accumulation, bf16 output) over all T rows instead of the selected ones;
+ * Retrieval-zone rows are read in place (mapped host memory when
+ * retrieval_on_host = 1).  q: device, dtype, [batch][Hq][d]; out: device
+ * bf16 [batch][Hq][d] (zeros while the cache is empty).  Streams every K/V
+ * row once per call for all query heads of its KV head (at most 16 query
+ * heads per KV head, else PARIS_EINVAL), split over about one block per SM;
+ * the query enters the products as two bf16 parts, the softmax weights
+ * rounded to bf16.
+ * Its scratch is allocated by paris_create.                                 */
+paris_status paris_dense_attend(paris_ctx* ctx, const void* q, paris_dtype dtype, void* out_bf16, void* stream);
+
 /* One decode step: paris_append_decode(k, v), then paris_retrieve(q, ...),
  * then paris_sparse_attend(q, topk_idx, out), with the same arguments.  The
  * top-k positions, their estimates and k_eff are bit for bit those of the
@@ -231,7 +247,8 @@ typedef enum {
                                    attention and the append of the step's token      */
   PARIS_KERNEL_ATTEND = 5,      /* standalone sparse attention and the merge of its splits */
   PARIS_KERNEL_FILL = 6,        /* empty-result fill                                     */
-  PARIS_KERNEL_COUNT = 7
+  PARIS_KERNEL_DENSE = 7,       /* dense comparator: attention over every cached token   */
+  PARIS_KERNEL_COUNT = 8
 } paris_kernel;
 
 /* Cumulative kernel launches of this context since paris_create, per

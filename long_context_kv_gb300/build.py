@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libparis.so")
-SOURCES = ["paris_api.cu", "kernels_cache.cu", "kernels_decode.cu", "kernels_attend.cu"]
+SOURCES = ["paris_api.cu", "kernels_cache.cu", "kernels_decode.cu", "kernels_attend.cu", "kernels_dense.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

@@ -1,0 +1,343 @@
+// Dense decode attention over every cached token (Sink, Retrieval zone,
+// Local, Update Buffer): the full-attention baseline that ParisKV's decode
+// throughput is measured against (ParisKV -- Experiments, "Efficiency":
+// throughput over full attention; the dense path reads every K/V row once
+// per step, the sparse path a few percent of them).
+//
+// Streaming split-K flash decoding, bound by the read of K and V (HBM, or
+// C2C for a Retrieval zone in pinned host memory).  Block (split, sequence
+// x KV head) reads the K and V rows of its token range once for all G query
+// heads of the KV head (GQA), in tiles of 128 rows through a 3-deep ring of
+// 16-byte asynchronous copies.  The G heads are the rows of bf16 mma tiles
+// (m16n8k16, float32 accumulation; the query as two bf16 parts): each
+// warp takes 16 rows of a tile, S = Q K^T, an online softmax per head, and
+// O += P V with P rounded to bf16.  The warps merge in shared memory, the
+// block writes one partial (max, sum, o) per head, and the last block of a
+// (sequence, KV head) to finish merges the splits (an atomic counter after
+// a memory fence; nothing waits).  The tensor pipe is a small fraction of
+// the time: it only keeps the per-row instruction count low enough for the
+// copies to stream at the memory's rate.
+#include <float.h>
+
+#include "paris_device.cuh"
+
+namespace paris {
+namespace {
+
+constexpr int kDThreads = 256;
+constexpr int kDWarps = kDThreads / 32;
+constexpr int kDRowsW = 16;                // rows per warp and tile: one 16-deep k step of P V
+constexpr int kDTile = kDRowsW * kDWarps;  // 128 rows per tile
+constexpr int kDStages = 3;
+constexpr int kDStride = kDim + 8;         // bf16 per staged row: 272 B, conflict-free 8-row matrix loads
+constexpr int kDMaxHeads = 16;             // query heads per block: the rows of one mma tile
+static_assert(kDTile * 16 == kDThreads * 8, "16-byte pieces: 8 per thread and tile for K, 8 for V");
+
+constexpr size_t kDenseSmem = (size_t)2 * kDStages * kDTile * kDStride * sizeof(uint16_t);
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Four 8x8 bf16 matrices from shared memory (lane i gives the address of
+// row i % 8 of matrix i / 8), plain or transposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+// d += a b: a 16x16 bf16 (rows: query heads), b 16x8 bf16, d 16x8 float32.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};\n"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Block (split, sequence x KV head): the G <= 16 query heads of the KV head
+// are the rows of the mma tiles (rows G .. 15 are zero).  Warp w takes rows
+// 16 w .. 16 w + 15 of every 128-row tile: S = Q K^T over them (two 8-row
+// n-tiles, eight 16-deep k steps), an online softmax per head, then
+// O += P V (one 16-deep k step, sixteen 8-wide n-tiles of output
+// dimensions).  Fragment layouts are those of mma.m16n8k16: lane l holds
+// rows l / 4 and l / 4 + 8 and columns 2 (l % 4), 2 (l % 4) + 1.
+__global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
+  extern __shared__ __align__(16) uint16_t dsm[];
+  uint16_t* stK = dsm;                                // [kDStages][kDTile][kDStride]
+  uint16_t* stV = dsm + kDStages * kDTile * kDStride;
+  __shared__ __align__(16) uint16_t qsh[2][kDMaxHeads][kDStride];  // the query as bf16 hi + lo
+  __shared__ float wml[kDWarps][kDMaxHeads][2];
+  __shared__ float fs[kDMaxHeads][kDWarps];
+  __shared__ int s_last;
+
+  const int split = blockIdx.x;
+  const int sh_i = blockIdx.y;  // sequence * Hkv + KV head
+  const int seq = sh_i / a.s.hkv, kvh = sh_i - seq * a.s.hkv;
+  const int64_t sh = (int64_t)sh_i;
+  const int G = a.s.g, qh0 = kvh * G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t t0 = (int64_t)split * a.rows_per_split;
+  const int64_t t1 = min64(a.T, t0 + a.rows_per_split);
+  const int nrows = (int)max64(0, t1 - t0);
+  const int ntiles = (nrows + kDTile - 1) / kDTile;
+  const int ring = a.s.local + a.s.ubuf;
+
+  // where token t's K/V row is: the Sink slots and the Local/Buffer ring of
+  // the window arrays, or the Retrieval-zone store
+  auto row_ptrs = [&](int64_t t, const __nv_bfloat16*& kp, const __nv_bfloat16*& vp) {
+    if (t < a.s.sink || t >= a.s.sink + a.N) {
+      const int64_t slot = t < a.s.sink ? t : a.s.sink + (t - a.s.sink) % ring;
+      kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
+      vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
+    } else {
+      kp = a.kv.st_k + (sh * a.kv.rcap + (t - a.s.sink)) * kDim;
+      vp = a.kv.st_v + (sh * a.kv.rcap + (t - a.s.sink)) * kDim;
+    }
+  };
+  // tile i into stage i % kDStages: thread t copies pieces (t % 16) of rows
+  // t / 16 + 16 j, j = 0 .. 7, of K and of V
+  auto issue = [&](int i) {
+    if (i < ntiles) {
+      const int st = i % kDStages, ch = tid & 15;
+#pragma unroll
+      for (int j = 0; j < kDTile * 16 / kDThreads; ++j) {
+        const int rr = (tid >> 4) + 16 * j;
+        const int64_t t = t0 + (int64_t)i * kDTile + rr;
+        uint16_t* kd = stK + (st * kDTile + rr) * kDStride + 8 * ch;
+        uint16_t* vd = stV + (st * kDTile + rr) * kDStride + 8 * ch;
+        if (t < t1) {
+          const __nv_bfloat16 *kp, *vp;
+          row_ptrs(t, kp, vp);
+          cp_async16(kd, kp + 8 * ch);
+          cp_async16(vd, vp + 8 * ch);
+        } else {
+          // past the split: zeros, so the products read finite values
+          *reinterpret_cast<uint4*>(kd) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vd) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kDStages - 1; ++i) issue(i);
+
+  // the KV head's queries, scaled by log2(e) / sqrt(d) (softmax in base 2),
+  // as the sum of two bf16 parts (hi, and the rest rounded again): the
+  // scores keep about 16 significant bits of q
+  for (int e = tid; e < kDMaxHeads * kDim; e += kDThreads) {
+    const int h = e / kDim, d = e % kDim;
+    const float v = h < G ? load1(a.q, a.qdtype, ((int64_t)seq * a.s.hq + qh0 + h) * kDim + d) * a.qscale : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    reinterpret_cast<__nv_bfloat16*>(qsh[0][h])[d] = hi;
+    reinterpret_cast<__nv_bfloat16*>(qsh[1][h])[d] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+  __syncthreads();
+  uint32_t qa[2][kDim / 16][4];  // A fragments of Q (hi, lo), one per 16-deep k step
+#pragma unroll
+  for (int p2 = 0; p2 < 2; ++p2)
+#pragma unroll
+    for (int ks = 0; ks < kDim / 16; ++ks)
+      ldsm_x4(qa[p2][ks], &qsh[p2][(lane & 7) + ((lane >> 3) & 1) * 8][16 * ks + (lane >> 4) * 8]);
+
+  const int hr = lane >> 2, cc = 2 * (lane & 3);  // fragment row (head hr and hr + 8), column pair
+  float M[2] = {-FLT_MAX, -FLT_MAX}, l[2] = {0.f, 0.f};
+  float o[kDim / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < kDim / 8; ++nt)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[nt][k] = 0.f;
+
+  for (int i = 0; i < ntiles; ++i) {
+    cp_async_wait_group<kDStages - 2>();  // tile i has landed
+    __syncthreads();                      // ... for every thread; stage (i - 1) % kDStages is free
+    issue(i + kDStages - 1);
+    const int st = i % kDStages;
+    const uint16_t* kt = stK + (st * kDTile + kDRowsW * warp) * kDStride;
+    const uint16_t* vt = stV + (st * kDTile + kDRowsW * warp) * kDStride;
+    // S = Q K^T for the warp's 16 rows: n-tile r holds rows 8 r .. 8 r + 7
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+#pragma unroll
+      for (int k2 = 0; k2 < kDim / 32; ++k2) {
+        // matrices: rows 8 r .. 8 r + 7, dims 32 k2 + 8 m .. + 7
+        uint32_t b[4];
+        ldsm_x4(b, kt + (8 * r + (lane & 7)) * kDStride + 32 * k2 + 8 * (lane >> 3));
+        mma16816(s[r], qa[0][2 * k2], b[0], b[1]);
+        mma16816(s[r], qa[1][2 * k2], b[0], b[1]);
+        mma16816(s[r], qa[0][2 * k2 + 1], b[2], b[3]);
+        mma16816(s[r], qa[1][2 * k2 + 1], b[2], b[3]);
+      }
+    }
+    // online softmax per head: rows past the split score -inf
+    const int64_t rbase = t0 + (int64_t)i * kDTile + kDRowsW * warp;
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (rbase + 8 * r + cc + (k & 1) >= t1) s[r][k] = -FLT_MAX;
+    float sc[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {  // head hr (hh = 0) and hr + 8 (hh = 1)
+      float mx = fmaxf(fmaxf(s[0][2 * hh], s[0][2 * hh + 1]), fmaxf(s[1][2 * hh], s[1][2 * hh + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+      const float Mn = fmaxf(M[hh], mx);
+      sc[hh] = exp2f(M[hh] - Mn);
+      float ps = 0.f;
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int k = 2 * hh; k < 2 * hh + 2; ++k) {
+          s[r][k] = s[r][k] == -FLT_MAX ? 0.f : exp2f(s[r][k] - Mn);
+          ps += s[r][k];
+        }
+      ps += __shfl_xor_sync(kFull, ps, 1);
+      ps += __shfl_xor_sync(kFull, ps, 2);
+      l[hh] = l[hh] * sc[hh] + ps;
+      M[hh] = Mn;
+    }
+    // O = O * scale + P V: P as the A fragment of one 16-deep k step over the rows
+    uint32_t pa[4];
+    pa[0] = pack_bf16(s[0][0], s[0][1]);
+    pa[1] = pack_bf16(s[0][2], s[0][3]);
+    pa[2] = pack_bf16(s[1][0], s[1][1]);
+    pa[3] = pack_bf16(s[1][2], s[1][3]);
+#pragma unroll
+    for (int n2 = 0; n2 < kDim / 16; ++n2) {
+      // matrices: rows 0-7 / 8-15 of the warp's rows, dims 16 n2 .. + 7 / + 8 .. + 15
+      uint32_t b[4];
+      ldsm_x4_t(b, vt + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kDStride + 16 * n2 + 8 * (lane >> 4));
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        float* on = o[2 * n2 + h2];
+        on[0] *= sc[0];
+        on[1] *= sc[0];
+        on[2] *= sc[1];
+        on[3] *= sc[1];
+        mma16816(o[2 * n2 + h2], pa, b[2 * h2], b[2 * h2 + 1]);
+      }
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // merge the warps: wo[w][head][d] in the (now idle) stage area
+  float* wo = reinterpret_cast<float*>(dsm);
+  static_assert((size_t)kDWarps * kDMaxHeads * kDim * sizeof(float) <= kDenseSmem, "warp partials fit the stage area");
+#pragma unroll
+  for (int nt = 0; nt < kDim / 8; ++nt) {
+    wo[(warp * kDMaxHeads + hr) * kDim + 8 * nt + cc] = o[nt][0];
+    wo[(warp * kDMaxHeads + hr) * kDim + 8 * nt + cc + 1] = o[nt][1];
+    wo[(warp * kDMaxHeads + hr + 8) * kDim + 8 * nt + cc] = o[nt][2];
+    wo[(warp * kDMaxHeads + hr + 8) * kDim + 8 * nt + cc + 1] = o[nt][3];
+  }
+  if ((lane & 3) == 0) {
+    wml[warp][hr][0] = M[0];
+    wml[warp][hr][1] = l[0];
+    wml[warp][hr + 8][0] = M[1];
+    wml[warp][hr + 8][1] = l[1];
+  }
+  __syncthreads();
+  float* part = a.part + (((int64_t)seq * a.s.hq + qh0) * a.nsplit_max + split) * kPartStride;
+  for (int h = warp; h < G; h += kDWarps) {
+    // head h's weights exp2(m_w - max) over the warps (0 for a warp without rows)
+    const float mw = lane < kDWarps ? wml[lane][h][0] : -FLT_MAX, lw = lane < kDWarps ? wml[lane][h][1] : 0.f;
+    float mx = lw > 0.f ? mw : -FLT_MAX;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    const float f = lw > 0.f ? exp2f(mw - mx) : 0.f;
+    if (lane < kDWarps) fs[h][lane] = f;
+    float lb = lw * f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lb += __shfl_xor_sync(kFull, lb, off);
+    if (lane == 0) {
+      part[(int64_t)h * a.nsplit_max * kPartStride] = mx;
+      part[(int64_t)h * a.nsplit_max * kPartStride + 1] = lb;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < G * kDim; e += kDThreads) {
+    const int h = e / kDim, d = e % kDim;
+    float ob = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDWarps; ++w) ob += wo[(w * kDMaxHeads + h) * kDim + d] * fs[h][w];
+    part[(int64_t)h * a.nsplit_max * kPartStride + 4 + d] = ob;
+  }
+
+  // the last split of the (sequence, KV head) merges all splits
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&a.counter[blockIdx.y], 1u) == (uint32_t)(gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int nsplit = gridDim.x;
+  for (int e = tid; e < G * kDim; e += kDThreads) {
+    const int h = e / kDim, d = e % kDim;
+    const float* ph = a.part + (((int64_t)seq * a.s.hq + qh0 + h) * a.nsplit_max) * kPartStride;
+    float Mx = -FLT_MAX;
+    for (int s0 = 0; s0 < nsplit; ++s0)
+      if (__ldcg(ph + (int64_t)s0 * kPartStride + 1) > 0.f) Mx = fmaxf(Mx, __ldcg(ph + (int64_t)s0 * kPartStride));
+    float Lt = 0.f, ot = 0.f;
+    for (int s0 = 0; s0 < nsplit; ++s0) {
+      const float mm = __ldcg(ph + (int64_t)s0 * kPartStride), ll = __ldcg(ph + (int64_t)s0 * kPartStride + 1);
+      if (ll > 0.f) {
+        const float f = exp2f(mm - Mx);
+        Lt += ll * f;
+        ot += __ldcg(ph + (int64_t)s0 * kPartStride + 4 + d) * f;
+      }
+    }
+    a.out[((int64_t)seq * a.s.hq + qh0 + h) * kDim + d] = __float2bfloat16_rn(Lt > 0.f ? ot / Lt : 0.f);
+  }
+  if (tid == 0) a.counter[blockIdx.y] = 0;
+}
+
+}  // namespace
+
+int dense_group(int g) { return g; }
+
+int dense_splits(const DenseArgs& a, int sm_count) {
+  // one block per SM over the whole grid, at least one tile per split
+  const int64_t units = (int64_t)a.s.batch * a.s.hkv;
+  const int64_t want = (sm_count + units - 1) / units;
+  const int64_t most = (a.T + kDTile - 1) / kDTile;
+  int64_t n = want < most ? want : most;
+  if (n < 1) n = 1;
+  return (int)(n < a.nsplit_max ? n : a.nsplit_max);
+}
+
+int64_t dense_rows_per_split(int64_t T, int nsplit) {
+  const int64_t r = (T + nsplit - 1) / nsplit;
+  return (r + kDTile - 1) / kDTile * kDTile;
+}
+
+cudaError_t launch_dense(const DenseArgs& a, int nsplit, cudaStream_t st) {
+  if (a.s.g > kDMaxHeads) return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_dense, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDenseSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(k_dense, dim3(nsplit, a.s.batch * a.s.hkv), dim3(kDThreads), kDenseSmem, st, a);
+}
+
+}  // namespace paris

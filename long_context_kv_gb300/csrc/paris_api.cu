@@ -43,6 +43,9 @@ struct paris_ctx {
   float* part;
   uint32_t* status;
   uint32_t* counters;  // [2][batch*Hq]: rerank blocks, attention splits finished
+  float* dense_part;   // dense comparator: [batch*Hq][dense_splits_max][kPartStride]
+  uint32_t* dense_counter;  // [batch*Hkv*groups]
+  int dense_splits_max, sm_count;
   uint64_t* trace;     // kTraceSlots phase timestamps
   bool tracing;        // PARIS_TRACE=1 in the environment at creation
   std::string err;
@@ -151,7 +154,7 @@ void lloyd_max_levels(int m, double lev[8], double thr[7]) {
 void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
                  c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status,
-                 c->counters, c->trace};
+                 c->counters, c->trace, c->dense_part, c->dense_counter};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_store) {
@@ -413,12 +416,26 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   TRY(dalloc(c, &c->status, sizeof(uint32_t), "status word"));
   TRY(dalloc(c, &c->counters, (size_t)2 * bq * sizeof(uint32_t), "block counters"));
   {
+    int dev = 0;
+    c->sm_count = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      c->sm_count = 1;
+    }
+    const int64_t units = bh * (f.n_q_heads / f.n_kv_heads / dense_group(f.n_q_heads / f.n_kv_heads));
+    c->dense_splits_max = (int)std::max<int64_t>(1, (4LL * c->sm_count + units - 1) / units);
+  }
+  TRY(dalloc(c, &c->dense_part, (size_t)bq * c->dense_splits_max * kPartStride * sizeof(float), "dense partials"));
+  TRY(dalloc(c, &c->dense_counter, (size_t)bq * sizeof(uint32_t), "dense counters"));
+  {
     const char* env = std::getenv("PARIS_TRACE");
     c->tracing = env != nullptr && env[0] == '1';
   }
   TRY(dalloc(c, &c->trace, (c->tracing ? kTraceWords : kTraceSlots) * sizeof(uint64_t), "phase trace"));
   cudaError_t e = cudaMemset(c->status, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (size_t)2 * bq * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->dense_counter, 0, (size_t)bq * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->trace, 0, (c->tracing ? kTraceWords : kTraceSlots) * sizeof(uint64_t));
   if (e != cudaSuccess) TRY(cuda_fail(c, e, "initialising the context"));
   e = cudaDeviceSynchronize();
@@ -503,6 +520,32 @@ paris_status paris_sparse_attend(paris_ctx* c, const void* q, paris_dtype dtype,
   const AttendArgs a = attend_args(c, topk_idx, out_bf16);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_ATTEND, s, [&] { return launch_attend(q, dtype, a, s); }));
+  return PARIS_OK;
+}
+
+paris_status paris_dense_attend(paris_ctx* c, const void* q, paris_dtype dtype, void* out_bf16, void* stream) {
+  if (!c) return fail(nullptr, PARIS_EINVAL, "ctx is NULL");
+  paris_status st = check_dtype(c, dtype);
+  if (st != PARIS_OK) return st;
+  if (!q || !out_bf16) return fail(c, PARIS_EINVAL, "q and out must not be NULL");
+  if (c->s.g > 16) return fail(c, PARIS_EINVAL, "paris_dense_attend: at most 16 query heads per KV head");
+  DenseArgs a;
+  a.s = c->s;
+  a.kv = c->kv;
+  a.T = c->T;
+  a.N = c->N;
+  a.q = q;
+  a.qdtype = dtype;
+  a.qscale = 1.4426950408889634f / std::sqrt((float)kDim);
+  a.part = c->dense_part;
+  a.nsplit_max = c->dense_splits_max;
+  a.counter = c->dense_counter;
+  a.out = static_cast<__nv_bfloat16*>(out_bf16);
+  int nsplit = dense_splits(a, c->sm_count);
+  a.rows_per_split = dense_rows_per_split(std::max<int64_t>(1, c->T), nsplit);
+  nsplit = (int)std::max<int64_t>(1, (c->T + a.rows_per_split - 1) / a.rows_per_split);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_DENSE, s, [&] { return launch_dense(a, nsplit, s); }));
   return PARIS_OK;
 }
 

@@ -154,6 +154,25 @@ struct AttendArgs {
 int attend_splits(const AttendArgs& a);
 cudaError_t launch_attend(const void* q, int dtype, const AttendArgs& a, cudaStream_t st);
 
+// ---- dense comparator: attention over every cached token --------------------
+struct DenseArgs {
+  Shape s;
+  KvStore kv;
+  int64_t T, N;               // tokens cached, Retrieval-zone tokens
+  int64_t rows_per_split;     // tokens per block (a multiple of the tile)
+  const void* q;
+  int qdtype;
+  float qscale;               // log2(e) / sqrt(d)
+  float* part;                // [batch*Hq][nsplit_max][kPartStride]
+  int nsplit_max;
+  uint32_t* counter;          // [batch*Hkv*groups] splits finished, reset by the last one
+  __nv_bfloat16* out;
+};
+int dense_group(int g);                              // query heads per block (all G of a KV head)
+int dense_splits(const DenseArgs& a, int sm_count);  // splits per (sequence, head group)
+int64_t dense_rows_per_split(int64_t T, int nsplit);
+cudaError_t launch_dense(const DenseArgs& a, int nsplit, cudaStream_t st);
+
 // Status word bits.
 constexpr uint32_t kStatusBadIndex = 1u;
 
