@@ -112,15 +112,18 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
+TRAFFIC_SOURCES = {"decode": ["kernels_decode.cu", "kernels_attend.cu"], "dense": ["kernels_dense.cu"]}
+
+
 def traffic_record(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the kernel source changed since the counters were taken."""
+    None when the kernel's source changed since the counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in TRAFFIC_SOURCES:
         return None
-    src = open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", "kernels_decode.cu"), "rb").read() + \
-        open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", "kernels_attend.cu"), "rb").read()
+    src = b"".join(open(os.path.join(ROOT, "long_context_kv_gb300", "csrc", f), "rb").read()
+                   for f in TRAFFIC_SOURCES[kernel])
     sha = hashlib.sha1(src).hexdigest()[:12]
     for line in open(path):
         parts = line.split()
@@ -469,6 +472,7 @@ def run_ours(args, rank, world):
             "decode_step_speedup": ms_dense / (ms / args.steps),
             "hbm_gbs": b * hkv * tokens_dense * 4 * d / (ms_dense * 1e-3) / 1e9,
             "hbm_frac": round(b * hkv * tokens_dense * 4 * d / (ms_dense * 1e-3) / 1e9 / peak, 4),
+            "traffic": traffic_record("dense"),
         },
         "recall_at_k": recall,
         "kernels": kernels,
