@@ -34,10 +34,27 @@ WORKLOADS = {
     # the small case the oracle finishes in seconds
     "tiny-4k": dict(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=128, n_sub=16, rho=4, sink=0, local=0,
                     update_buf=128, topk=64, cand_bp=1000, context=4096, layers=64),
+    # Qwen3-8B-shaped long generation: batch 8, 32768-token prompt, decode keys
+    # drifting by 0.02 sigma per 256 steps, the Update Buffer flushed every 128
+    "qwen3-8b-drift": dict(batch=8, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16,
+                           local=512, update_buf=128, topk=1024, cand_bp=500, context=32768, layers=8, drift=0.02),
+    # 1M-token context, Retrieval-zone K/V in pinned host memory read through UVA
+    "1m-uva": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16, local=512,
+                   update_buf=128, topk=2048, cand_bp=500, context=1048576, layers=2, retrieval_on_host=1),
+    # the same 1M-token context with the whole cache in HBM (it fits: ~4 GiB per layer of 280 GB)
+    "1m-hbm": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16, local=512,
+                   update_buf=128, topk=2048, cand_bp=500, context=1048576, layers=2, retrieval_on_host=0),
+    # one point of the 256K batch-5 sweep (candidate fraction, rho and k from the command line)
+    "sweep-256k": dict(batch=5, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16, local=512,
+                       update_buf=128, topk=1024, cand_bp=500, context=262144, layers=4),
 }
 DESCRIPTION = {
     "llama8b-128k": "Llama-3.1-8B-shaped decode layer, 131072-token context",
     "tiny-4k": "one KV head, 4096 float32 keys",
+    "qwen3-8b-drift": "Qwen3-8B-shaped long generation, batch 8, 32768-token prompt, drifting decode keys",
+    "1m-uva": "1M-token context, Retrieval-zone K/V in pinned host memory (UVA)",
+    "1m-hbm": "1M-token context, the whole cache in HBM",
+    "sweep-256k": "256K-token context, batch 5 (one point of the candidate-fraction x rho x k sweep)",
 }
 
 
@@ -178,7 +195,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     B.build()
     P.load()
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     nl = args.layers or w["layers"]
     ctxlen, d = w["context"], w["head_dim"]
     b, hkv, hq, S = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["sink"]
@@ -193,7 +210,7 @@ def run_ours(args, rank, world):
         seed = rank_seed(rank, li)
         cfg = P.make_config(batch=b, n_kv_heads=hkv, n_q_heads=hq, head_dim=d, n_sub=w["n_sub"], rho=w["rho"],
                             sink=S, local=w["local"], update_buf=w["update_buf"], topk=w["topk"],
-                            cand_bp=w["cand_bp"], max_ctx=max_ctx, retrieval_on_host=0)
+                            cand_bp=w["cand_bp"], max_ctx=max_ctx, retrieval_on_host=w.get("retrieval_on_host", 0))
         ctx = P.Context(cfg, synth.srht_signs(seed, d))
         scale = torch.from_numpy(synth.channel_scale(seed, hkv, d)).cuda()
         gen.manual_seed(seed)
@@ -203,7 +220,13 @@ def run_ours(args, rank, world):
         st = ctx.paris_get_state()
         N0 = st["N"]
         # per decode step of this layer: new token and the query (a Retrieval-zone key + N(0, 0.5^2))
-        kn = (torch.randn((per_layer_steps, b, hkv, d), generator=gen, device="cuda") * scale[None, None]).to(fdt)
+        kn = torch.randn((per_layer_steps, b, hkv, d), generator=gen, device="cuda") * scale[None, None]
+        if w.get("drift"):
+            # mu(t) = rate (t / 256) delta s, delta a fixed random +-1 vector per KV head
+            delta = torch.randint(0, 2, (hkv, d), generator=gen, device="cuda").float() * 2 - 1
+            t = torch.arange(per_layer_steps, device="cuda", dtype=torch.float32) * nl + li
+            kn = kn + w["drift"] * (t / 256.0)[:, None, None, None] * (delta * scale)[None, None]
+        kn = kn.to(fdt)
         vn = torch.randn((per_layer_steps, b, hkv, d), generator=gen, device="cuda").to(fdt)
         pos = torch.randint(S, S + N0, (per_layer_steps, b, hq), generator=gen, device="cuda")
         kvh_of = torch.arange(hq, device="cuda") // (hq // hkv)
@@ -457,6 +480,7 @@ def run_ours(args, rank, world):
         "config": {"workload": DESCRIPTION[args.workload], "batch": b, "n_q_heads": hq, "n_kv_heads": hkv,
                    "head_dim": d, "context": ctxlen, "sink": S, "local": w["local"], "update_buf": w["update_buf"],
                    "n_sub": w["n_sub"], "rho": w["rho"], "cand_pct": w["cand_bp"] / 100, "topk": w["topk"],
+                   "retrieval_on_host": w.get("retrieval_on_host", 0), "drift_sigma_per_256_steps": w.get("drift", 0.0),
                    "kv_dtype": "bf16" if fdt == torch.bfloat16 else "f32", "layers_rotated": nl,
                    "l2": f"inputs larger than L2: {nl} layer contexts rotated, each revisited after "
                          f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"},
@@ -490,12 +514,23 @@ def cpu_baseline(args):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", args.workload,
+           "--cand-bp", str(args.cand_bp), "--rho", str(args.rho), "--topk", str(args.topk),
            "--steps", str(args.cpu_steps), "--warmup", str(args.warmup if args.impl == "reference" else 0)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         log(r.stderr[-2000:])
         return None
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def workload_of(args) -> dict:
+    """The workload's parameters, with the sweep point's overrides applied."""
+    w = dict(WORKLOADS[args.workload])
+    for key in ("cand_bp", "rho", "topk"):
+        v = getattr(args, key, None)
+        if v:
+            w[key] = v
+    return w
 
 
 def oracle_sample(args):
@@ -506,7 +541,7 @@ def oracle_sample(args):
     from long_context_kv_gb300 import synth
     from oracle import pariskv as o
 
-    w = WORKLOADS[args.workload]
+    w = workload_of(args)
     d, S, L, U = w["head_dim"], w["sink"], w["local"], w["update_buf"]
     G = w["n_q_heads"] // w["n_kv_heads"]
     T = w["context"]
@@ -562,6 +597,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b-128k", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--cand-bp", dest="cand_bp", type=int, default=0, help="candidates in basis points (sweep point)")
+    ap.add_argument("--rho", type=int, default=0, help="hot centroids per subspace (sweep point)")
+    ap.add_argument("--topk", type=int, default=0, help="k (sweep point)")
     ap.add_argument("--cpu-steps", type=int, default=60)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)

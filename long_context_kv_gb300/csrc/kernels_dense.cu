@@ -19,6 +19,8 @@
 // copies to stream at the memory's rate.
 #include <float.h>
 
+#include <algorithm>
+
 #include "paris_device.cuh"
 
 namespace paris {
@@ -312,16 +314,27 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
 
 }  // namespace
 
-int dense_group(int g) { return g; }
-
 int dense_splits(const DenseArgs& a, int sm_count) {
-  // one block per SM over the whole grid, at least one tile per split
+  // Splits per (sequence, KV head): the fewest that fill whole waves of one
+  // block per SM (every block of a split has the same rows, so a partial
+  // last wave idles SMs), at least one tile per split.
   const int64_t units = (int64_t)a.s.batch * a.s.hkv;
-  const int64_t want = (sm_count + units - 1) / units;
-  const int64_t most = (a.T + kDTile - 1) / kDTile;
-  int64_t n = want < most ? want : most;
-  if (n < 1) n = 1;
-  return (int)(n < a.nsplit_max ? n : a.nsplit_max);
+  const int64_t most = std::max<int64_t>(1, std::min<int64_t>({(a.T + kDTile - 1) / kDTile, (int64_t)a.nsplit_max}));
+  int64_t best = 1;
+  double best_eff = -1.0;
+  for (int64_t n = 1; n <= most; ++n) {
+    const int64_t blocks = n * units;
+    const int64_t waves = (blocks + sm_count - 1) / sm_count;
+    // fraction of the SM slots of those waves that hold a block, counting
+    // one wave as full when the grid is smaller than the GPU
+    const double eff = blocks < sm_count ? (double)blocks / sm_count : (double)blocks / (waves * sm_count);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = n;
+    }
+    if (eff > 0.999) break;
+  }
+  return (int)best;
 }
 
 int64_t dense_rows_per_split(int64_t T, int nsplit) {

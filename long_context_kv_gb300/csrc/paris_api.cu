@@ -423,8 +423,7 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
       cudaGetLastError();
       c->sm_count = 1;
     }
-    const int64_t units = bh * (f.n_q_heads / f.n_kv_heads / dense_group(f.n_q_heads / f.n_kv_heads));
-    c->dense_splits_max = (int)std::max<int64_t>(1, (4LL * c->sm_count + units - 1) / units);
+    c->dense_splits_max = std::max(1, c->sm_count);  // splits per (sequence, KV head), at most one per SM
   }
   TRY(dalloc(c, &c->dense_part, (size_t)bq * c->dense_splits_max * kPartStride * sizeof(float), "dense partials"));
   TRY(dalloc(c, &c->dense_counter, (size_t)bq * sizeof(uint32_t), "dense counters"));

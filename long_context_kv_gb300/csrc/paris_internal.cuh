@@ -168,8 +168,7 @@ struct DenseArgs {
   uint32_t* counter;          // [batch*Hkv*groups] splits finished, reset by the last one
   __nv_bfloat16* out;
 };
-int dense_group(int g);                              // query heads per block (all G of a KV head)
-int dense_splits(const DenseArgs& a, int sm_count);  // splits per (sequence, head group)
+int dense_splits(const DenseArgs& a, int sm_count);  // splits per (sequence, KV head)
 int64_t dense_rows_per_split(int64_t T, int nsplit);
 cudaError_t launch_dense(const DenseArgs& a, int nsplit, cudaStream_t st);
 
