@@ -31,6 +31,10 @@ WORKLOADS = {
     # B = 16 (m = 8), rho = 4, candidates 5%, k = 1024.
     "llama8b-128k": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16, local=512,
                          update_buf=128, topk=1024, cand_bp=500, context=131072, layers=8),
+    # the same layer shape, 32 layer contexts: one captured graph steps a token
+    # through every layer (the whole model's decode-time retrieval and attention)
+    "llama8b-128k-32l": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16,
+                             local=512, update_buf=128, topk=1024, cand_bp=500, context=131072, layers=32),
     # the small case the oracle finishes in seconds
     "tiny-4k": dict(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=128, n_sub=16, rho=4, sink=0, local=0,
                     update_buf=128, topk=64, cand_bp=1000, context=4096, layers=64),
@@ -51,6 +55,7 @@ WORKLOADS = {
 DESCRIPTION = {
     "llama8b-128k": "Llama-3.1-8B-shaped decode layer, 131072-token context",
     "tiny-4k": "one KV head, 4096 float32 keys",
+    "llama8b-128k-32l": "Llama-3.1-8B-shaped decode, 32 layers of 131072-token context",
     "qwen3-8b-drift": "Qwen3-8B-shaped long generation, batch 8, 32768-token prompt, drifting decode keys",
     "1m-uva": "1M-token context, Retrieval-zone K/V in pinned host memory (UVA)",
     "1m-hbm": "1M-token context, the whole cache in HBM",
@@ -354,10 +359,20 @@ def run_ours(args, rank, world):
     def call_dense(L, _):
         L["ctx"].paris_dense_attend(L["qs"][L["step"]], L["out"])
 
+    def call_gqa(L, _):
+        L["ctx"].paris_sparse_attend_gqa(L["qs"][L["step"]], L["idx"], L["out"])
+
     keys_retrieve = sum(L["ctx"].paris_get_state()["N"] * b * hkv for L in layers) / nl
     ms_retrieve = timed_calls(call_retrieve)
     ms_attend = timed_calls(call_attend)
     ms_dense = timed_calls(call_dense)
+    ms_gqa = timed_calls(call_gqa)
+    # rows the GQA-shared attention reads per KV head (the union of its query heads' top-k), layer 0
+    G = hq // hkv
+    st0 = layers[0]["ctx"].paris_get_state()
+    k_eff0 = int(st0["k_eff"])
+    idx0 = layers[0]["idx"][:, :, :k_eff0].reshape(b, hkv, G * k_eff0)
+    union_rows = sum(int(torch.unique(idx0[s_, h_]).numel()) for s_ in range(b) for h_ in range(hkv)) / (b * hkv)
     tokens_dense = sum(L["ctx"].paris_get_state()["T"] for L in layers) / nl
     ms_append = timed_calls(call_append)
 
@@ -485,11 +500,18 @@ def run_ours(args, rank, world):
                    "l2": f"inputs larger than L2: {nl} layer contexts rotated, each revisited after "
                          f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"},
         "us_per_decode_step": 1e3 * ms / args.steps,
+        # one token through all rotated layers: the graph launches the layers' steps back to back
+        "us_per_token_all_layers": 1e3 * ms / args.steps * nl,
         "us_per_decode_step_eager": 1e3 * ms_eager / args.steps,
         "us_decode_kernel": us_decode,
         "us_per_decode_step_eager_p10_p50_p90": [round(pct(0.1), 2), round(pct(0.5), 2), round(pct(0.9), 2)],
         "us_retrieve": 1e3 * ms_retrieve, "keys_per_s_retrieve": job_throughput(keys_retrieve, world, ms_retrieve),
         "us_sparse_attend": 1e3 * ms_attend, "us_append": 1e3 * ms_append,
+        # GQA-shared variant: the union of a KV head's query heads' top-k, each row read once per KV head
+        "gqa_shared_attention": {
+            "us_per_step": 1e3 * ms_gqa, "us_per_head_sparse_attention": 1e3 * ms_attend,
+            "union_rows_per_kv_head": union_rows, "per_head_rows_per_kv_head": G * k_eff0,
+        },
         # the full-attention comparator on the same cache: every K/V row once per step
         "dense_attention": {
             "us_per_step": 1e3 * ms_dense,

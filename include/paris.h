@@ -167,6 +167,22 @@ paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtyp
 paris_status paris_sparse_attend_noalloc(paris_ctx* ctx, const void* q, paris_dtype dtype,
                                          const int32_t* topk_idx, void* out_bf16, void* stream);
 
+/* GQA-shared sparse attention: every query head of a KV head attends over
+ * Sink U Local U Update Buffer U the union of the retrieved tokens of all G
+ * query heads of that KV head, so each K/V row is read once per KV head
+ * instead of once per query head that retrieved it (the GQA-shared
+ * retrieval variant: K/V gather bytes fall by up to G when the heads'
+ * top-k sets overlap).  Each head's set is a superset of its own
+ * paris_sparse_attend set; with G = 1 the two calls attend over the same
+ * rows.  topk_idx: device int32 [batch][Hq][topk] as produced by
+ * paris_retrieve (ascending per head; entries < 0 are skipped, entries
+ * outside the Retrieval zone skipped and flagged).  q and out as in
+ * paris_sparse_attend.  Same arithmetic as paris_dense_attend.  Limits: at
+ * most 16 query heads per KV head and G x k_eff <= 32768, else PARIS_EINVAL.
+ * Two launches (the union, then the attention); scratch from paris_create. */
+paris_status paris_sparse_attend_gqa(paris_ctx* ctx, const void* q, paris_dtype dtype, const int32_t* topk_idx,
+                                     void* out_bf16, void* stream);
+
 /* Dense decode attention over every cached token -- Sink, Retrieval zone,
  * Local and Update Buffer -- for each query head: the full-attention
  * baseline ParisKV's decode throughput is compared against (ParisKV,
@@ -247,8 +263,10 @@ typedef enum {
                                    attention and the append of the step's token      */
   PARIS_KERNEL_ATTEND = 5,      /* standalone sparse attention and the merge of its splits */
   PARIS_KERNEL_FILL = 6,        /* empty-result fill                                     */
-  PARIS_KERNEL_DENSE = 7,       /* dense comparator: attention over every cached token   */
-  PARIS_KERNEL_COUNT = 8
+  PARIS_KERNEL_DENSE = 7,       /* attention streaming rows once per KV head: the dense
+                                   comparator, and the GQA-shared sparse attention      */
+  PARIS_KERNEL_UNION = 8,       /* union of a KV head's top-k lists (GQA-shared attention) */
+  PARIS_KERNEL_COUNT = 9
 } paris_kernel;
 
 /* Cumulative kernel launches of this context since paris_create, per

@@ -95,14 +95,25 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   const int G = a.s.g, qh0 = kvh * G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t0 = (int64_t)split * a.rows_per_split;
-  const int64_t t1 = min64(a.T, t0 + a.rows_per_split);
+  // rows of the (sequence, KV head): every token, or the window rows then the list
+  const int64_t total = a.list ? a.nwin + __ldcg(a.list_n + sh) : a.T;
+  const int64_t t1 = min64(total, t0 + a.rows_per_split);
   const int nrows = (int)max64(0, t1 - t0);
   const int ntiles = (nrows + kDTile - 1) / kDTile;
   const int ring = a.s.local + a.s.ubuf;
 
-  // where token t's K/V row is: the Sink slots and the Local/Buffer ring of
-  // the window arrays, or the Retrieval-zone store
+  // where row t's K/V is: the Sink slots and the Local/Buffer ring of the
+  // window arrays, or the Retrieval-zone store.  Dense: row t is token t.
+  // List: rows below nwin are the window (Sink, then Local and Buffer in
+  // position order), the rest the listed Retrieval-zone tokens.
   auto row_ptrs = [&](int64_t t, const __nv_bfloat16*& kp, const __nv_bfloat16*& vp) {
+    if (a.list) {
+      if (t < a.nwin) {
+        t = t < a.nsink ? t : a.s.sink + a.N + (t - a.nsink);
+      } else {
+        t = __ldcg(a.list + sh * a.list_stride + (t - a.nwin));
+      }
+    }
     if (t < a.s.sink || t >= a.s.sink + a.N) {
       const int64_t slot = t < a.s.sink ? t : a.s.sink + (t - a.s.sink) % ring;
       kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
@@ -312,7 +323,66 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   if (tid == 0) a.counter[blockIdx.y] = 0;
 }
 
+// The union of the G query heads' top-k lists of (sequence, KV head)
+// blockIdx.x.  Each list is ascending with distinct positions, so a
+// position of head h's list is a repeat exactly when a binary search finds
+// it in the list of an earlier head; the kept positions are compacted in
+// list order (head by head).  Positions outside the Retrieval zone are
+// dropped and flagged.
+constexpr int kUnionThreads = 1024;
+__global__ void __launch_bounds__(kUnionThreads) k_union(const int32_t* __restrict__ topk_idx, int64_t k, int k_eff,
+                                                         Shape s, int64_t N, int32_t* list, int32_t* n,
+                                                         int64_t stride, uint32_t* status) {
+  extern __shared__ int32_t ul[];  // [G][k_eff]
+  __shared__ uint32_t tmp[33];
+  const int sh = blockIdx.x, seq = sh / s.hkv, kvh = sh - seq * s.hkv;
+  const int G = s.g, tot = G * k_eff, tid = threadIdx.x;
+  for (int e = tid; e < tot; e += kUnionThreads) {
+    const int h = e / k_eff, i = e - h * k_eff;
+    ul[e] = __ldg(topk_idx + ((int64_t)seq * s.hq + kvh * G + h) * k + i);
+  }
+  __syncthreads();
+  // thread t owns entries [t per, t per + per) of the G k_eff entries
+  const int per = (tot + kUnionThreads - 1) / kUnionThreads;
+  const int e0 = min(tot, tid * per), e1 = min(tot, e0 + per);
+  uint32_t keep = 0;  // bit j: entry e0 + j is kept (per <= 32)
+  for (int e = e0; e < e1; ++e) {
+    const int32_t x = ul[e];
+    bool kp = x >= s.sink && x < s.sink + N;
+    if (!kp && x >= 0) atomicOr(status, kStatusBadIndex);
+    for (int h2 = 0; kp && h2 < e / k_eff; ++h2) {
+      int lo = 0, hi = k_eff;  // first entry >= x in list h2
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (ul[h2 * k_eff + mid] < x) lo = mid + 1; else hi = mid;
+      }
+      if (lo < k_eff && ul[h2 * k_eff + lo] == x) kp = false;
+    }
+    if (kp) keep |= 1u << (e - e0);
+  }
+  uint32_t total;
+  uint32_t at = block_excl_scan((uint32_t)__popc(keep), tmp, &total);
+  for (int e = e0; e < e1; ++e)
+    if ((keep >> (e - e0)) & 1u) list[(int64_t)sh * stride + at++] = ul[e];
+  if (tid == 0) n[sh] = (int32_t)total;
+}
+
 }  // namespace
+
+cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shape s, int64_t N, int32_t* list,
+                         int32_t* n, int64_t stride, uint32_t* status, cudaStream_t st) {
+  const int64_t tot = (int64_t)s.g * k_eff;
+  if (tot > 32 * kUnionThreads) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)std::max<int64_t>(1, tot) * sizeof(int32_t);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_union, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * kUnionThreads * 4);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(k_union, dim3(s.batch * s.hkv), dim3(kUnionThreads), smem, st, topk_idx, k, (int)k_eff, s, N,
+                    list, n, stride, status);
+}
 
 int dense_splits(const DenseArgs& a, int sm_count) {
   // Splits per (sequence, KV head): the fewest that fill whole waves of one

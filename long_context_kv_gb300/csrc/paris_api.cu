@@ -44,7 +44,9 @@ struct paris_ctx {
   uint32_t* status;
   uint32_t* counters;  // [2][batch*Hq]: rerank blocks, attention splits finished
   float* dense_part;   // dense comparator: [batch*Hq][dense_splits_max][kPartStride]
-  uint32_t* dense_counter;  // [batch*Hkv*groups]
+  uint32_t* dense_counter;  // [batch*Hkv]
+  int32_t* union_list;  // GQA-shared attention: [batch*Hkv][G*topk] union of the G top-k lists
+  int32_t* union_n;     // [batch*Hkv]
   int dense_splits_max, sm_count;
   uint64_t* trace;     // kTraceSlots phase timestamps
   bool tracing;        // PARIS_TRACE=1 in the environment at creation
@@ -154,7 +156,7 @@ void lloyd_max_levels(int m, double lev[8], double thr[7]) {
 void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
                  c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status,
-                 c->counters, c->trace, c->dense_part, c->dense_counter};
+                 c->counters, c->trace, c->dense_part, c->dense_counter, c->union_list, c->union_n};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_store) {
@@ -427,6 +429,8 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   }
   TRY(dalloc(c, &c->dense_part, (size_t)bq * c->dense_splits_max * kPartStride * sizeof(float), "dense partials"));
   TRY(dalloc(c, &c->dense_counter, (size_t)bq * sizeof(uint32_t), "dense counters"));
+  TRY(dalloc(c, &c->union_list, (size_t)bq * f.topk * sizeof(int32_t), "top-k unions"));
+  TRY(dalloc(c, &c->union_n, (size_t)bh * sizeof(int32_t), "top-k union sizes"));
   {
     const char* env = std::getenv("PARIS_TRACE");
     c->tracing = env != nullptr && env[0] == '1';
@@ -522,6 +526,46 @@ paris_status paris_sparse_attend(paris_ctx* c, const void* q, paris_dtype dtype,
   return PARIS_OK;
 }
 
+paris_status paris_sparse_attend_gqa(paris_ctx* c, const void* q, paris_dtype dtype, const int32_t* topk_idx,
+                                     void* out_bf16, void* stream) {
+  if (!c) return fail(nullptr, PARIS_EINVAL, "ctx is NULL");
+  paris_status st = check_dtype(c, dtype);
+  if (st != PARIS_OK) return st;
+  if (!q || !out_bf16 || (!topk_idx && c->N > 0)) return fail(c, PARIS_EINVAL, "q, topk_idx and out must not be NULL");
+  if (c->s.g > 16) return fail(c, PARIS_EINVAL, "paris_sparse_attend_gqa: at most 16 query heads per KV head");
+  const int64_t k = c->cfg.topk;
+  const int64_t k_eff = c->N > 0 ? std::min<int64_t>(k, candidate_count(c->N, c->cfg.cand_bp, k)) : 0;
+  if ((int64_t)c->s.g * k_eff > 32768)
+    return fail(c, PARIS_EINVAL, "paris_sparse_attend_gqa: query heads per KV head x k_eff must be at most 32768");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t stride = (int64_t)c->s.g * k;
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_UNION, s, [&] {
+    return launch_union(topk_idx, k, k_eff, c->s, c->N, c->union_list, c->union_n, stride, c->status, s);
+  }));
+  DenseArgs a;
+  a.s = c->s;
+  a.kv = c->kv;
+  a.N = c->N;
+  a.q = q;
+  a.qdtype = dtype;
+  a.qscale = 1.4426950408889634f / std::sqrt((float)kDim);
+  a.part = c->dense_part;
+  a.nsplit_max = c->dense_splits_max;
+  a.counter = c->dense_counter;
+  a.out = static_cast<__nv_bfloat16*>(out_bf16);
+  a.list = c->union_list;
+  a.list_n = c->union_n;
+  a.list_stride = stride;
+  a.nsink = std::min<int64_t>(c->cfg.sink, c->T);
+  a.nwin = a.nsink + c->n_local + c->n_buf;
+  a.T = a.nwin + (int64_t)c->s.g * k_eff;  // the most rows a (sequence, KV head) can have
+  int nsplit = dense_splits(a, c->sm_count);
+  a.rows_per_split = dense_rows_per_split(std::max<int64_t>(1, a.T), nsplit);
+  nsplit = (int)std::max<int64_t>(1, (a.T + a.rows_per_split - 1) / a.rows_per_split);
+  PARIS_CUDA(c, launch(c, PARIS_KERNEL_DENSE, s, [&] { return launch_dense(a, nsplit, s); }));
+  return PARIS_OK;
+}
+
 paris_status paris_dense_attend(paris_ctx* c, const void* q, paris_dtype dtype, void* out_bf16, void* stream) {
   if (!c) return fail(nullptr, PARIS_EINVAL, "ctx is NULL");
   paris_status st = check_dtype(c, dtype);
@@ -540,6 +584,9 @@ paris_status paris_dense_attend(paris_ctx* c, const void* q, paris_dtype dtype, 
   a.nsplit_max = c->dense_splits_max;
   a.counter = c->dense_counter;
   a.out = static_cast<__nv_bfloat16*>(out_bf16);
+  a.list = nullptr;
+  a.list_n = nullptr;
+  a.list_stride = a.nsink = a.nwin = 0;
   int nsplit = dense_splits(a, c->sm_count);
   a.rows_per_split = dense_rows_per_split(std::max<int64_t>(1, c->T), nsplit);
   nsplit = (int)std::max<int64_t>(1, (c->T + a.rows_per_split - 1) / a.rows_per_split);

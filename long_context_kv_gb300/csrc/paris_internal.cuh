@@ -165,9 +165,19 @@ struct DenseArgs {
   float qscale;               // log2(e) / sqrt(d)
   float* part;                // [batch*Hq][nsplit_max][kPartStride]
   int nsplit_max;
-  uint32_t* counter;          // [batch*Hkv*groups] splits finished, reset by the last one
+  uint32_t* counter;          // [batch*Hkv] splits finished, reset by the last one
   __nv_bfloat16* out;
+  // list mode (GQA-shared sparse attention): the rows are the window (nsink
+  // Sink rows, then Local and Buffer) and then list[sh][0 .. list_n[sh]),
+  // Retrieval-zone positions; list == nullptr: every token
+  const int32_t* list;
+  const int32_t* list_n;
+  int64_t list_stride, nsink, nwin;
 };
+// The union of the G query heads' top-k lists of every (sequence, KV head):
+// list[sh][0 .. n[sh]) in no particular order, each position once.
+cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shape s, int64_t N, int32_t* list,
+                         int32_t* n, int64_t stride, uint32_t* status, cudaStream_t st);
 int dense_splits(const DenseArgs& a, int sm_count);  // splits per (sequence, KV head)
 int64_t dense_rows_per_split(int64_t T, int nsplit);
 cudaError_t launch_dense(const DenseArgs& a, int nsplit, cudaStream_t st);

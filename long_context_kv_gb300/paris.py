@@ -39,6 +39,8 @@ _SIGNATURES = {
                                         ctypes.c_void_p, ctypes.c_size_t]),
     "paris_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
     "paris_rsq_levels": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "paris_sparse_attend_gqa": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p]),
     "paris_dense_attend": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_void_p]),
     "paris_sparse_attend_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
@@ -51,7 +53,7 @@ _SIGNATURES = {
     "paris_profile_end": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
 }
 
-KERNELS = ["place_kv", "encode", "build_index", "append", "decode", "attend", "fill", "dense"]
+KERNELS = ["place_kv", "encode", "build_index", "append", "decode", "attend", "fill", "dense", "union"]
 
 
 class paris_config(ctypes.Structure):
@@ -182,6 +184,11 @@ class Context:
     def paris_sparse_attend(self, q, topk_idx, out, stream=None):
         _check(load().paris_sparse_attend(self._h, _ptr(q), _dtype_code(q), _ptr(topk_idx), _ptr(out),
                                           _stream(stream)), self._h)
+
+    def paris_sparse_attend_gqa(self, q, topk_idx, out, stream=None):
+        """Sparse attention over the window and the union of the KV head's query heads' top-k."""
+        _check(load().paris_sparse_attend_gqa(self._h, _ptr(q), _dtype_code(q), _ptr(topk_idx), _ptr(out),
+                                              _stream(stream)), self._h)
 
     def paris_dense_attend(self, q, out, stream=None):
         """Dense attention over every cached token (the full-attention comparator)."""

@@ -1,0 +1,99 @@
+"""GQA-shared sparse attention (paris_sparse_attend_gqa) against the oracle:
+every query head of a KV head attends over Sink, Local, the Update Buffer
+and the union of the retrieved tokens of all the KV head's query heads
+(each row read once per KV head), within 2e-2 of float64.  With one query
+head per KV head it attends over the same rows as paris_sparse_attend."""
+import numpy as np
+import pytest
+import torch
+
+from long_context_kv_gb300 import paris as P
+from long_context_kv_gb300 import synth
+from oracle import pariskv as o
+from tests import gpu_cases as g
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from long_context_kv_gb300 import build
+    build.build()
+    P.load()
+
+
+def gqa(c: g.Case, qd: torch.Tensor, idx: torch.Tensor) -> np.ndarray:
+    b, hq, d = c.cfg["batch"], c.cfg["n_q_heads"], c.cfg["head_dim"]
+    out = torch.full((b, hq, d), 3.0, dtype=torch.bfloat16, device="cuda")
+    c.ctx.paris_sparse_attend_gqa(qd, idx, out)
+    c.ctx.paris_check_device()
+    return out.float().cpu().numpy()
+
+
+def check_gqa(c: g.Case, qd: torch.Tensor, idx: torch.Tensor, k_eff: int, heads=None):
+    out = gqa(c, qd, idx)
+    q_seen = qd.float().cpu().numpy()
+    idx_h = idx.cpu().numpy()
+    Kb, Vb = g.as_seen(c.K, torch.bfloat16), g.as_seen(c.V, torch.bfloat16)
+    z = c.zones
+    heads = heads or [(s, h) for s in range(c.cfg["batch"]) for h in range(c.cfg["n_q_heads"])]
+    sizes = {}
+    for seq, qh in heads:
+        kvh = qh // c.G
+        group = idx_h[seq, kvh * c.G:(kvh + 1) * c.G, :k_eff]
+        union = np.unique(group[group >= 0])
+        sizes[(seq, kvh)] = len(union)
+        rows = np.concatenate([z.sink(), z.local(), z.buffer(), union]).astype(np.int64)
+        assert len(np.unique(rows)) == len(rows)
+        ref = o.attention(q_seen[seq, qh], Kb[seq, kvh, rows], Vb[seq, kvh, rows])
+        err = float(np.max(np.abs(out[seq, qh] - ref)))
+        assert err <= g.ATTN_ATOL, (seq, qh, err)
+    return out, sizes
+
+
+@pytest.mark.parametrize("hkv,hq", [(2, 4), (2, 8), (1, 3)])
+def test_gqa_attends_over_the_union_of_the_group(hkv, hq):
+    c = g.make_case(6000, seed=61, batch=2, n_kv_heads=hkv, n_q_heads=hq, sink=16, local=256, update_buf=64,
+                    topk=256, cand_bp=500)
+    qd, idx, _, k_eff = g.run_retrieve(c, g.queries_from_zone(c))
+    _, sizes = check_gqa(c, qd, idx, k_eff)
+    assert all(k_eff <= n <= c.G * k_eff for n in sizes.values())
+
+
+def test_one_query_head_per_kv_head_equals_sparse_attention():
+    c = g.make_case(5000, seed=62, batch=1, n_kv_heads=2, n_q_heads=2, sink=16, local=128, update_buf=32,
+                    topk=200, cand_bp=1000)
+    qd, idx, _, k_eff = g.run_retrieve(c, g.queries_from_zone(c))
+    out, _ = check_gqa(c, qd, idx, k_eff)
+    sparse = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda")
+    c.ctx.paris_sparse_attend(qd, idx, sparse)
+    assert np.max(np.abs(out - sparse.float().cpu().numpy())) <= 2 * g.ATTN_ATOL
+
+
+def test_shared_rows_after_appends_and_from_host_memory():
+    c = g.make_case(3000, seed=63, batch=1, n_kv_heads=2, n_q_heads=8, sink=16, local=128, update_buf=32,
+                    topk=128, cand_bp=1000, retrieval_on_host=1)
+    for step in range(100):
+        g.append(c, synth.decode_keys(c.seed, 1, 2, step, 128, c.scale), synth.decode_values(c.seed, 1, 2, step, 128))
+    qd, idx, _, k_eff = g.run_retrieve(c, g.queries_from_zone(c, step=5))
+    check_gqa(c, qd, idx, k_eff)
+
+
+def test_overlapping_heads_share_their_rows():
+    # every query head of a group copies the same key (different noise): their top-k sets overlap
+    c = g.make_case(8000, seed=64, batch=1, n_kv_heads=2, n_q_heads=8, sink=16, local=128, update_buf=32,
+                    topk=256, cand_bp=500)
+    q = g.queries_from_zone(c)
+    for kvh in range(2):
+        q[0, 4 * kvh + 1:4 * kvh + 4] = q[0, 4 * kvh] + 0.05 * np.random.default_rng(kvh).standard_normal((3, 128))
+    qd, idx, _, k_eff = g.run_retrieve(c, q)
+    _, sizes = check_gqa(c, qd, idx, k_eff)
+    assert all(n < 2 * k_eff for n in sizes.values()), sizes
+
+
+def test_gqa_at_full_size_on_sampled_heads():
+    T0 = 131072
+    c = g.make_case(T0, seed=65, max_ctx=T0 + 64, batch=1, n_kv_heads=8, n_q_heads=32, sink=16, local=512,
+                    update_buf=128, topk=1024, cand_bp=500)
+    qd, idx, _, k_eff = g.run_retrieve(c, g.queries_from_zone(c))
+    check_gqa(c, qd, idx, k_eff, heads=[(0, 0), (0, 13), (0, 31)])
