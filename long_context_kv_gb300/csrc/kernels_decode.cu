@@ -12,7 +12,7 @@
 // (sequence, query head); block r owns a contiguous range of index chunks
 // of the Retrieval zone, so block order is position order.  What a block
 // hands to the others it stores straight into their shared memory before a
-// cluster barrier.  Four barriers separate the steps:
+// cluster barrier.  Five barriers separate the steps (four without attention):
 //   1. each block: q~, ||q|| and the hot centroids (redundantly), the votes
 //      of its chunks and their histogram, pushed to every block;
 //   2. barrier; every block sums the histograms, finds the vote threshold
@@ -23,12 +23,13 @@
 //      estimates (and their range) to every block;
 //   4. barrier; every block finds the k-th best key over all C (a counting
 //      pass in shared memory), counts the entries taken before its slice and
-//      writes the ones its slice takes at their place in the top-k; those
-//      rows and its share of the window rows are its attention rows, staged
-//      in rounds of 128 rows, two rounds in flight, every warp scoring 4 rows
-//      of a round with its own online softmax; the block's partial goes to
-//      block 0;
-//   5. barrier; block 0 merges the partials.
+//      writes the ones its slice takes at their place in the top-k, and
+//      pushes their count to every block;
+//   5. barrier; those rows, topped up with window rows to an even share of
+//      all rows, are the block's attention rows, staged in rounds of 128
+//      rows, two rounds in flight, every warp scoring 4 rows of a round with
+//      its own online softmax; the block's partial goes to block 0;
+//   6. barrier; block 0 merges the partials.
 // A decode token appended in the same step is read from the caller's k/v
 // where the attention needs it, and written to the cache by one warp while
 // the query is prepared (nothing in this launch reads the slots it writes).
@@ -94,6 +95,7 @@ struct DecodeArgs {
   // q = CS): the rerank slices of the candidate list and the blocks' shares
   // of the window rows
   int64_t ccut[kClusterMax + 1], wcut[kClusterMax + 1];
+  int64_t rcut[kClusterMax + 1];  // (nwin + k_eff) q / CS: the blocks' even shares of the attention rows
   uint32_t nmod;        // ring slot of the first Local token
   const void* q;
   int qdtype;
@@ -385,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ uint32_t tot[kMaxBins];
   __shared__ uint32_t hall[kClusterMax][kMaxBins];           // every block's histogram, pushed by its owner
   __shared__ uint32_t skey_mm[kClusterMax][2];               // smallest and largest order key of every block
+  __shared__ uint32_t staken[kClusterMax];                   // top-k entries every block's slice took
   __shared__ __align__(16) float pall[kClusterMax][kPartStride];  // attention partials, pushed to block 0
   __shared__ uint32_t tmp[33];
   __shared__ uint32_t red[2 * kWarps + 2];
@@ -1033,8 +1036,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 
   // ---- 5. sparse attention ---------------------------------------------------
   if (a.out != nullptr) {
-    // the block's rows: its share of the window rows, then the entries its slice took
-    const int64_t wl = cut_at(a.wcut, r), wh = cut_at(a.wcut, r + 1);
+    // The block's rows: the entries its slice took, topped up with window rows
+    // so that every block has about (nwin + k_eff) / cs rows (block q's
+    // window rows follow block q - 1's).  The slices' counts go to every block.
+    if (tid < cs) dsmem_st_u32(dsmem_addr(&staken[r], tid), nsel);
+    cluster_sync();
+    int wl = 0, wh = 0;
+    if (tid == 0) {
+      int wrun = 0;
+      for (int q = 0; q < cs; ++q) {
+        const int lo = wrun;
+        const int share = (int)(cut_at(a.rcut, q + 1) - cut_at(a.rcut, q));
+        wrun = q == cs - 1 ? (int)a.nwin : min((int)a.nwin, wrun + max(0, share - (int)staken[q]));
+        if (q == r) {
+          wl = lo;
+          wh = wrun;
+        }
+      }
+      red[0] = (uint32_t)wl;
+      red[1] = (uint32_t)wh;
+    }
+    __syncthreads();
+    wl = (int)red[0];
+    wh = (int)red[1];
     const int nwb = (int)(wh - wl);
     const int nrows = nwb + (int)min64(nsel, a.k_eff - out_off);
     const int ring = a.s.local + a.s.ubuf;
@@ -1279,6 +1303,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
     const int qq = q < cs ? q : cs;
     a.ccut[q] = ra.C * qq / cs;
     a.wcut[q] = L.nwin * qq / cs;
+    a.rcut[q] = (L.nwin + ra.k_eff) * qq / cs;
   }
   {
     const int ring = ra.s.local + ra.s.ubuf;
