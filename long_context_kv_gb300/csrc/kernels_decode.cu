@@ -385,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ float tq[kDim * 16];
   __shared__ uint32_t hist[kMaxBins];                // read by the cluster
   __shared__ uint32_t tot[kMaxBins];
+  __shared__ uint32_t wcnt[7][kWarps];                       // per-warp counts of votes 1..7
   __shared__ uint32_t hall[kClusterMax][kMaxBins];           // every block's histogram, pushed by its owner
   __shared__ uint32_t skey_mm[kClusterMax][2];               // smallest and largest order key of every block
   __shared__ uint32_t staken[kClusterMax];                   // top-k entries every block's slice took
@@ -708,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 #pragma unroll
     for (int v = 0; v < 7; ++v) {
       const uint32_t n = __reduce_add_sync(kFull, cnt[v]);
-      if (lane == 0 && n) atomicAdd(&hist[v + 1], n);
+      if (lane == 0) wcnt[v][warp] = n;
     }
     uint32_t nz_all;
     block_excl_scan(nz_mine, tmp, &nz_all);  // (its barriers also order the per-warp counts)
@@ -717,6 +718,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 #pragma unroll 8
       for (int w = 0; w < kWarps; ++w) n += whist[w * kWarpBins + tid];
       if (n) atomicAdd(&hist[8 + tid], n);
+    } else if (tid < kWarpBins + 7) {
+      // votes 1..7: one thread per value sums the warps (no other writer)
+      const int v = tid - kWarpBins;
+      uint32_t n = 0;
+#pragma unroll 8
+      for (int w = 0; w < kWarps; ++w) n += wcnt[v][w];
+      hist[v + 1] = n;
     }
     if (tid == 0) hist[0] = (uint32_t)own_len - nz_all;
   }
