@@ -167,6 +167,20 @@ paris_status paris_sparse_attend(paris_ctx* ctx, const void* q, paris_dtype dtyp
 paris_status paris_sparse_attend_noalloc(paris_ctx* ctx, const void* q, paris_dtype dtype,
                                          const int32_t* topk_idx, void* out_bf16, void* stream);
 
+/* Learned-centroid baseline (ParisKV, "Problem definition": learned
+ * codebooks such as k-means centroids fitted on the prefill keys, against
+ * which the analytic centroids are compared under drift): centroids
+ * replaces the 2^m sign-pattern centroids of every subspace by a table,
+ * device float32 [Hkv][B][2^m][m] (m = 8), for this context's bucket ids
+ * and query scores.  A key's id in subspace b is the centroid c with the
+ * largest float32 score ((0 + z_0 c_0) + z_1 c_1) + ... + z_7 c_7 over the
+ * rotated subvector z (lowest id on ties); a query's centroid scores are
+ * the same sums, its top-rho chosen as with the analytic centroids.
+ * Everything else (codes, w, votes, rerank) is unchanged.  The table is
+ * copied into the context.  centroids = NULL restores the analytic
+ * centroids.  Only while the cache is empty (else PARIS_ESTATE).           */
+paris_status paris_set_centroids(paris_ctx* ctx, const float* centroids, void* stream);
+
 /* GQA-shared sparse attention: every query head of a KV head attends over
  * Sink U Local U Update Buffer U the union of the retrieved tokens of all G
  * query heads of that KV head, so each K/V row is read once per KV head

@@ -26,7 +26,8 @@ __global__ void __launch_bounds__(256) k_encode(const void* __restrict__ K, int 
     float y[4];
     load4(K, dtype, (sh * T + pos) * kDim + 4 * lane, y);
     const int64_t row = sh * t.rcap + (pos - s.sink);
-    encode_key_warp(y, lane, sm, rp, t.ids + row * kSub, t.rec + row * kRecBytes);
+    encode_key_warp(y, lane, sm, rp, t.ids + row * kSub, t.rec + row * kRecBytes,
+                    t.cent ? t.cent + (sh % s.hkv) * kTabPerHead : nullptr);
   }
 }
 
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(256) k_append(const void* __restrict__ k, cons
   const int lane = threadIdx.x & 31;
   const int64_t sh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (sh >= (int64_t)s.batch * s.hkv) return;
-  append_token_warp(k, v, dtype, pos, sh, lane, s, kv, t, sm, rp);
+  append_token_warp(k, v, dtype, pos, sh, lane, s, kv, t, sm, rp, t.cent);
 }
 
 // Inverted bucket index of one chunk of one (sequence, KV head): for every

@@ -378,6 +378,9 @@ __device__ __forceinline__ uint32_t select_kth(KeyOf key_of, const int64_t C, co
   return prefix;
 }
 
+// kTable: the query's centroid scores come from a learned-centroid table
+// (a separate instantiation, so the analytic path's code is untouched).
+template <bool kTable>
 __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ __align__(16) float qs[kDim];
   __shared__ __align__(16) float zs[kDim];
@@ -488,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     // the step's own token into the cache (nothing in this launch reads the
     // ring slot or table row it writes: the attention takes it from k/v)
     if (a.new_pos >= 0 && r == 0 && qh % a.s.g == 0)
-      append_token_warp(a.k_new, a.v_new, a.kvdtype, a.new_pos, sh, lane, a.s, a.kv, a.t, a.sm, a.rp);
+      append_token_warp(a.k_new, a.v_new, a.kvdtype, a.new_pos, sh, lane, a.s, a.kv, a.t, a.sm, a.rp,
+                        kTable ? a.t.cent : nullptr);
   } else if (warp > kSub + 1) {
     // warm L2 with the window rows this block's attention will read
     if (a.out != nullptr) {
@@ -518,16 +522,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     float zz[kM];
 #pragma unroll
     for (int j = 0; j < kM; ++j) zz[j] = zs[b * kM + j];
-    float acc5 = 0.f;
+    float a8[8];
+    if constexpr (!kTable) {
+      float acc5 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 5; ++j) acc5 = __fadd_rn(acc5, ((lane >> j) & 1) ? -zz[j] : zz[j]);
-    float a6[2], a7[4], a8[8];
+      for (int j = 0; j < 5; ++j) acc5 = __fadd_rn(acc5, ((lane >> j) & 1) ? -zz[j] : zz[j]);
+      float a6[2], a7[4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) a6[t] = __fadd_rn(acc5, (t & 1) ? -zz[5] : zz[5]);
+      for (int t = 0; t < 2; ++t) a6[t] = __fadd_rn(acc5, (t & 1) ? -zz[5] : zz[5]);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) a7[t] = __fadd_rn(a6[t & 1], (t & 2) ? -zz[6] : zz[6]);
+      for (int t = 0; t < 4; ++t) a7[t] = __fadd_rn(a6[t & 1], (t & 2) ? -zz[6] : zz[6]);
 #pragma unroll
-    for (int t = 0; t < 8; ++t) a8[t] = __fadd_rn(a7[t & 3], (t & 4) ? -zz[7] : zz[7]);
+      for (int t = 0; t < 8; ++t) a8[t] = __fadd_rn(a7[t & 3], (t & 4) ? -zz[7] : zz[7]);
+    } else {
+      // learned centroids: score of centroid c = ((0 + z_0 c_0) + z_1 c_1) + ... + z_7 c_7
+      const float* tab = a.t.cent + (int64_t)kvh * kTabPerHead + (int64_t)b * kCentroids * kM;
+#pragma unroll 1
+      for (int i = 0; i < 8; ++i) {
+        const float4 c0 = __ldg(reinterpret_cast<const float4*>(tab + (lane + 32 * i) * kM));
+        const float4 c1 = __ldg(reinterpret_cast<const float4*>(tab + (lane + 32 * i) * kM + 4));
+        float sc = __fmul_rn(zz[0], c0.x);
+        sc = __fadd_rn(sc, __fmul_rn(zz[1], c0.y));
+        sc = __fadd_rn(sc, __fmul_rn(zz[2], c0.z));
+        sc = __fadd_rn(sc, __fmul_rn(zz[3], c0.w));
+        sc = __fadd_rn(sc, __fmul_rn(zz[4], c1.x));
+        sc = __fadd_rn(sc, __fmul_rn(zz[5], c1.y));
+        sc = __fadd_rn(sc, __fmul_rn(zz[6], c1.z));
+        sc = __fadd_rn(sc, __fmul_rn(zz[7], c1.w));
+        a8[i] = sc;
+      }
+    }
     uint32_t key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) key[i] = order_key(a8[i]);  // never 0 for a finite score
@@ -1337,7 +1361,8 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.out = L.out;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kUBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUBytes);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1355,7 +1380,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_decode, a);
+  return a.t.cent ? cudaLaunchKernelEx(&cfg, k_decode<true>, a) : cudaLaunchKernelEx(&cfg, k_decode<false>, a);
 }
 
 }  // namespace paris

@@ -47,6 +47,7 @@ struct paris_ctx {
   uint32_t* dense_counter;  // [batch*Hkv]
   int32_t* union_list;  // GQA-shared attention: [batch*Hkv][G*topk] union of the G top-k lists
   int32_t* union_n;     // [batch*Hkv]
+  float* cent_table;    // learned centroids [Hkv][16][256][8] (used when t.cent points to it)
   int dense_splits_max, sm_count;
   uint64_t* trace;     // kTraceSlots phase timestamps
   bool tracing;        // PARIS_TRACE=1 in the environment at creation
@@ -156,7 +157,8 @@ void lloyd_max_levels(int m, double lev[8], double thr[7]) {
 void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
                  c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status,
-                 c->counters, c->trace, c->dense_part, c->dense_counter, c->union_list, c->union_n};
+                 c->counters, c->trace, c->dense_part, c->dense_counter, c->union_list, c->union_n,
+                 c->cent_table};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_store) {
@@ -431,6 +433,7 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   TRY(dalloc(c, &c->dense_counter, (size_t)bq * sizeof(uint32_t), "dense counters"));
   TRY(dalloc(c, &c->union_list, (size_t)bq * f.topk * sizeof(int32_t), "top-k unions"));
   TRY(dalloc(c, &c->union_n, (size_t)bh * sizeof(int32_t), "top-k union sizes"));
+  TRY(dalloc(c, &c->cent_table, (size_t)f.n_kv_heads * kTabPerHead * sizeof(float), "centroid table"));
   {
     const char* env = std::getenv("PARIS_TRACE");
     c->tracing = env != nullptr && env[0] == '1';
@@ -563,6 +566,20 @@ paris_status paris_sparse_attend_gqa(paris_ctx* c, const void* q, paris_dtype dt
   a.rows_per_split = dense_rows_per_split(std::max<int64_t>(1, a.T), nsplit);
   nsplit = (int)std::max<int64_t>(1, (a.T + a.rows_per_split - 1) / a.rows_per_split);
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_DENSE, s, [&] { return launch_dense(a, nsplit, s); }));
+  return PARIS_OK;
+}
+
+paris_status paris_set_centroids(paris_ctx* c, const float* centroids, void* stream) {
+  if (!c) return fail(nullptr, PARIS_EINVAL, "ctx is NULL");
+  if (c->T > 0) return fail(c, PARIS_ESTATE, "paris_set_centroids: the cache must be empty (call it before prefill)");
+  if (!centroids) {
+    c->t.cent = nullptr;
+    return PARIS_OK;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PARIS_CUDA(c, cudaMemcpyAsync(c->cent_table, centroids, (size_t)c->s.hkv * kTabPerHead * sizeof(float),
+                                cudaMemcpyDeviceToDevice, s));
+  c->t.cent = c->cent_table;
   return PARIS_OK;
 }
 

@@ -138,9 +138,49 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* tmp, u
 // Subspace b is lanes 2b (j = 0..3) and 2b+1 (j = 4..7); a sequential sum
 // over j starts in the even lane and continues in the odd lane.
 // Writes the 16 ids and the 128-byte record (16 code words, 16 w) of the key.
+// Bucket id of subspace b = lane / 2 against a table of 256 learned
+// centroids (tab: [16][256][8] of the key's KV head): the centroid c with
+// the largest fp32 score ((0 + z_0 c_0) + z_1 c_1) + ... + z_7 c_7, the
+// lowest id among equal scores.  Lanes 2b (ids 0..127) and 2b + 1 (ids
+// 128..255) each scan half the table; all lanes return the id.
+__device__ __forceinline__ uint32_t table_id_warp(const float (&y)[4], int lane, const float* __restrict__ tab) {
+  const bool odd = (lane & 1) != 0;
+  float z[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float o = __shfl_xor_sync(kFull, y[i], 1);
+    z[i] = odd ? o : y[i];
+    z[4 + i] = odd ? y[i] : o;
+  }
+  const float* row = tab + ((lane >> 1) * kCentroids + (odd ? kCentroids / 2 : 0)) * kM;
+  float best = -INFINITY;
+  uint32_t bid = odd ? kCentroids / 2 : 0;
+  for (int c = 0; c < kCentroids / 2; ++c) {
+    const float4 c0 = __ldg(reinterpret_cast<const float4*>(row + c * kM));
+    const float4 c1 = __ldg(reinterpret_cast<const float4*>(row + c * kM + 4));
+    float sc = __fmul_rn(z[0], c0.x);
+    sc = __fadd_rn(sc, __fmul_rn(z[1], c0.y));
+    sc = __fadd_rn(sc, __fmul_rn(z[2], c0.z));
+    sc = __fadd_rn(sc, __fmul_rn(z[3], c0.w));
+    sc = __fadd_rn(sc, __fmul_rn(z[4], c1.x));
+    sc = __fadd_rn(sc, __fmul_rn(z[5], c1.y));
+    sc = __fadd_rn(sc, __fmul_rn(z[6], c1.z));
+    sc = __fadd_rn(sc, __fmul_rn(z[7], c1.w));
+    if (sc > best) {  // strict: among equal scores the lower id stays
+      best = sc;
+      bid = (odd ? kCentroids / 2 : 0) + c;
+    }
+  }
+  const float ob = __shfl_xor_sync(kFull, best, 1);
+  const uint32_t oid = __shfl_xor_sync(kFull, bid, 1);
+  // the even lane holds the lower ids: it wins ties
+  if (odd ? ob >= best : ob > best) return oid;
+  return bid;
+}
+
 __device__ __forceinline__ void encode_key_warp(float (&y)[4], int lane, const SignMask& sm,
                                                 const RsqParams& rp, uint8_t* ids_row,
-                                                uint8_t* rec_row) {
+                                                uint8_t* rec_row, const float* tab = nullptr) {
   apply_signs(y, sm, lane);
   fwht128_warp(y, lane);
   const bool odd = (lane & 1) != 0;
@@ -149,7 +189,7 @@ __device__ __forceinline__ void encode_key_warp(float (&y)[4], int lane, const S
 #pragma unroll
   for (int i = 0; i < 4; ++i) bits |= (y[i] < 0.f ? 1u : 0u) << i;
   const uint32_t obits = __shfl_xor_sync(kFull, bits, 1);
-  const uint32_t id = odd ? (obits | (bits << 4)) : (bits | (obits << 4));
+  const uint32_t id = tab ? table_id_warp(y, lane, tab) : odd ? (obits | (bits << 4)) : (bits | (obits << 4));
 
   float acc = 0.f;
 #pragma unroll
@@ -244,7 +284,8 @@ __device__ __forceinline__ void place_row(uint4 kk, uint4 vv, int64_t sh, int64_
 // encode its key at table row pos - S.
 __device__ __forceinline__ void append_token_warp(const void* k, const void* v, int dtype, int64_t pos,
                                                   int64_t sh, int lane, const Shape& s, const KvStore& kv,
-                                                  const Tables& t, const SignMask& sm, const RsqParams& rp) {
+                                                  const Tables& t, const SignMask& sm, const RsqParams& rp,
+                                                  const float* cent) {
   if (lane < 16) {
     const uint4 kk = load8_as_bf16(k, dtype, sh * kDim + 8 * lane);
     const uint4 vv = load8_as_bf16(v, dtype, sh * kDim + 8 * lane);
@@ -256,7 +297,8 @@ __device__ __forceinline__ void append_token_warp(const void* k, const void* v, 
   float y[4];
   load4(k, dtype, sh * kDim + 4 * lane, y);
   const int64_t row = sh * t.rcap + (pos - s.sink);
-  encode_key_warp(y, lane, sm, rp, t.ids + row * kSub, t.rec + row * kRecBytes);
+  encode_key_warp(y, lane, sm, rp, t.ids + row * kSub, t.rec + row * kRecBytes,
+                  cent ? cent + (sh % s.hkv) * kTabPerHead : nullptr);
 }
 
 // Order-preserving map of a float to an unsigned key (larger float, larger

@@ -45,7 +45,9 @@ struct Tables {
   uint32_t* off;     // [batch][Hkv][nchunk][16][kOffStride]
   int64_t rcap;      // Retrieval-zone capacity (rows)
   int nchunk;        // chunks per (sequence, KV head)
+  const float* cent; // learned centroids [Hkv][16][256][8] (nullptr: the analytic sign patterns)
 };
+constexpr int kTabPerHead = kSub * kCentroids * kM;  // floats of one KV head's centroid table
 
 struct KvStore {
   __nv_bfloat16* win_k;  // [batch][Hkv][win][d]: sink slots then the Local/Buffer ring

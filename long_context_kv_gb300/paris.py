@@ -41,6 +41,7 @@ _SIGNATURES = {
     "paris_rsq_levels": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "paris_sparse_attend_gqa": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p]),
+    "paris_set_centroids": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "paris_dense_attend": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_void_p]),
     "paris_sparse_attend_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
@@ -189,6 +190,11 @@ class Context:
         """Sparse attention over the window and the union of the KV head's query heads' top-k."""
         _check(load().paris_sparse_attend_gqa(self._h, _ptr(q), _dtype_code(q), _ptr(topk_idx), _ptr(out),
                                               _stream(stream)), self._h)
+
+    def paris_set_centroids(self, centroids=None, stream=None):
+        """Learned centroids, device float32 [Hkv][16][256][8] (None: the analytic sign patterns)."""
+        _check(load().paris_set_centroids(self._h, _ptr(centroids) if centroids is not None else None,
+                                          _stream(stream)), self._h)
 
     def paris_dense_attend(self, q, out, stream=None):
         """Dense attention over every cached token (the full-attention comparator)."""

@@ -188,6 +188,56 @@ def sign_pattern_ids(z: np.ndarray, n_sub: int) -> np.ndarray:
     return ids.astype(np.uint8 if m <= 8 else np.uint16)
 
 
+def table_scores(z: np.ndarray, n_sub: int, table: np.ndarray) -> np.ndarray:
+    """float32 [..., n_sub, C]: score of centroid c of subspace b against the
+    subvector z_b, ((0 + z_0 c_0) + z_1 c_1) + ... + z_{m-1} c_{m-1}, each
+    product and sum rounded to float32 (the learned-centroid baseline;
+    table: float32 [n_sub, C, m])."""
+    z = np.asarray(z, dtype=F32)
+    table = np.asarray(table, dtype=F32)
+    m = table.shape[-1]
+    zb = z.reshape(z.shape[:-1] + (n_sub, 1, m))
+    acc = (zb[..., 0] * table[..., 0]).astype(F32)
+    for j in range(1, m):
+        acc = (acc + (zb[..., j] * table[..., j]).astype(F32)).astype(F32)
+    return acc
+
+
+def table_ids(z: np.ndarray, n_sub: int, table: np.ndarray) -> np.ndarray:
+    """Bucket id per subspace against a table of learned centroids: the
+    centroid with the largest table_scores, the lowest id on ties (the
+    nearest centroid by inner product, as ParisKV assigns keys)."""
+    sc = table_scores(z, n_sub, table)
+    return np.argmax(sc, axis=-1).astype(np.uint8 if table.shape[-2] <= 256 else np.uint16)
+
+
+def kmeans_table(zb_keys: np.ndarray, n_centroids: int, iters: int, seed: int) -> np.ndarray:
+    """Learned centroids for the baseline: spherical k-means in float64 on the
+    unit subvectors of the prefill keys, per subspace.  zb_keys: [N, n_sub, m]
+    rotated key subvectors; start: n_centroids distinct keys drawn with the
+    seeded generator; each iteration assigns every key to the centroid of
+    largest inner product (lowest index on ties) and replaces each centroid
+    by the normalised mean of its keys (an empty centroid keeps its place).
+    Returns float32 [n_sub, n_centroids, m] of unit vectors."""
+    zb = np.asarray(zb_keys, dtype=np.float64)
+    N, n_sub, m = zb.shape
+    nrm = np.linalg.norm(zb, axis=-1, keepdims=True)
+    u = np.divide(zb, nrm, out=np.zeros_like(zb), where=nrm > 0)
+    rng = np.random.default_rng(seed)
+    out = np.empty((n_sub, n_centroids, m))
+    for b in range(n_sub):
+        c = u[rng.choice(N, size=n_centroids, replace=False), b].copy()
+        for _ in range(iters):
+            a = np.argmax(u[:, b] @ c.T, axis=1)
+            sums = np.zeros_like(c)
+            np.add.at(sums, a, u[:, b])
+            nm = np.linalg.norm(sums, axis=1)
+            keep = nm > 0
+            c[keep] = sums[keep] / nm[keep, None]
+        out[b] = c
+    return out.astype(F32)
+
+
 def centroid(cid: int, m: int) -> np.ndarray:
     """Analytic centroid number cid: coordinate j is -1/sqrt(m) if bit j is set."""
     bits = (cid >> np.arange(m)) & 1
@@ -236,7 +286,7 @@ def encode_ideal(K: np.ndarray, signs: np.ndarray, n_sub: int, levels=None, thre
 
 
 def encode_contract(K32: np.ndarray, signs: np.ndarray, n_sub: int,
-                    lev32: np.ndarray, thr32: np.ndarray):
+                    lev32: np.ndarray, thr32: np.ndarray, table: np.ndarray = None):
     """float32 encoding of keys K32 [N, d] in the contract order.
 
     z = fwht(D * k) (exact sign flips, then the FWHT in its stage order);
@@ -245,13 +295,15 @@ def encode_contract(K32: np.ndarray, signs: np.ndarray, n_sub: int,
     v_j = (-1)^s_j * lev[t_j]; vx = sequential sum over j of v_j * x_j;
     w = n_b / (float32(sqrt(d)) * vx), and w = 0, codes 0 where n_b = 0.
     Returns dict ids uint8 [N, n_sub], nib uint8 [N, d], w float32 [N, n_sub].
+    table (learned-centroid baseline): ids from table_ids instead of the sign
+    patterns; everything else the same.
     """
     K32 = np.asarray(K32, dtype=F32)
     N, d = K32.shape
     m = d // n_sub
     z = fwht(K32 * np.asarray(signs, dtype=F32)[None, :])
     zb = z.reshape(N, n_sub, m)
-    ids = sign_pattern_ids(z, n_sub)
+    ids = sign_pattern_ids(z, n_sub) if table is None else table_ids(z, n_sub, table)
     acc = np.zeros((N, n_sub), dtype=F32)
     for j in range(m):
         acc = acc + zb[..., j] * zb[..., j]
@@ -301,7 +353,7 @@ def dequantise(nib: np.ndarray, levels: np.ndarray) -> np.ndarray:
 
 
 def query_prep_contract(q32: np.ndarray, signs: np.ndarray, n_sub: int, rho: int,
-                        weighting: str = "rank"):
+                        weighting: str = "rank", table: np.ndarray = None):
     """float32 query preparation for one query q32 [d].
 
     ||q|| = sqrt(sequential sum over j = 0..d-1 of q_j * q_j);
@@ -310,7 +362,8 @@ def query_prep_contract(q32: np.ndarray, signs: np.ndarray, n_sub: int, rho: int
     (-z_{b,j} if bit j of c else +z_{b,j}); the top rho ids per subspace by
     (score desc, id asc) get weight rho - r (rank r) or 1 (flat).
     Returns dict qnorm, qt [d], hot_ids [n_sub, rho], hot_w [n_sub, rho],
-    lut int [n_sub, 2^m] (the vote each bucket gives).
+    lut int [n_sub, 2^m] (the vote each bucket gives).  table: the learned
+    centroids' table_scores replace the sign-pattern scores.
     """
     q32 = np.asarray(q32, dtype=F32)
     d = q32.shape[0]
@@ -325,7 +378,7 @@ def query_prep_contract(q32: np.ndarray, signs: np.ndarray, n_sub: int, rho: int
         acc = F32(acc + z[j] * z[j])
     zn = F32(np.sqrt(acc))
     qt = (z / zn).astype(F32) if zn > 0 else np.zeros(d, dtype=F32)
-    scores = centroid_scores_contract(z, n_sub)
+    scores = centroid_scores_contract(z, n_sub) if table is None else table_scores(z, n_sub, table)
     hot_ids = top_rho(scores, rho)
     if weighting == "rank":
         hot_w = np.broadcast_to(rho - np.arange(rho), hot_ids.shape).astype(np.int64)
@@ -459,14 +512,15 @@ def recall(found: np.ndarray, truth: np.ndarray) -> float:
 
 
 def retrieve_contract(enc: dict, q32: np.ndarray, signs: np.ndarray, n_sub: int, rho: int,
-                      cand_bp: int, k: int, lev32: np.ndarray, weighting: str = "rank"):
+                      cand_bp: int, k: int, lev32: np.ndarray, weighting: str = "rank",
+                      table: np.ndarray = None):
     """The whole retrieval for one query over one encoded Retrieval zone.
 
     enc: dict(ids [N, n_sub], nib [N, d], w [N, n_sub]) from encode_contract.
     Returns dict(votes, cand, est (per candidate), top_idx, top_est, C, k_eff),
     indices relative to the zone start.
     """
-    qp = query_prep_contract(q32, signs, n_sub, rho, weighting)
+    qp = query_prep_contract(q32, signs, n_sub, rho, weighting, table)
     n = enc["ids"].shape[0]
     sc = votes(enc["ids"], qp["lut"])
     c = candidate_count(n, cand_bp, k)

@@ -41,13 +41,14 @@ class Case:
     ctx: P.Context = None
     zones: list = field(default_factory=list)
     appended: int = 0
+    table: np.ndarray = None  # learned centroids [Hkv][16][256][8] (None: analytic)
 
     @property
     def G(self):
         return self.cfg["n_q_heads"] // self.cfg["n_kv_heads"]
 
 
-def make_case(T: int, seed: int = 1, dtype=torch.bfloat16, K=None, **cfg_kw) -> Case:
+def make_case(T: int, seed: int = 1, dtype=torch.bfloat16, K=None, table=None, **cfg_kw) -> Case:
     cfg = dict(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=128, n_sub=16, rho=4, sink=0, local=0,
                update_buf=128, topk=64, cand_bp=1000, max_ctx=T + 1024, retrieval_on_host=0,
                vote_weighting=P.PARIS_VOTE_RANK)
@@ -60,6 +61,9 @@ def make_case(T: int, seed: int = 1, dtype=torch.bfloat16, K=None, **cfg_kw) -> 
     c = Case(cfg=cfg, seed=seed, dtype=dtype, T=T)
     c.signs = synth.srht_signs(seed, d)
     c.ctx = P.Context(P.make_config(**cfg), c.signs)
+    if table is not None:
+        c.table = np.ascontiguousarray(table, dtype=np.float32)
+        c.ctx.paris_set_centroids(torch.from_numpy(c.table).cuda())
     Kd, Vd = to_dev(K, dtype), to_dev(V, dtype)
     c.ctx.paris_encode_prefill(Kd, Vd, T)
     torch.cuda.synchronize()
@@ -84,7 +88,8 @@ def append(c: Case, k: np.ndarray, v: np.ndarray, device: bool = True):
 
 def oracle_encoding(c: Case, seq: int, kvh: int) -> dict:
     S, N = c.cfg["sink"], c.zones.N
-    return o.encode_contract(c.K[seq, kvh, S:S + N], c.signs, 16, LEV32, THR32)
+    return o.encode_contract(c.K[seq, kvh, S:S + N], c.signs, 16, LEV32, THR32,
+                             None if c.table is None else c.table[kvh])
 
 
 def check_state(c: Case):
@@ -149,7 +154,7 @@ def check_retrieve(c: Case, q: np.ndarray, heads=None, stages=True):
             e = oracle_encoding(c, seq, kvh)
             encs[(seq, kvh)] = e
         r = o.retrieve_contract(encs[(seq, kvh)], q_seen[seq, qh], c.signs, 16, c.cfg["rho"], c.cfg["cand_bp"],
-                                k, LEV32, weighting)
+                                k, LEV32, weighting, None if c.table is None else c.table[kvh])
         assert k_eff == r["k_eff"]
         if stages:
             qt = c.ctx.paris_debug_dump(P.DUMP_QT, seq, qh)
