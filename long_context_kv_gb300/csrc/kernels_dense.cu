@@ -34,6 +34,7 @@ constexpr int kDStages = 3;
 constexpr int kDStride = kDim + 8;         // bf16 per staged row: 272 B, conflict-free 8-row matrix loads
 constexpr int kDMaxHeads = 16;             // query heads per block: the rows of one mma tile
 static_assert(kDTile * 16 == kDThreads * 8, "16-byte pieces: 8 per thread and tile for K, 8 for V");
+constexpr int kDMaxSplits = 1024;  // splits per (sequence, KV head) the last block's merge tables hold
 
 constexpr size_t kDenseSmem = (size_t)2 * kDStages * kDTile * kDStride * sizeof(uint16_t);
 
@@ -302,23 +303,52 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // every split's (max, sum) of every head at once, then per head the
+  // weights exp2(m_s - max) (0 for a split without rows), then each output
+  // element's weighted sum over the splits with its loads eight at a time
   const int nsplit = gridDim.x;
+  float* ml = reinterpret_cast<float*>(dsm);  // [G][nsplit][2], then f [G][nsplit], then Lt [G]
+  float* fw = ml + 2 * G * nsplit;
+  float* lt = fw + G * nsplit;
+  for (int e = tid; e < G * nsplit; e += kDThreads) {
+    const int h = e / nsplit, s0 = e - h * nsplit;
+    const float* ph = a.part + (((int64_t)seq * a.s.hq + qh0 + h) * a.nsplit_max + s0) * kPartStride;
+    ml[2 * e] = __ldcg(ph);
+    ml[2 * e + 1] = __ldcg(ph + 1);
+  }
+  __syncthreads();
+  for (int h = warp; h < G; h += kDWarps) {
+    float Mx = -FLT_MAX;
+    for (int s0 = lane; s0 < nsplit; s0 += 32)
+      if (ml[2 * (h * nsplit + s0) + 1] > 0.f) Mx = fmaxf(Mx, ml[2 * (h * nsplit + s0)]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(kFull, Mx, off));
+    float L = 0.f;
+    for (int s0 = lane; s0 < nsplit; s0 += 32) {
+      const float mm = ml[2 * (h * nsplit + s0)], ll = ml[2 * (h * nsplit + s0) + 1];
+      const float f = ll > 0.f ? exp2f(mm - Mx) : 0.f;
+      fw[h * nsplit + s0] = f;
+      L += ll * f;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+    if (lane == 0) lt[h] = L;
+  }
+  __syncthreads();
   for (int e = tid; e < G * kDim; e += kDThreads) {
     const int h = e / kDim, d = e % kDim;
-    const float* ph = a.part + (((int64_t)seq * a.s.hq + qh0 + h) * a.nsplit_max) * kPartStride;
-    float Mx = -FLT_MAX;
-    for (int s0 = 0; s0 < nsplit; ++s0)
-      if (__ldcg(ph + (int64_t)s0 * kPartStride + 1) > 0.f) Mx = fmaxf(Mx, __ldcg(ph + (int64_t)s0 * kPartStride));
-    float Lt = 0.f, ot = 0.f;
-    for (int s0 = 0; s0 < nsplit; ++s0) {
-      const float mm = __ldcg(ph + (int64_t)s0 * kPartStride), ll = __ldcg(ph + (int64_t)s0 * kPartStride + 1);
-      if (ll > 0.f) {
-        const float f = exp2f(mm - Mx);
-        Lt += ll * f;
-        ot += __ldcg(ph + (int64_t)s0 * kPartStride + 4 + d) * f;
-      }
+    const float* ph = a.part + (((int64_t)seq * a.s.hq + qh0 + h) * a.nsplit_max) * kPartStride + 4 + d;
+    float ot = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += 8) {
+      float oo[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) oo[u] = s0 + u < nsplit ? __ldcg(ph + (int64_t)(s0 + u) * kPartStride) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (s0 + u < nsplit) ot += oo[u] * fw[h * nsplit + s0 + u];
     }
-    a.out[((int64_t)seq * a.s.hq + qh0 + h) * kDim + d] = __float2bfloat16_rn(Lt > 0.f ? ot / Lt : 0.f);
+    const float L = lt[h];
+    a.out[((int64_t)seq * a.s.hq + qh0 + h) * kDim + d] = __float2bfloat16_rn(L > 0.f ? ot / L : 0.f);
   }
   if (tid == 0) a.counter[blockIdx.y] = 0;
 }
@@ -413,7 +443,9 @@ int64_t dense_rows_per_split(int64_t T, int nsplit) {
 }
 
 cudaError_t launch_dense(const DenseArgs& a, int nsplit, cudaStream_t st) {
-  if (a.s.g > kDMaxHeads) return cudaErrorInvalidValue;
+  static_assert((size_t)(3 * kDMaxHeads * kDMaxSplits + kDMaxHeads) * sizeof(float) <= kDenseSmem,
+                "the merge tables fit the stage area");
+  if (a.s.g > kDMaxHeads || nsplit > kDMaxSplits) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_dense, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDenseSmem);
