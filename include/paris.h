@@ -59,10 +59,18 @@ typedef enum {
   PARIS_VOTE_FLAT = 1  /* every selected centroid gives 1 vote                     */
 } paris_vote_weighting;
 
+typedef enum {
+  PARIS_TOPK_BY_SCORE = 0,   /* best estimate first, equal estimates by ascending
+                                position (one block per list sorts it at the
+                                end of the retrieval kernel)                  */
+  PARIS_TOPK_BY_POSITION = 1 /* the same set in ascending position (no sort)   */
+} paris_topk_order;
+
 /* Shape and policy of one layer's cache.  Supported: head_dim = 128,
  * n_sub = 16 (m = 8), 1 <= rho <= 15 with rank weights or <= 256 with flat
  * weights, n_q_heads a multiple of n_kv_heads, update_buf >= 1,
- * 0 < cand_bp <= 10000, topk >= 1, max_ctx <= 2^31 - 1.                      */
+ * 0 < cand_bp <= 10000, topk >= 1 (at most 16384 with PARIS_TOPK_BY_SCORE),
+ * max_ctx <= 2^31 - 1.                                                       */
 typedef struct {
   int batch;             /* sequences decoded in lock step                     */
   int n_kv_heads;        /* Hkv                                                */
@@ -78,6 +86,7 @@ typedef struct {
   int max_ctx;           /* capacity in tokens per sequence                    */
   int retrieval_on_host; /* 1: Retrieval-zone K/V in mapped pinned host memory */
   int vote_weighting;    /* paris_vote_weighting                               */
+  int topk_order;        /* paris_topk_order of the top-k lists                */
 } paris_config;
 
 /* Zone bookkeeping, identical for every sequence of the batch.
@@ -130,10 +139,14 @@ paris_status paris_append_decode(paris_ctx* ctx, const void* k, const void* v, p
  * the top C = max(ceil(p N), min(k, N)) keys by (votes desc, position asc)
  * as candidates, RSQ-IP rerank, top min(k, C) by (estimate desc, position
  * asc)).  q: device, dtype, [batch][Hq][d].  topk_idx: device int32
- * [batch][Hq][topk] receives absolute token positions in ascending order;
- * topk_score: device float32, same layout, the RSQ-IP estimates of <k, q>;
- * entries past k_eff are -1 and -inf.  topk_score may be NULL.  k_eff: host,
- * receives min(topk, C) (0 while the Retrieval zone is empty).              */
+ * [batch][Hq][topk] receives absolute token positions, listed by (estimate
+ * desc, position asc) with topk_order = PARIS_TOPK_BY_SCORE, in ascending
+ * position with PARIS_TOPK_BY_POSITION; topk_score: device float32, same
+ * layout, the RSQ-IP estimates of <k, q> of those positions; entries past
+ * k_eff are -1 and -inf.  topk_score may be NULL.  k_eff: host, receives
+ * min(topk, C) (0 while the Retrieval zone is empty).  One launch (with
+ * PARIS_TOPK_BY_SCORE its blocks first write position order to context
+ * scratch, then one block per query head sorts it into topk_idx/score).    */
 paris_status paris_retrieve(paris_ctx* ctx, const void* q, paris_dtype dtype, int32_t* topk_idx,
                             float* topk_score, int64_t* k_eff, void* stream);
 
@@ -189,7 +202,7 @@ paris_status paris_set_centroids(paris_ctx* ctx, const float* centroids, void* s
  * top-k sets overlap).  Each head's set is a superset of its own
  * paris_sparse_attend set; with G = 1 the two calls attend over the same
  * rows.  topk_idx: device int32 [batch][Hq][topk] as produced by
- * paris_retrieve (ascending per head; entries < 0 are skipped, entries
+ * paris_retrieve (in either order; entries < 0 are skipped, entries
  * outside the Retrieval zone skipped and flagged).  q and out as in
  * paris_sparse_attend.  Same arithmetic as paris_dense_attend.  Limits: at
  * most 16 query heads per KV head and G x k_eff <= 32768, else PARIS_EINVAL.
@@ -221,7 +234,8 @@ paris_status paris_dense_attend(paris_ctx* ctx, const void* q, paris_dtype dtype
  * blocks that serve each query head).  One kernel launch when the append
  * does not fill the Update Buffer: the step's own token is read from k/v
  * where the attention needs it and written to the cache at the end of the
- * kernel.  When it does, the append, flush and index rebuild run first.
+ * kernel.
+ * When it does, the append, flush and index rebuild run first.
  * k, v: device, kv_dtype, [batch][Hkv][d]; q: device, q_dtype,
  * [batch][Hq][d]; outputs as in the three calls.                           */
 paris_status paris_decode_step(paris_ctx* ctx, const void* k, const void* v, paris_dtype kv_dtype, const void* q,

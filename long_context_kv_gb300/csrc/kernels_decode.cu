@@ -95,7 +95,8 @@ struct DecodeArgs {
   // q = CS): the rerank slices of the candidate list and the blocks' shares
   // of the window rows
   int64_t ccut[kClusterMax + 1], wcut[kClusterMax + 1];
-  int64_t rcut[kClusterMax + 1];  // (nwin + k_eff) q / CS: the blocks' even shares of the attention rows
+  int64_t rcut[kClusterMax + 1];  // (nwin + k_eff) q / CS: the blocks' shares of the attention rows (the last one
+                                  // smaller when it also sorts the top-k)
   uint32_t nmod;        // ring slot of the first Local token
   const void* q;
   int qdtype;
@@ -112,9 +113,11 @@ struct DecodeArgs {
   float* cand_est;
   uint32_t* status;
   uint64_t* trace;
-  int32_t* topk_idx;
+  int32_t* topk_idx;    // the lists in ascending position (every block writes its slice's entries)
   float* topk_score;
   __nv_bfloat16* out;   // nullptr: no attention
+  int32_t* ord_idx;     // nullptr: no reordering; else the lists best first go here
+  float* ord_sc;
 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -134,6 +137,11 @@ __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefe
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+// The same barrier in two halves: work between them overlaps the wait.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 
 // Address of the same shared-memory variable in block `rank` of the cluster,
 // and a 32-bit store there.  Stores to other blocks are made visible by the
@@ -378,8 +386,150 @@ __device__ __forceinline__ uint32_t select_kth(KeyOf key_of, const int64_t C, co
   return prefix;
 }
 
-// kTable: the query's centroid scores come from a learned-centroid table
-// (a separate instantiation, so the analytic path's code is untouched).
+// One query head's top-k list best first.  pos_in / sc_in: its k_eff
+// entries in ascending position (global memory, written by the blocks of
+// the cluster before a cluster barrier); idx_out / sc_out: k entries by
+// (estimate desc, position asc), then (-1, -inf).  Estimates compare by
+// order_key (monotone, -0 = +0), equal ones by slot (= position order).
+// Every thread of the block calls these; they start with a barrier (the
+// caller's last reads of `sm`, shared memory of kUAttnEnd bytes, are done).
+//
+// Up to kOrdCount entries: a counting sort.  The estimates go into nb bins
+// of equal width over [min, max] (bin floor((e - min) nb / (max - min)) in
+// float32, round to nearest: monotone in e), numbered from the largest
+// down; a bin's start is the number of entries in the bins before it, and
+// an entry's rank is its bin's start plus the entries of its bin that
+// precede it, found by comparing with them.  When a bin holds more than
+// kOrdBinMax entries (many equal estimates, or a few far from the rest) the
+// keys are sorted instead (order_bitonic), so the comparisons stay bounded.
+constexpr int kOrdCount = 4096;
+constexpr uint32_t kOrdBinMax = 64;
+
+// The bitonic sort of the 64-bit keys (~order_key << 32 | slot) at `skey`
+// (n2 >= k_eff, a power of two); positions and estimates come from spos /
+// ssc when given (shared memory), else from global memory again.
+__device__ __forceinline__ void order_bitonic(const int32_t* pos_in, const float* sc_in, int32_t* idx_out,
+                                              float* sc_out, int k, int k_eff, int n2, unsigned long long* skey,
+                                              const uint32_t* key, const int32_t* spos, const float* ssc) {
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    unsigned long long v = ~0ull;  // padding sorts last
+    if (i < k_eff) v = ((unsigned long long)~(key ? key[i] : order_key(__ldcg(sc_in + i))) << 32) | (uint32_t)i;
+    skey[i] = v;
+  }
+  block_sort_pow2(skey, n2);
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    int32_t p = -1;
+    float e = -INFINITY;
+    if (i < k_eff) {
+      const uint32_t slot = (uint32_t)skey[i];
+      p = spos ? spos[slot] : __ldcg(pos_in + slot);
+      e = ssc ? ssc[slot] : __ldcg(sc_in + slot);
+    }
+    idx_out[i] = p;
+    if (sc_out) sc_out[i] = e;
+  }
+}
+
+__device__ __forceinline__ void order_topk(const int32_t* pos_in, const float* sc_in, int32_t* idx_out, float* sc_out,
+                                           int k, int k_eff, uint8_t* sm, uint32_t* red, uint32_t* tmp) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  int n2 = 64;
+  while (n2 < k_eff) n2 <<= 1;
+  __syncthreads();
+  if (k_eff > kOrdCount) {
+    order_bitonic(pos_in, sc_in, idx_out, sc_out, k, k_eff, n2, reinterpret_cast<unsigned long long*>(sm), nullptr,
+                  nullptr, nullptr);
+    return;
+  }
+  // [0, 64 KB): key, position, estimate and the binned slots of kOrdCount
+  // entries; [64 KB, 128 KB): the bins' counts and starts (nb <= 8192)
+  uint32_t* key = reinterpret_cast<uint32_t*>(sm);
+  int32_t* spos = reinterpret_cast<int32_t*>(sm + 4 * kOrdCount);
+  float* ssc = reinterpret_cast<float*>(sm + 8 * kOrdCount);
+  uint32_t* bslot = reinterpret_cast<uint32_t*>(sm + 12 * kOrdCount);
+  const int nb = n2 >= 1024 ? 2 * n2 : 2048;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(sm + 16 * kOrdCount);
+  uint32_t* base = cnt + 2 * kOrdCount;
+  float fmin = INFINITY, fmax = -INFINITY;
+  for (int i = tid; i < k_eff; i += nt) {
+    const float e = __ldcg(sc_in + i);
+    key[i] = order_key(e);
+    spos[i] = __ldcg(pos_in + i);
+    ssc[i] = e;
+    fmin = fminf(fmin, e);
+    fmax = fmaxf(fmax, e);
+  }
+  for (int b = tid; b < nb; b += nt) cnt[b] = 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    fmin = fminf(fmin, __shfl_xor_sync(kFull, fmin, o));
+    fmax = fmaxf(fmax, __shfl_xor_sync(kFull, fmax, o));
+  }
+  if (lane == 0) {
+    red[warp] = __float_as_uint(fmin);
+    red[32 + warp] = __float_as_uint(fmax);
+  }
+  __syncthreads();
+  fmin = lane < nw ? __uint_as_float(red[lane]) : INFINITY;
+  fmax = lane < nw ? __uint_as_float(red[32 + lane]) : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    fmin = fminf(fmin, __shfl_xor_sync(kFull, fmin, o));
+    fmax = fmaxf(fmax, __shfl_xor_sync(kFull, fmax, o));
+  }
+  const float width = __fsub_rn(fmax, fmin);  // +inf: every entry in one bin, then the sort
+  const float scale = width > 0.f ? __fdiv_rn((float)nb, width) : 0.f;
+  // bin of slot i, numbered from the largest estimate down
+  auto bin_of = [&](int i) -> uint32_t {
+    const float x = fminf(__fmul_rn(__fsub_rn(ssc[i], fmin), scale), (float)(nb - 1));
+    return (uint32_t)(nb - 1) - (uint32_t)x;
+  };
+  for (int i = tid; i < k_eff; i += nt) atomicAdd(&cnt[bin_of(i)], 1u);
+  __syncthreads();
+  const int per = nb / nt;  // nb >= 2048 >= nt
+  uint32_t sum = 0, cm = 0;
+  for (int j = 0; j < per; ++j) {
+    const uint32_t c = cnt[tid * per + j];
+    sum += c;
+    cm = max(cm, c);
+  }
+  uint32_t total;
+  uint32_t off = block_excl_scan(sum, tmp, &total);  // its barriers also end the reads of red above
+  for (int j = 0; j < per; ++j) {
+    base[tid * per + j] = off;
+    off += cnt[tid * per + j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cm = max(cm, __shfl_xor_sync(kFull, cm, o));
+  if (lane == 0) red[warp] = cm;
+  __syncthreads();
+  cm = lane < nw ? red[lane] : 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cm = max(cm, __shfl_xor_sync(kFull, cm, o));
+  if (cm > kOrdBinMax) {  // the same in every thread; the counts and starts are read no more
+    __syncthreads();
+    order_bitonic(pos_in, sc_in, idx_out, sc_out, k, k_eff, n2, reinterpret_cast<unsigned long long*>(cnt), key,
+                  spos, ssc);
+    return;
+  }
+  for (int i = tid; i < k_eff; i += nt) bslot[atomicAdd(&base[bin_of(i)], 1u)] = (uint32_t)i;  // base: bin ends
+  __syncthreads();
+  for (int i = tid; i < k_eff; i += nt) {
+    const uint32_t kk = key[i], b = bin_of(i), end = base[b];
+    uint32_t rank = end - cnt[b];
+    for (uint32_t m = end - cnt[b]; m < end; ++m) {
+      const uint32_t s2 = bslot[m], k2 = key[s2];
+      rank += (k2 > kk || (k2 == kk && s2 < (uint32_t)i)) ? 1u : 0u;
+    }
+    idx_out[rank] = spos[i];
+    if (sc_out) sc_out[rank] = ssc[i];
+  }
+  for (int i = k_eff + tid; i < k; i += nt) {
+    idx_out[i] = -1;
+    if (sc_out) sc_out[i] = -INFINITY;
+  }
+}
+
 template <bool kTable>
 __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ __align__(16) float qs[kDim];
@@ -419,6 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 
   const int r = blockIdx.x, cs = gridDim.x, sq = blockIdx.y;
   const int seq = sq / a.s.hq, qh = sq - seq * a.s.hq, kvh = qh / a.s.g;
+  // the query head's list best first, sorted in the attention staging area
+  auto order_tail = [&]() {
+    const int64_t row = (int64_t)sq * a.k;
+    order_topk(a.topk_idx + row, a.topk_score + row, a.ord_idx + row, a.ord_sc ? a.ord_sc + row : nullptr,
+               (int)a.k, (int)a.k_eff, U, red, tmp);
+  };
   const int64_t sh = (int64_t)seq * a.s.hkv + kvh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c_lo = min(r * a.cpb, a.nchunk_active), c_hi = min(c_lo + a.cpb, a.nchunk_active);
@@ -1258,7 +1414,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       for (int w2 = 0; w2 < kWarps; ++w2) ob += wo[w2 * kDim + tid] * wml[2 * w2 + 1];
       dsmem_st_u32(dsmem_addr(&pall[r][4 + tid], 0), __float_as_uint(ob));
     }
-    // every block's partial is in block 0; only block 0 reads shared memory after this
+    // every block's partial is in block 0; only block 0 reads shared memory
+    // after this.  Between the halves of the barrier the last block (not
+    // block 0) lists the top-k best first (every slice's entries were in
+    // global memory at the barrier before the attention; its row share is
+    // the smaller one), then it is done.
+    if (a.ord_idx != nullptr && r == cs - 1 && r != 0) {
+      cluster_arrive();
+      trace_block(a.trace, kTkDecode2, 3);
+      order_tail();
+      trace_block(a.trace, kTkDecode2, 2);
+      cluster_wait();
+      return;
+    }
     cluster_sync();
     trace_mark(tr, kTrDecode5);
     if (r == 0 && tid < kDim) {
@@ -1285,6 +1453,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       a.out[(int64_t)sq * kDim + tid] = __float2bfloat16_rn(Lt > 0.f ? ot / Lt : 0.f);
     }
     trace_block(a.trace, kTkDecode2, 1);
+  }
+
+  // ---- 6. the list best first ------------------------------------------------
+  // Without attention every slice's entries are in global memory after one
+  // more barrier, and the last block sorts them; with attention a cluster
+  // of one block sorts here (a larger one did inside its last barrier).
+  if (a.ord_idx != nullptr) {
+    if (a.out == nullptr) cluster_sync();
+    if (r == cs - 1 && (a.out == nullptr || cs == 1)) order_tail();
   }
 
   trace_mark(tr, kTrDecode6);
@@ -1359,6 +1536,28 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.topk_idx = ra.topk_idx;
   a.topk_score = ra.topk_score;
   a.out = L.out;
+  a.ord_idx = L.ord_idx;
+  a.ord_sc = L.ord_sc;
+  static_assert(kOrderMax * 8 <= kUAttnEnd && 32 * kOrdCount <= kUAttnEnd, "the orderings fit the staging area");
+  // With the sort, the last block's share of the attention rows is cut by
+  // up to two rounds of rows below what an even share needs (the sort takes
+  // about as long as two rounds), as far as the other blocks' larger shares
+  // still fit the rounds an even share needs: the sort then overlaps the
+  // other blocks' attention.
+  if (L.ord_idx != nullptr && L.out != nullptr && cs > 1) {
+    constexpr int64_t kRoundRows = 128;  // rows per attention round
+    const int64_t total = L.nwin + ra.k_eff;
+    const int64_t rounds = ((total + cs - 1) / cs + kRoundRows - 1) / kRoundRows;
+    for (int64_t cut = 2; cut >= 1; --cut) {
+      if (rounds - cut < 0) continue;
+      const int64_t last = (rounds - cut) * kRoundRows, rest = total - last;
+      if ((rest + cs - 2) / (cs - 1) <= rounds * kRoundRows) {
+        for (int q = 0; q <= kClusterMax; ++q) a.rcut[q] = q < cs ? rest * q / (cs - 1) : total;
+        break;
+      }
+    }
+  }
+  if (L.ord_idx != nullptr && (ra.k_eff > kOrderMax || ra.topk_score == nullptr)) return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUBytes);

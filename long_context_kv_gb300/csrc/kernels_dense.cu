@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   __shared__ float wml[kDWarps][kDMaxHeads][2];
   __shared__ float fs[kDMaxHeads][kDWarps];
   __shared__ int s_last;
+  pdl_wait();  // the list, its length and the cache may come from the kernel before
 
   const int split = blockIdx.x;
   const int sh_i = blockIdx.y;  // sequence * Hkv + KV head
@@ -363,37 +364,34 @@ constexpr int kUnionThreads = 1024;
 __global__ void __launch_bounds__(kUnionThreads) k_union(const int32_t* __restrict__ topk_idx, int64_t k, int k_eff,
                                                          Shape s, int64_t N, int32_t* list, int32_t* n,
                                                          int64_t stride, uint32_t* status) {
-  extern __shared__ int32_t ul[];  // [G][k_eff]
+  extern __shared__ uint32_t ul[];  // [n2]: the G k_eff entries, then padding; sorted ascending
   __shared__ uint32_t tmp[33];
   const int sh = blockIdx.x, seq = sh / s.hkv, kvh = sh - seq * s.hkv;
   const int G = s.g, tot = G * k_eff, tid = threadIdx.x;
-  for (int e = tid; e < tot; e += kUnionThreads) {
-    const int h = e / k_eff, i = e - h * k_eff;
-    ul[e] = __ldg(topk_idx + ((int64_t)seq * s.hq + kvh * G + h) * k + i);
-  }
-  __syncthreads();
-  // thread t owns entries [t per, t per + per) of the G k_eff entries
-  const int per = (tot + kUnionThreads - 1) / kUnionThreads;
-  const int e0 = min(tot, tid * per), e1 = min(tot, e0 + per);
-  uint32_t keep = 0;  // bit j: entry e0 + j is kept (per <= 32)
-  for (int e = e0; e < e1; ++e) {
-    const int32_t x = ul[e];
-    bool kp = x >= s.sink && x < s.sink + N;
-    if (!kp && x >= 0) atomicOr(status, kStatusBadIndex);
-    for (int h2 = 0; kp && h2 < e / k_eff; ++h2) {
-      int lo = 0, hi = k_eff;  // first entry >= x in list h2
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (ul[h2 * k_eff + mid] < x) lo = mid + 1; else hi = mid;
-      }
-      if (lo < k_eff && ul[h2 * k_eff + lo] == x) kp = false;
+  int n2 = 64;
+  while (n2 < tot) n2 <<= 1;
+  pdl_wait();
+  for (int e = tid; e < n2; e += kUnionThreads) {
+    uint32_t x = 0xffffffffu;  // skipped: padding, entries < 0, entries outside the Retrieval zone
+    if (e < tot) {
+      const int h = e / k_eff, i = e - h * k_eff;
+      const int32_t p = topk_idx[((int64_t)seq * s.hq + kvh * G + h) * k + i];
+      if (p >= s.sink && p < s.sink + N) x = (uint32_t)p;
+      else if (p >= 0) atomicOr(status, kStatusBadIndex);
     }
-    if (kp) keep |= 1u << (e - e0);
+    ul[e] = x;
   }
+  block_sort_pow2(ul, n2);
+  // thread t owns entries [t per, t per + per): it keeps the first of each run
+  const int per = n2 / kUnionThreads > 0 ? n2 / kUnionThreads : 1;
+  const int e0 = min(n2, tid * per), e1 = min(n2, e0 + per);
+  uint32_t keep = 0;  // bit j: entry e0 + j is kept (per <= 32)
+  for (int e = e0; e < e1; ++e)
+    if (ul[e] != 0xffffffffu && (e == 0 || ul[e - 1] != ul[e])) keep |= 1u << (e - e0);
   uint32_t total;
   uint32_t at = block_excl_scan((uint32_t)__popc(keep), tmp, &total);
   for (int e = e0; e < e1; ++e)
-    if ((keep >> (e - e0)) & 1u) list[(int64_t)sh * stride + at++] = ul[e];
+    if ((keep >> (e - e0)) & 1u) list[(int64_t)sh * stride + at++] = (int32_t)ul[e];
   if (tid == 0) n[sh] = (int32_t)total;
 }
 
@@ -403,7 +401,9 @@ cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shap
                          int32_t* n, int64_t stride, uint32_t* status, cudaStream_t st) {
   const int64_t tot = (int64_t)s.g * k_eff;
   if (tot > 32 * kUnionThreads) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)std::max<int64_t>(1, tot) * sizeof(int32_t);
+  int64_t n2 = 64;
+  while (n2 < tot) n2 <<= 1;
+  const size_t smem = (size_t)n2 * sizeof(uint32_t);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_union, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * kUnionThreads * 4);

@@ -48,6 +48,8 @@ struct paris_ctx {
   int32_t* union_list;  // GQA-shared attention: [batch*Hkv][G*topk] union of the G top-k lists
   int32_t* union_n;     // [batch*Hkv]
   float* cent_table;    // learned centroids [Hkv][16][256][8] (used when t.cent points to it)
+  int32_t* ord_idx;     // top-k by score: the decode kernel's [batch*Hq][topk] positions, ascending
+  float* ord_sc;        // and their estimates, before the order kernel lists them best first
   int dense_splits_max, sm_count;
   uint64_t* trace;     // kTraceSlots phase timestamps
   bool tracing;        // PARIS_TRACE=1 in the environment at creation
@@ -158,7 +160,7 @@ void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
                  c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status,
                  c->counters, c->trace, c->dense_part, c->dense_counter, c->union_list, c->union_n,
-                 c->cent_table};
+                 c->cent_table, c->ord_idx, c->ord_sc};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_store) {
@@ -295,8 +297,11 @@ paris_status retrieve_launch(paris_ctx* c, const void* q, paris_dtype dtype, int
     }
     return PARIS_OK;
   }
+  // by score: the decode kernel writes position order to the context's
+  // scratch and, at its end, lists it best first into the caller's arrays
+  const bool by_score = c->cfg.topk_order == PARIS_TOPK_BY_SCORE;
   DecodeLaunch L;
-  L.ra = retrieve_args(c, topk_idx, topk_score);
+  L.ra = by_score ? retrieve_args(c, c->ord_idx, c->ord_sc) : retrieve_args(c, topk_idx, topk_score);
   L.kv = c->kv;
   L.nsink = std::min<int64_t>(c->s.sink, c->T);
   L.nwin = L.nsink + c->n_local + c->n_buf;
@@ -308,6 +313,8 @@ paris_status retrieve_launch(paris_ctx* c, const void* q, paris_dtype dtype, int
   L.new_pos = tok ? tok->pos : -1;
   L.status = c->status;
   L.out = static_cast<__nv_bfloat16*>(out);
+  L.ord_idx = by_score ? topk_idx : nullptr;
+  L.ord_sc = by_score ? topk_score : nullptr;
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_DECODE, s, [&] { return launch_decode(L, s); }));
   *k_eff = L.ra.k_eff;
   return PARIS_OK;
@@ -339,6 +346,10 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   if (f.sink < 0 || f.local < 0 || f.update_buf < 1 || f.topk < 1 || f.cand_bp < 1 || f.cand_bp > 10000 ||
       f.max_ctx < 0)
     return fail(nullptr, PARIS_EINVAL, "sink, local >= 0; update_buf, topk >= 1; cand_bp in [1, 10000]; max_ctx >= 0");
+  if (f.topk_order != PARIS_TOPK_BY_SCORE && f.topk_order != PARIS_TOPK_BY_POSITION)
+    return fail(nullptr, PARIS_EINVAL, "unknown topk_order");
+  if (f.topk_order == PARIS_TOPK_BY_SCORE && f.topk > kOrderMax)
+    return fail(nullptr, PARIS_EINVAL, "topk above %lld needs topk_order = PARIS_TOPK_BY_POSITION", (long long)kOrderMax);
   for (int i = 0; i < kDim; ++i)
     if (srht_signs[i] != 1 && srht_signs[i] != -1) return fail(nullptr, PARIS_EINVAL, "srht_signs[%d] is not +-1", i);
 
@@ -434,6 +445,10 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   TRY(dalloc(c, &c->union_list, (size_t)bq * f.topk * sizeof(int32_t), "top-k unions"));
   TRY(dalloc(c, &c->union_n, (size_t)bh * sizeof(int32_t), "top-k union sizes"));
   TRY(dalloc(c, &c->cent_table, (size_t)f.n_kv_heads * kTabPerHead * sizeof(float), "centroid table"));
+  if (f.topk_order == PARIS_TOPK_BY_SCORE) {
+    TRY(dalloc(c, &c->ord_idx, (size_t)bq * f.topk * sizeof(int32_t), "top-k positions before ordering"));
+    TRY(dalloc(c, &c->ord_sc, (size_t)bq * f.topk * sizeof(float), "top-k estimates before ordering"));
+  }
   {
     const char* env = std::getenv("PARIS_TRACE");
     c->tracing = env != nullptr && env[0] == '1';

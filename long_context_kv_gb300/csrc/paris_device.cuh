@@ -128,6 +128,76 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* tmp, u
   return r;
 }
 
+__device__ __forceinline__ uint32_t shfl_xor_key(uint32_t x, int j) { return __shfl_xor_sync(kFull, x, j); }
+__device__ __forceinline__ unsigned long long shfl_xor_key(unsigned long long x, int j) {
+  return __shfl_xor_sync(kFull, x, j);
+}
+
+// One merge level k of Batcher's bitonic network on an aligned 64-element
+// chunk held by a warp, two elements per lane (a = element ea = c + lane,
+// b = element ea + 32): the distances min(k/2, 32) .. 1, ascending where
+// bit k of the element index is 0.
+template <typename T>
+__device__ __forceinline__ void warp_merge_level(T& a, T& b, int ea, int lane, int k) {
+  if (k >= 64) {  // distance 32: the pair (a, b), one direction for both
+    const T lo = a < b ? a : b, hi = a < b ? b : a;
+    const bool asc = (ea & k) == 0;
+    a = asc ? lo : hi;
+    b = asc ? hi : lo;
+  }
+  const bool asc_a = (ea & k) == 0, asc_b = ((ea + 32) & k) == 0;
+#pragma unroll
+  for (int j = 16; j >= 1; j >>= 1) {
+    if (j < k) {
+      const bool lower = (lane & j) == 0;
+      const T pa = shfl_xor_key(a, j), pb = shfl_xor_key(b, j);
+      a = ((lower == asc_a) == (pa < a)) ? pa : a;  // the smaller of the pair where lower == ascending
+      b = ((lower == asc_b) == (pb < b)) ? pb : b;
+    }
+  }
+}
+
+// Sort s[0, n) ascending in shared memory (Batcher's bitonic network); n a
+// power of two >= 64, keys distinct or not, every thread of the block calls
+// it (blockDim.x a multiple of 32).  A merge of level k compares elements j
+// apart for j = k/2 .. 1, ascending where bit k of the lower index is 0.
+// Distances j >= 64 go through shared memory, one barrier each; j <= 32 run
+// inside one warp on aligned 64-element chunks (warp_merge_level).  Starts
+// and ends with a barrier.
+template <typename T>
+__device__ void block_sort_pow2(T* s, int n) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();
+  for (int c = warp * 64; c < n; c += nw * 64) {  // levels 2 .. 64 inside each chunk
+    T a = s[c + lane], b = s[c + 32 + lane];
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1) warp_merge_level(a, b, c + lane, lane, k);
+    s[c + lane] = a;
+    s[c + 32 + lane] = b;
+  }
+  __syncthreads();
+  for (int k = 128; k <= n; k <<= 1) {
+    for (int j = k >> 1; j >= 64; j >>= 1) {
+      for (int i = threadIdx.x; i < (n >> 1); i += blockDim.x) {
+        const int lo = 2 * i - (i & (j - 1)), hi = lo + j;
+        const T x = s[lo], y = s[hi];
+        if ((y < x) == ((lo & k) == 0)) {
+          s[lo] = y;
+          s[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+    for (int c = warp * 64; c < n; c += nw * 64) {
+      T a = s[c + lane], b = s[c + 32 + lane];
+      warp_merge_level(a, b, c + lane, lane, k);
+      s[c + lane] = a;
+      s[c + 32 + lane] = b;
+    }
+    __syncthreads();
+  }
+}
+
 // Encode one key held by a warp (lane l owns coordinates 4l..4l+3 of the
 // raw key).  Float32 order, every operation rounded once:
 //   z = fwht(D * k);  id_b bit j = [z_{b,j} < 0];

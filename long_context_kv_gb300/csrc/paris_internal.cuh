@@ -115,6 +115,10 @@ struct DecodeLaunch {
   int64_t new_pos;
   uint32_t* status;
   __nv_bfloat16* out;
+  // the caller's arrays for the lists best first (ord_idx nullptr: the lists
+  // stay in ra.topk_idx / ra.topk_score in ascending position)
+  int32_t* ord_idx;
+  float* ord_sc;
 };
 
 // Launch `kern` so that it may start while the preceding kernel of the
@@ -181,6 +185,11 @@ struct DenseArgs {
 cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shape s, int64_t N, int32_t* list,
                          int32_t* n, int64_t stride, uint32_t* status, cudaStream_t st);
 int dense_splits(const DenseArgs& a, int sm_count);  // splits per (sequence, KV head)
+
+// Top-k lists best first: at most kOrderMax entries per query head are
+// sorted by (estimate descending, position ascending) in one block's shared
+// memory at the end of the decode kernel.
+constexpr int64_t kOrderMax = 16384;
 int64_t dense_rows_per_split(int64_t T, int nsplit);
 cudaError_t launch_dense(const DenseArgs& a, int nsplit, cudaStream_t st);
 

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libparis.so")
 PARIS_OK, PARIS_EINVAL, PARIS_ENOMEM, PARIS_ECUDA, PARIS_ESTATE, PARIS_ECAPACITY, PARIS_EDEVICE = 0, -1, -2, -3, -4, -6, -7
 PARIS_F32, PARIS_BF16 = 0, 1
 PARIS_VOTE_RANK, PARIS_VOTE_FLAT = 0, 1
+PARIS_TOPK_BY_SCORE, PARIS_TOPK_BY_POSITION = 0, 1
 (DUMP_IDS, DUMP_CODES, DUMP_W, DUMP_VOTES, DUMP_CANDS, DUMP_CAND_EST, DUMP_QT, DUMP_QNORM, DUMP_HOT,
  DUMP_LEVELS, DUMP_KV, DUMP_TRACE) = range(12)
 
@@ -60,7 +61,7 @@ KERNELS = ["place_kv", "encode", "build_index", "append", "decode", "attend", "f
 class paris_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "batch", "n_kv_heads", "n_q_heads", "head_dim", "n_sub", "rho", "sink", "local", "update_buf",
-        "topk", "cand_bp", "max_ctx", "retrieval_on_host", "vote_weighting")]
+        "topk", "cand_bp", "max_ctx", "retrieval_on_host", "vote_weighting", "topk_order")]
 
 
 class paris_state(ctypes.Structure):
@@ -135,7 +136,7 @@ def make_config(**kw) -> paris_config:
     cfg = paris_config()
     defaults = dict(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=128, n_sub=16, rho=4, sink=0, local=0,
                     update_buf=128, topk=64, cand_bp=1000, max_ctx=4096, retrieval_on_host=0,
-                    vote_weighting=PARIS_VOTE_RANK)
+                    vote_weighting=PARIS_VOTE_RANK, topk_order=PARIS_TOPK_BY_SCORE)
     defaults.update(kw)
     for k, v in defaults.items():
         setattr(cfg, k, int(v))

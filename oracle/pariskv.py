@@ -488,12 +488,12 @@ def estimator_ideal(v: np.ndarray, w: np.ndarray, qnorm: float, qt: np.ndarray) 
 
 
 def topk(est: np.ndarray, cand: np.ndarray, k: int):
-    """The first min(k, C) candidates by (est desc, index asc), listed by
-    ascending index.  Returns (indices, their estimates)."""
+    """The first min(k, C) candidates by (est desc, index asc), listed in
+    that order.  Returns (indices, their estimates)."""
     est = np.asarray(est)
     cand = np.asarray(cand, dtype=np.int64)
     order = np.lexsort((cand, -est.astype(np.float64)))
-    keep = np.sort(order[:min(k, len(cand))])
+    keep = order[:min(k, len(cand))]
     return cand[keep], est[keep]
 
 

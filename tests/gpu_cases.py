@@ -201,3 +201,11 @@ def check_attention(c: Case, qd: torch.Tensor, idx: torch.Tensor, k_eff: int, he
         worst = max(worst, err)
         assert err <= ATTN_ATOL, (seq, qh, err)
     return worst
+
+
+def assert_score_order(idx: np.ndarray, sc: np.ndarray, k_eff: int):
+    """Each top-k list (last axis) is listed by (estimate desc, position asc)
+    over its first k_eff entries: the order the top-k contract fixes."""
+    dk = np.diff(sc[..., :k_eff].astype(np.float64), axis=-1)
+    di = np.diff(idx[..., :k_eff].astype(np.int64), axis=-1)
+    assert np.all((dk < 0) | ((dk == 0) & (di > 0)))

@@ -324,11 +324,16 @@ def pin_candidate_counts(o):
         assert o.candidate_count(n, bp, k) == c, row
 
 
-def _check_ordered_selection(keys, chosen, c):
-    """chosen must be the c best by (key desc, index asc)."""
+def _check_ordered_selection(keys, chosen, c, listed="index"):
+    """chosen must be the c best by (key desc, index asc), listed by ascending
+    index or (listed="key") in that order."""
     keys = np.asarray(keys)
     n = len(keys)
     assert len(chosen) == c and len(set(chosen.tolist())) == c
+    if listed == "key":
+        dk, di = np.diff(keys[chosen].astype(np.float64)), np.diff(chosen)
+        assert np.all((dk < 0) | ((dk == 0) & (di > 0)))
+        chosen = np.sort(chosen)
     assert np.all(np.diff(chosen) > 0)
     if c == 0 or c == n:
         return
@@ -353,7 +358,7 @@ def pin_selection(o):
             cand = np.sort(rng.choice(10 * n, n, replace=False))
             ti, te = o.topk(est, cand, c)
             pos = np.searchsorted(cand, ti)
-            _check_ordered_selection(est + 0.0, pos, c)
+            _check_ordered_selection(est + 0.0, pos, c, listed="key")
             np.testing.assert_array_equal(te, est[pos])
     assert len(o.select_candidates(np.arange(10), 10)) == 10
 
@@ -372,6 +377,8 @@ def pin_recall_one_at_full_candidates(o):
     est = o.estimator_ideal(enc["v"], enc["w"], qn, qt)
     top, _ = o.topk(est, cand, 64)
     assert o.recall(top, o.exact_topk(K, q, 64)) == 1.0
+    # and listed best first, as a library sort of the exact products lists them
+    np.testing.assert_array_equal(top, np.argsort(-(K @ q), kind="stable")[:64])
 
 
 # --- attention and zones ---------------------------------------------------

@@ -52,6 +52,8 @@ MUTATIONS = [
      "order = np.lexsort((idx, np.asarray(scores, dtype=np.int64)))", P.pin_selection),
     ("top-k ties to higher index", "order = np.lexsort((cand, -est.astype(np.float64)))",
      "order = np.lexsort((-cand, -est.astype(np.float64)))", P.pin_selection),
+    ("top-k listed by position", "keep = order[:min(k, len(cand))]", "keep = np.sort(order[:min(k, len(cand))])",
+     P.pin_selection),
     ("attention unscaled", "s = K @ q / math.sqrt(q.shape[0])", "s = K @ q", P.pin_attention_dense),
     ("zone eviction off by one", "evict = max(0, self.n_local - self.L)", "evict = max(0, self.n_local - self.L - 1)",
      P.pin_zones),
