@@ -355,29 +355,63 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
 }
 
 // The union of the G query heads' top-k lists of (sequence, KV head)
-// blockIdx.x.  Each list is ascending with distinct positions, so a
-// position of head h's list is a repeat exactly when a binary search finds
-// it in the list of an earlier head; the kept positions are compacted in
-// list order (head by head).  Positions outside the Retrieval zone are
-// dropped and flagged.
+// blockIdx.x, in ascending position, whatever order the lists are in.
+// While the Retrieval zone's bitmap fits shared memory (N <= 32 x
+// kUnionThreads x 32 tokens), every listed position sets its bit and the
+// set bits are read out in order (each thread owns a run of words; a block
+// scan of the runs' bit counts places them).  Otherwise the concatenated
+// lists are sorted (bitonic) and the first of each run of equal positions
+// kept.  Positions outside the Retrieval zone are dropped and flagged.
 constexpr int kUnionThreads = 1024;
+constexpr int64_t kUnionWords = 32 * kUnionThreads;  // shared-memory words: bitmap or sort keys
 __global__ void __launch_bounds__(kUnionThreads) k_union(const int32_t* __restrict__ topk_idx, int64_t k, int k_eff,
                                                          Shape s, int64_t N, int32_t* list, int32_t* n,
                                                          int64_t stride, uint32_t* status) {
-  extern __shared__ uint32_t ul[];  // [n2]: the G k_eff entries, then padding; sorted ascending
+  extern __shared__ uint32_t ul[];  // the bitmap of the zone, or the G k_eff entries sorted
   __shared__ uint32_t tmp[33];
   const int sh = blockIdx.x, seq = sh / s.hkv, kvh = sh - seq * s.hkv;
   const int G = s.g, tot = G * k_eff, tid = threadIdx.x;
+  const int64_t nwords = (N + 31) / 32;
+  auto entry = [&](int e) -> int32_t {
+    const int h = e / k_eff, i = e - h * k_eff;
+    const int32_t p = topk_idx[((int64_t)seq * s.hq + kvh * G + h) * k + i];
+    if (p >= s.sink && p < s.sink + N) return p;
+    if (p >= 0) atomicOr(status, kStatusBadIndex);
+    return -1;
+  };
+  pdl_wait();
+  if (nwords <= kUnionWords) {
+    for (int64_t w = tid; w < nwords; w += kUnionThreads) ul[w] = 0u;
+    __syncthreads();
+    for (int e = tid; e < tot; e += kUnionThreads) {
+      const int32_t p = entry(e);
+      if (p >= 0) atomicOr(&ul[(p - s.sink) >> 5], 1u << ((p - s.sink) & 31));
+    }
+    __syncthreads();
+    const int64_t per = (nwords + kUnionThreads - 1) / kUnionThreads;
+    const int64_t w0 = min64(nwords, tid * per), w1 = min64(nwords, w0 + per);
+    uint32_t cnt = 0;
+    for (int64_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(ul[w]);
+    uint32_t total;
+    uint32_t at = block_excl_scan(cnt, tmp, &total);
+    for (int64_t w = w0; w < w1; ++w) {
+      uint32_t bits = ul[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        list[(int64_t)sh * stride + at++] = (int32_t)(s.sink + w * 32 + b);
+      }
+    }
+    if (tid == 0) n[sh] = (int32_t)total;
+    return;
+  }
   int n2 = 64;
   while (n2 < tot) n2 <<= 1;
-  pdl_wait();
   for (int e = tid; e < n2; e += kUnionThreads) {
-    uint32_t x = 0xffffffffu;  // skipped: padding, entries < 0, entries outside the Retrieval zone
+    uint32_t x = 0xffffffffu;  // skipped: padding and dropped entries
     if (e < tot) {
-      const int h = e / k_eff, i = e - h * k_eff;
-      const int32_t p = topk_idx[((int64_t)seq * s.hq + kvh * G + h) * k + i];
-      if (p >= s.sink && p < s.sink + N) x = (uint32_t)p;
-      else if (p >= 0) atomicOr(status, kStatusBadIndex);
+      const int32_t p = entry(e);
+      if (p >= 0) x = (uint32_t)p;
     }
     ul[e] = x;
   }
@@ -403,10 +437,11 @@ cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shap
   if (tot > 32 * kUnionThreads) return cudaErrorInvalidValue;
   int64_t n2 = 64;
   while (n2 < tot) n2 <<= 1;
-  const size_t smem = (size_t)n2 * sizeof(uint32_t);
+  const int64_t nwords = (N + 31) / 32;
+  const size_t smem = (size_t)std::max<int64_t>(1, nwords <= kUnionWords ? nwords : n2) * sizeof(uint32_t);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_union, cudaFuncAttributeMaxDynamicSharedMemorySize, 32 * kUnionThreads * 4);
+    cudaError_t e = cudaFuncSetAttribute(k_union, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kUnionWords * 4));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
