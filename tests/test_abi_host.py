@@ -53,7 +53,7 @@ def test_rsq_levels_match_oracle_bitwise(lib):
 @pytest.mark.parametrize("bad", [
     dict(head_dim=64), dict(n_sub=32), dict(rho=0), dict(rho=16), dict(n_q_heads=3, n_kv_heads=2),
     dict(cand_bp=0), dict(cand_bp=10001), dict(topk=0), dict(update_buf=0), dict(vote_weighting=7),
-    dict(batch=0), dict(sink=-1), dict(max_ctx=-5),
+    dict(batch=0), dict(sink=-1), dict(max_ctx=-5), dict(topk_order=2), dict(topk=16385),
 ])
 def test_create_rejects_bad_config(lib, bad):
     cfg = P.make_config(**bad)
@@ -79,3 +79,23 @@ def test_null_context_calls_fail_cleanly(lib):
     assert lib.paris_retrieve(None, None, 0, None, None, ctypes.byref(k), None) == P.PARIS_EINVAL
     assert lib.paris_append_decode(None, None, None, 0, None) == P.PARIS_EINVAL
     lib.paris_destroy(None)
+
+
+def _header_nocomments():
+    return re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+
+
+def test_binding_structs_and_enums_match_the_header():
+    src = _header_nocomments()
+    body = re.search(r"typedef struct \{(.*?)\} paris_config;", src, flags=re.S).group(1)
+    fields = re.findall(r"\bint\s+([a-z_0-9]+);", body)
+    assert fields == [n for n, _ in P.paris_config._fields_]
+    enum = dict((k, int(v)) for k, v in re.findall(r"\b(PARIS_[A-Z_0-9]+)\s*=\s*(\d+)", src))
+    assert (enum["PARIS_TOPK_BY_SCORE"], enum["PARIS_TOPK_BY_POSITION"]) == (P.PARIS_TOPK_BY_SCORE,
+                                                                              P.PARIS_TOPK_BY_POSITION)
+    assert (enum["PARIS_VOTE_RANK"], enum["PARIS_VOTE_FLAT"]) == (P.PARIS_VOTE_RANK, P.PARIS_VOTE_FLAT)
+    assert enum["PARIS_KERNEL_COUNT"] == len(P.KERNELS)
+    for name, i in enum.items():
+        if name.startswith("PARIS_KERNEL_") and name != "PARIS_KERNEL_COUNT":
+            assert P.KERNELS[i] == name[len("PARIS_KERNEL_"):].lower(), name
+    assert P.make_config().topk_order == P.PARIS_TOPK_BY_SCORE  # the contract's order is the default
