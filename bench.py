@@ -188,6 +188,20 @@ def job_throughput(keys_per_rank: float, world: int, ms_max: float) -> float:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def run_config(args, world) -> dict:
+    """The JSON line's config: the workload with the parameters it runs at."""
+    w = workload_of(args)
+    nl = args.layers or w["layers"]
+    return {"workload": DESCRIPTION[args.workload], "batch": w["batch"], "n_q_heads": w["n_q_heads"],
+            "n_kv_heads": w["n_kv_heads"], "head_dim": w["head_dim"], "context": w["context"], "sink": w["sink"],
+            "local": w["local"], "update_buf": w["update_buf"], "n_sub": w["n_sub"], "rho": w["rho"],
+            "cand_pct": w["cand_bp"] / 100, "topk": w["topk"], "topk_order": args.topk_order,
+            "retrieval_on_host": w.get("retrieval_on_host", 0), "drift_sigma_per_256_steps": w.get("drift", 0.0),
+            "kv_dtype": "f32" if args.workload == "tiny-4k" else "bf16", "layers_rotated": nl,
+            "l2": f"inputs larger than L2: {nl} layer contexts rotated, each revisited after "
+                  f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"}
+
+
 def run_ours(args, rank, world):
     import numpy as np
     import torch
@@ -215,7 +229,8 @@ def run_ours(args, rank, world):
         seed = rank_seed(rank, li)
         cfg = P.make_config(batch=b, n_kv_heads=hkv, n_q_heads=hq, head_dim=d, n_sub=w["n_sub"], rho=w["rho"],
                             sink=S, local=w["local"], update_buf=w["update_buf"], topk=w["topk"],
-                            cand_bp=w["cand_bp"], max_ctx=max_ctx, retrieval_on_host=w.get("retrieval_on_host", 0))
+                            cand_bp=w["cand_bp"], max_ctx=max_ctx, retrieval_on_host=w.get("retrieval_on_host", 0),
+                            topk_order=P.PARIS_TOPK_BY_POSITION if args.topk_order == "position" else P.PARIS_TOPK_BY_SCORE)
         ctx = P.Context(cfg, synth.srht_signs(seed, d))
         scale = torch.from_numpy(synth.channel_scale(seed, hkv, d)).cuda()
         gen.manual_seed(seed)
@@ -496,13 +511,7 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": DESCRIPTION[args.workload], "batch": b, "n_q_heads": hq, "n_kv_heads": hkv,
-                   "head_dim": d, "context": ctxlen, "sink": S, "local": w["local"], "update_buf": w["update_buf"],
-                   "n_sub": w["n_sub"], "rho": w["rho"], "cand_pct": w["cand_bp"] / 100, "topk": w["topk"],
-                   "retrieval_on_host": w.get("retrieval_on_host", 0), "drift_sigma_per_256_steps": w.get("drift", 0.0),
-                   "kv_dtype": "bf16" if fdt == torch.bfloat16 else "f32", "layers_rotated": nl,
-                   "l2": f"inputs larger than L2: {nl} layer contexts rotated, each revisited after "
-                         f"{nl - 1} other layers' steps", "parallelism": f"replicas x{world}"},
+        "config": run_config(args, world),
         "us_per_decode_step": 1e3 * ms / args.steps,
         # one token through all rotated layers: the graph launches the layers' steps back to back
         "us_per_token_all_layers": 1e3 * ms / args.steps * nl,
@@ -626,6 +635,8 @@ def main():
     ap.add_argument("--cand-bp", dest="cand_bp", type=int, default=0, help="candidates in basis points (sweep point)")
     ap.add_argument("--rho", type=int, default=0, help="hot centroids per subspace (sweep point)")
     ap.add_argument("--topk", type=int, default=0, help="k (sweep point)")
+    ap.add_argument("--topk-order", dest="topk_order", default="score", choices=["score", "position"],
+                    help="top-k lists best first (the contract's order) or in ascending position (no sort)")
     ap.add_argument("--cpu-steps", type=int, default=60)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
@@ -649,7 +660,7 @@ def main():
             "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": DESCRIPTION[args.workload]},
+            "config": run_config(args, world),
             "cpu_baseline": {"value": cb["value"], "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
                              "sample": cb["sample"]},
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
