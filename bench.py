@@ -137,9 +137,16 @@ def hbm_peak():
 TRAFFIC_SOURCES = {"decode": ["kernels_decode.cu", "kernels_attend.cu"], "dense": ["kernels_dense.cu"]}
 
 
-def traffic_record(kernel: str):
+TRAFFIC_WORKLOAD = "llama8b-128k"  # the workload the committed counters were taken on
+
+
+def traffic_record(kernel: str, args):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the kernel's source changed since the counters were taken."""
+    None when the kernel's source changed since the counters were taken or
+    the run is not the one they were taken on (its workload at its own
+    parameters, top-k best first: the bytes of a launch depend on them)."""
+    if args.workload != TRAFFIC_WORKLOAD or args.cand_bp or args.rho or args.topk or args.topk_order != "score":
+        return None
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path) or kernel not in TRAFFIC_SOURCES:
@@ -444,7 +451,7 @@ def run_ours(args, rank, world):
     if dom in alg:
         ach = alg[dom] / (kernels[dom]["us_per_launch"] * 1e-6) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom),
+                "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom, args),
                 "algorithmic_bytes": alg[dom], "design_bytes": design[dom]}
 
     # end to end through the public API with host buffers: each step's inputs
@@ -531,7 +538,7 @@ def run_ours(args, rank, world):
             "decode_step_speedup": ms_dense / (ms / args.steps),
             "hbm_gbs": b * hkv * tokens_dense * 4 * d / (ms_dense * 1e-3) / 1e9,
             "hbm_frac": round(b * hkv * tokens_dense * 4 * d / (ms_dense * 1e-3) / 1e9 / peak, 4),
-            "traffic": traffic_record("dense"),
+            "traffic": traffic_record("dense", args),
         },
         "recall_at_k": recall,
         "kernels": kernels,
