@@ -450,6 +450,7 @@ __device__ __forceinline__ void order_topk(const int32_t* pos_in, const float* s
   const int nb = n2 >= 1024 ? 2 * n2 : 2048;
   uint32_t* cnt = reinterpret_cast<uint32_t*>(sm + 16 * kOrdCount);
   uint32_t* base = cnt + 2 * kOrdCount;
+  if (tid == 0) red[64] = 0u;  // the largest bin count
   float fmin = INFINITY, fmax = -INFINITY;
   for (int i = tid; i < k_eff; i += nt) {
     const float e = __ldcg(sc_in + i);
@@ -493,19 +494,14 @@ __device__ __forceinline__ void order_topk(const int32_t* pos_in, const float* s
     sum += c;
     cm = max(cm, c);
   }
+  atomicMax(&red[64], cm);
   uint32_t total;
-  uint32_t off = block_excl_scan(sum, tmp, &total);  // its barriers also end the reads of red above
+  uint32_t off = block_excl_scan(sum, tmp, &total);  // its barriers also publish red[64]
   for (int j = 0; j < per; ++j) {
     base[tid * per + j] = off;
     off += cnt[tid * per + j];
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cm = max(cm, __shfl_xor_sync(kFull, cm, o));
-  if (lane == 0) red[warp] = cm;
-  __syncthreads();
-  cm = lane < nw ? red[lane] : 0u;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cm = max(cm, __shfl_xor_sync(kFull, cm, o));
+  cm = red[64];
   if (cm > kOrdBinMax) {  // the same in every thread; the counts and starts are read no more
     __syncthreads();
     order_bitonic(pos_in, sc_in, idx_out, sc_out, k, k_eff, n2, reinterpret_cast<unsigned long long*>(cnt), key,
@@ -530,6 +526,8 @@ __device__ __forceinline__ void order_topk(const int32_t* pos_in, const float* s
   }
 }
 
+// kTable: the query's centroid scores come from a learned-centroid table
+// (a separate instantiation, so the analytic path's code is untouched).
 template <bool kTable>
 __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ __align__(16) float qs[kDim];
