@@ -381,6 +381,97 @@ def pin_recall_one_at_full_candidates(o):
     np.testing.assert_array_equal(top, np.argsort(-(K @ q), kind="stable")[:64])
 
 
+# --- the composed retrieval (coarse candidates -> rerank -> top-k) -------------
+
+def _keys_with_duplicates(rng, n, d, n_dup):
+    """float32 keys [n, d] where n_dup rows repeat earlier rows (equal bucket
+    ids and equal estimates), so votes and estimates tie.  Returns the keys
+    and the repeated rows."""
+    K = rng.standard_normal((n, d)).astype(np.float32)
+    dups = rng.choice(np.arange(1, n), size=n_dup, replace=False) if n > 1 else np.zeros(0, np.int64)
+    for r in dups:
+        K[r] = K[rng.integers(0, r)]
+    return K, dups
+
+
+def _row_estimates(o, enc, q32, D, n_sub, lev):
+    """Estimate of every row on its own (a row's estimate does not depend on
+    which other rows are candidates), one row per call of the rerank."""
+    qp = o.query_prep_contract(q32, D, n_sub, 1, "flat")
+    return np.array([o.rerank_contract(enc["nib"][i:i + 1], enc["w"][i:i + 1], qp["qnorm"], qp["qt"], lev, n_sub)[0]
+                     for i in range(enc["nib"].shape[0])], dtype=np.float32)
+
+
+def pin_pipeline_full_candidates(o):
+    """Candidates = 100% (cand_bp = 10000): the pipeline's top-k is the first k
+    of every row sorted by (estimate desc, index asc), the brute-force top-k of
+    the estimator over the whole zone; equal estimates from duplicated keys
+    go to the lower index."""
+    rng = np.random.default_rng(23)
+    d, n_sub, m = 128, 16, 8
+    D = _signs(d, 24)
+    lev, thr = o.rsq_levels_f32(m)
+    for n, k in ((300, 40), (97, 97), (50, 200)):
+        K, dups = _keys_with_duplicates(rng, n, d, n // 5)
+        enc = o.encode_contract(K, D, n_sub, lev, thr)
+        q = (K[dups[0]] + 0.1 * rng.standard_normal(d)).astype(np.float32)  # near a key that has a copy
+        r = o.retrieve_contract(enc, q, D, n_sub, 4, 10000, k, lev)
+        est = _row_estimates(o, enc, q, D, n_sub, lev)
+        want = sorted(range(n), key=lambda i: (-float(est[i]), i))[:min(k, n)]
+        assert r["C"] == n and r["k_eff"] == min(k, n)
+        np.testing.assert_array_equal(r["cand"], np.arange(n))
+        np.testing.assert_array_equal(r["top_idx"], want)
+        np.testing.assert_array_equal(r["top_est"].view(np.uint32), est[want].view(np.uint32))
+        assert len(set(est[want].tolist())) < len(want), "the case must hold equal estimates in the top-k"
+
+
+def pin_pipeline_tiny_full_sort(o):
+    """N <= 64 with duplicated keys: the votes are the hot-list weights summed
+    by explicit loops, the candidates the first C of a full sort by (votes
+    desc, index asc), the top-k the first min(k, C) candidates of a full sort
+    by (estimate desc, index asc), and k_eff = min(k, C)."""
+    rng = np.random.default_rng(25)
+    d, n_sub, m = 128, 16, 8
+    D = _signs(d, 26)
+    lev, thr = o.rsq_levels_f32(m)
+    cases = ((64, 2500, 30, 4), (64, 1000, 5, 2), (40, 3000, 100, 8), (17, 10000, 3, 1), (1, 500, 4, 4))
+    for n, bp, k, rho in cases:
+        K, _ = _keys_with_duplicates(rng, n, d, n // 4)
+        enc = o.encode_contract(K, D, n_sub, lev, thr)
+        q = (K[n // 2] + 0.5 * rng.standard_normal(d)).astype(np.float32)
+        r = o.retrieve_contract(enc, q, D, n_sub, rho, bp, k, lev)
+        qp = r["qp"]
+        votes = np.zeros(n, dtype=np.int64)
+        for i in range(n):
+            for b in range(n_sub):
+                for rr in range(rho):
+                    if enc["ids"][i, b] == qp["hot_ids"][b, rr]:
+                        votes[i] += rho - rr
+        np.testing.assert_array_equal(r["votes"], votes)
+        c = max(-(-bp * n // 10000), min(k, n))
+        c = min(c, n)
+        cand = sorted(sorted(range(n), key=lambda i: (-int(votes[i]), i))[:c])
+        assert r["C"] == c and r["k_eff"] == min(k, c)
+        np.testing.assert_array_equal(r["cand"], cand)
+        est = _row_estimates(o, enc, q, D, n_sub, lev)
+        np.testing.assert_array_equal(r["est"].view(np.uint32), est[cand].view(np.uint32))
+        top = sorted(cand, key=lambda i: (-float(est[i]), i))[:min(k, c)]
+        np.testing.assert_array_equal(r["top_idx"], top)
+        np.testing.assert_array_equal(r["top_est"].view(np.uint32), est[top].view(np.uint32))
+    # the cases above must include candidates that are not a prefix of the zone and k > C
+    assert any(min(max(-(-bp * n // 10000), min(k, n)), n) < k for n, bp, k, _ in cases)
+
+
+def pin_recall_hand_made_sets(o):
+    """recall = |found intersect truth| / |truth|, each position once."""
+    assert o.recall(np.array([1, 2, 3, 4]), np.array([3, 4, 5, 6])) == 0.5
+    assert o.recall(np.array([3, 3, 3, 9]), np.array([3, 4])) == 0.5
+    assert o.recall(np.array([], dtype=np.int64), np.array([1, 2, 3])) == 0.0
+    assert o.recall(np.array([5, 6]), np.array([], dtype=np.int64)) == 1.0
+    assert o.recall(np.array([7, 1, 5]), np.array([1, 5, 7])) == 1.0
+    assert o.recall(np.array([2]), np.array([1, 2, 3, 4, 5])) == 0.2
+
+
 # --- attention and zones ---------------------------------------------------
 
 def pin_attention_dense(o):

@@ -54,7 +54,18 @@ MUTATIONS = [
      "order = np.lexsort((-cand, -est.astype(np.float64)))", P.pin_selection),
     ("top-k listed by position", "keep = order[:min(k, len(cand))]", "keep = np.sort(order[:min(k, len(cand))])",
      P.pin_selection),
-    ("attention unscaled", "s = K @ q / math.sqrt(q.shape[0])", "s = K @ q", P.pin_attention_dense),
+    ("top-k over positions that are not the candidates", "top_idx, top_est = topk(est, cand, k)",
+     "top_idx, top_est = topk(est, np.arange(c), k)", P.pin_pipeline_tiny_full_sort),
+    ("k_eff not capped by C", "C=c, k_eff=min(k, c)", "C=c, k_eff=k", P.pin_pipeline_tiny_full_sort),
+    ("rerank of the wrong rows", 'est = rerank_contract(enc["nib"][cand], enc["w"][cand]',
+     'est = rerank_contract(enc["nib"][:c], enc["w"][:c]', P.pin_pipeline_tiny_full_sort),
+    ("pipeline candidate count ignores k", "c = candidate_count(n, cand_bp, k)",
+     "c = candidate_count(n, cand_bp, 0)", P.pin_pipeline_tiny_full_sort),
+    ("recall over found", "return len(np.intersect1d(found, truth)) / len(truth)",
+     "return len(np.intersect1d(found, truth)) / max(1, len(found))", P.pin_recall_hand_made_sets),
+    ("recall counts duplicates", "return len(np.intersect1d(found, truth)) / len(truth)",
+     "return int(np.isin(found, truth).sum()) / len(truth)", P.pin_recall_hand_made_sets),
+    ("attention unscaled","s = K @ q / math.sqrt(q.shape[0])", "s = K @ q", P.pin_attention_dense),
     ("zone eviction off by one", "evict = max(0, self.n_local - self.L)", "evict = max(0, self.n_local - self.L - 1)",
      P.pin_zones),
     ("sink overwritten", "if p < self.S:\n            return (0, 0)", "if p < 0:\n            return (0, 0)", P.pin_zones),
