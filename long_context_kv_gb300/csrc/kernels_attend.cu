@@ -56,9 +56,13 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   trace_mark(tr, kTrAttend0);
   trace_block(a.trace, kTkAttend, 0);
 
-  // find row `row` of the split and copy half of its K and V.  Window rows
-  // (written by earlier appends) and q are copied before the wait; the
-  // retrieved rows need the top-k, written by the preceding kernel.
+  // find row `row` of the split and copy half of its K and V.  Everything
+  // is read after the wait: the preceding kernel may be a decode step that
+  // writes its own token into a window slot, or the retrieval that writes
+  // the top-k.
+  pdl_wait();
+  pdl_trigger();
+  trace_block(a.trace, kTkAttend, 1);
   const int64_t r = (int64_t)split * kAttnSplit + row;
   const __nv_bfloat16 *kp = nullptr, *vp = nullptr;
   const int c0 = half * (kDim / 2);
@@ -77,9 +81,6 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
     }
   }
   qf[tid] = load1(q, dtype, (int64_t)sq * kDim + tid) * qscale;
-  pdl_wait();
-  pdl_trigger();
-  trace_block(a.trace, kTkAttend, 1);
   if (r >= nwin && r < R) {
     const int64_t pos = __ldcg(a.topk_idx + (int64_t)sq * a.k + (r - nwin));
     if (pos >= a.s.sink && pos < a.s.sink + a.N) {
@@ -217,11 +218,9 @@ int attend_splits(const AttendArgs& a) {
 cudaError_t launch_attend(const void* q, int dtype, const AttendArgs& a, cudaStream_t st) {
   const int nsplit = attend_splits(a);
   if (nsplit > a.nsplit_max) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attend, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttendSmem);
+  {
+    const cudaError_t e = set_smem_limit((const void*)k_attend, (int)kAttendSmem, kSmemAttend);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int64_t nsink = min64(a.s.sink, a.T);
   const int64_t nwin = nsink + a.n_local_buf;

@@ -1556,12 +1556,10 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
     }
   }
   if (L.ord_idx != nullptr && (ra.k_eff > kOrderMax || ra.topk_score == nullptr)) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUBytes);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUBytes);
+  {
+    cudaError_t e = a.t.cent ? set_smem_limit((const void*)k_decode<true>, kUBytes, kSmemDecodeTable)
+                             : set_smem_limit((const void*)k_decode<false>, kUBytes, kSmemDecode);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, ra.s.batch * ra.s.hq);

@@ -439,11 +439,9 @@ cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shap
   while (n2 < tot) n2 <<= 1;
   const int64_t nwords = (N + 31) / 32;
   const size_t smem = (size_t)std::max<int64_t>(1, nwords <= kUnionWords ? nwords : n2) * sizeof(uint32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_union, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kUnionWords * 4));
+  {
+    const cudaError_t e = set_smem_limit((const void*)k_union, (int)(kUnionWords * 4), kSmemUnion);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_pdl(k_union, dim3(s.batch * s.hkv), dim3(kUnionThreads), smem, st, topk_idx, k, (int)k_eff, s, N,
                     list, n, stride, status);
@@ -481,11 +479,9 @@ cudaError_t launch_dense(const DenseArgs& a, int nsplit, cudaStream_t st) {
   static_assert((size_t)(3 * kDMaxHeads * kDMaxSplits + kDMaxHeads) * sizeof(float) <= kDenseSmem,
                 "the merge tables fit the stage area");
   if (a.s.g > kDMaxHeads || nsplit > kDMaxSplits) return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_dense, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDenseSmem);
+  {
+    const cudaError_t e = set_smem_limit((const void*)k_dense, (int)kDenseSmem, kSmemDense);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   return launch_pdl(k_dense, dim3(nsplit, a.s.batch * a.s.hkv), dim3(kDThreads), kDenseSmem, st, a);
 }

@@ -191,6 +191,28 @@ paris_status check_dtype(paris_ctx* c, int dtype) {
 
 }  // namespace
 
+namespace paris {
+
+namespace {
+constexpr int kSmemMaxDevices = 64;
+std::mutex g_smem_mu;
+bool g_smem_set[kSmemMaxDevices][kSmemKernelCount];
+}  // namespace
+
+cudaError_t set_smem_limit(const void* func, int bytes, SmemKernel which) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kSmemMaxDevices) return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  if (g_smem_set[dev][which]) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) g_smem_set[dev][which] = true;
+  return e;
+}
+
+}  // namespace paris
+
 namespace {
 
 RetrieveArgs retrieve_args(paris_ctx* c, int32_t* topk_idx, float* topk_score) {

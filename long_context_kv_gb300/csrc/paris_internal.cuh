@@ -139,6 +139,12 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
   return cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
 }
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to one device, so it is set once per
+// (device, kernel) pair; safe to call from several host threads.
+enum SmemKernel { kSmemDecode = 0, kSmemDecodeTable, kSmemAttend, kSmemDense, kSmemUnion, kSmemKernelCount };
+cudaError_t set_smem_limit(const void* func, int bytes, SmemKernel which);
+
 int decode_cluster_size(int nchunk_active);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st);
 cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_t st);

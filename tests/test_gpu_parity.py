@@ -227,3 +227,37 @@ def test_decode_step_equals_the_three_calls():
             qd2, idx, k_eff = g.check_retrieve(a, q)
             g.check_attention(a, qd2, idx, k_eff)
     assert a.ctx.paris_get_state()["n_flushes"] == b.ctx.paris_get_state()["n_flushes"] > 0
+
+
+def test_sparse_attend_right_after_a_decode_step_sees_its_token():
+    """paris_sparse_attend enqueued on the same stream directly behind
+    paris_decode_step (no host synchronisation between them) attends over
+    the step's own token as the decode step wrote it into the window: the
+    same rows, so the same output up to float32 order, and the oracle's."""
+    c = g.make_case(16 + 20000 + 64, seed=27, batch=1, n_kv_heads=2, n_q_heads=8, sink=16, local=64,
+                    update_buf=16, topk=64, cand_bp=500, rho=4)
+    shp = (1, 8, 64)
+    for t in range(40):
+        k = synth.decode_keys(27, 1, 2, t, 128, c.scale)
+        v = synth.decode_values(27, 1, 2, t, 128)
+        q = g.queries_from_zone(c, step=t)
+        kd, vd, qd = g.to_dev(k, torch.bfloat16), g.to_dev(v, torch.bfloat16), g.to_dev(q, torch.bfloat16)
+        idx = torch.empty(shp, dtype=torch.int32, device="cuda")
+        sc = torch.empty(shp, dtype=torch.float32, device="cuda")
+        o_step = torch.empty((1, 8, 128), dtype=torch.bfloat16, device="cuda")
+        o_call = torch.full((1, 8, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        k_eff = c.ctx.paris_decode_step(kd, vd, qd, idx, sc, o_step)
+        c.ctx.paris_sparse_attend(qd, idx, o_call)
+        torch.cuda.synchronize()
+        torch.testing.assert_close(o_call.float(), o_step.float(), rtol=0, atol=g.ATTN_ATOL)
+        g.append(c, k, v, device=False)
+        if t % 8 == 7:
+            out_h = o_call.float().cpu().numpy()
+            idx_h = idx.cpu().numpy()
+            Kb, Vb = g.as_seen(c.K, torch.bfloat16), g.as_seen(c.V, torch.bfloat16)
+            z = c.zones
+            for h in range(8):
+                rows = np.concatenate([z.sink(), z.local(), z.buffer(), idx_h[0, h, :k_eff]]).astype(np.int64)
+                ref = g.o.attention(qd[0, h].float().cpu().numpy(), Kb[0, h // 4, rows], Vb[0, h // 4, rows])
+                assert np.max(np.abs(out_h[0, h] - ref)) <= g.ATTN_ATOL, (t, h)
+    c.ctx.paris_check_device()

@@ -39,6 +39,35 @@ def test_noalloc_attention_matches_the_context_scratch_version_twice():
         assert k_eff == 256
 
 
+def test_noalloc_attention_across_contexts_of_different_shapes():
+    """Calls on two contexts of different shapes share the one area: a large
+    call right at its limit (16 query heads x 64 splits = 1024 rows) before
+    and after small calls of another shape.  Each must still equal
+    paris_sparse_attend (no stale merge counter, no row stride carried over)."""
+    big = g.make_case(16 + 5000 + 64, seed=33, n_kv_heads=4, n_q_heads=16, sink=16, local=64, update_buf=16,
+                      topk=4000, cand_bp=10000)
+    small = g.make_case(16 + 20000 + 64, seed=34, batch=2, n_kv_heads=2, n_q_heads=8, sink=16, local=64,
+                        update_buf=16, topk=256, cand_bp=500)
+
+    def compare(c, step):
+        b, hq = c.cfg["batch"], c.cfg["n_q_heads"]
+        q = g.queries_from_zone(c, step=step)
+        qd, idx, _, k_eff = g.run_retrieve(c, q)
+        ref = torch.zeros((b, hq, 128), dtype=torch.bfloat16, device="cuda")
+        got = torch.full((b, hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        c.ctx.paris_sparse_attend(qd, idx, ref)
+        c.ctx.paris_sparse_attend_noalloc(qd, idx, got)
+        torch.cuda.synchronize()
+        c.ctx.paris_check_device()
+        np.testing.assert_allclose(got.float().cpu().numpy(), ref.float().cpu().numpy(), rtol=0, atol=g.ATTN_ATOL)
+        return k_eff
+
+    assert compare(big, 0) == 4000  # (16 + 64 + 4000) rows -> 64 splits per head
+    assert compare(small, 0) == 256
+    assert compare(small, 1) == 256
+    assert compare(big, 1) == 4000
+
+
 def test_noalloc_attention_rejects_shapes_beyond_its_area():
     # 64 query heads x ceil((16 + 64 + 4096) / 64) = 66 splits = 4224 rows > 1024
     c = g.make_case(16 + 5000 + 64, seed=32, n_kv_heads=8, n_q_heads=64, sink=16, local=64, update_buf=16,
