@@ -225,7 +225,9 @@ def run_ours(args, rank, world):
     nl = args.layers or w["layers"]
     ctxlen, d = w["context"], w["head_dim"]
     b, hkv, hq, S = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["sink"]
-    per_layer_steps = (args.warmup + 8 * args.steps + 64 + nl - 1) // nl + 2
+    # inputs per layer: every timed and untimed step below, plus up to one
+    # Update Buffer's worth of steps to bring each layer to a flushing append
+    per_layer_steps = (args.warmup + 8 * args.steps + 64 + nl - 1) // nl + w["update_buf"] + 4
     max_ctx = ctxlen + per_layer_steps + 8
     fdt = torch.bfloat16 if args.workload != "tiny-4k" else torch.float32
     gen = torch.Generator(device="cuda")
@@ -270,11 +272,13 @@ def run_ours(args, rank, world):
     log(f"[rank {rank}] setup {time.time() - t_setup:.1f}s, {nl} layer contexts, "
         f"{torch.cuda.memory_allocated() / 2**30:.1f} GiB allocated by torch")
 
-    def step(i):
-        L = layers[i % nl]
+    def step_layer(L):
         j = L["step"]
         L["step"] = j + 1
         L["ctx"].paris_decode_step(L["kn"][j], L["vn"][j], L["qs"][j], L["idx"], L["sc"], L["out"])
+
+    def step(i):
+        step_layer(layers[i % nl])
 
     if args.profile_case:
         # the decode steps, then as many dense-attention calls on the same caches
@@ -398,6 +402,31 @@ def run_ours(args, rank, world):
     tokens_dense = sum(L["ctx"].paris_get_state()["T"] for L in layers) / nl
     ms_append = timed_calls(call_append)
 
+    # a decode step whose append fills the Update Buffer: the append, the
+    # flush (Local's oldest tokens join the Retrieval zone and the touched
+    # chunks' index is rebuilt), then retrieval and attention.  Each layer is
+    # first brought (eagerly, untimed) to the step before its next flush;
+    # then one flushing step per layer is captured and replayed (idempotent:
+    # the same token, the same rebuilt index, the same zones).
+    U = w["update_buf"]
+    for L in layers:
+        while L["ctx"].paris_get_state()["n_buf"] != U - 1:
+            step_layer(L)
+    torch.cuda.synchronize()
+    cs_f = torch.cuda.Stream()
+    g_flush = torch.cuda.CUDAGraph()
+    f0 = [L["ctx"].paris_launch_counts() for L in layers]
+    with torch.cuda.graph(g_flush, stream=cs_f):
+        for L in layers:
+            step_layer(L)
+    f1 = [L["ctx"].paris_launch_counts() for L in layers]
+    flush_launches = {k: sum(f1[li][k] - f0[li][k] for li in range(nl)) for k in f1[0]}
+    assert all(L["ctx"].paris_get_state()["n_buf"] == 0 for L in layers), "every captured step must flush"
+    g_flush.replay()
+    torch.cuda.synchronize()
+    ms_flush = timed(g_flush.replay) / nl
+    del g_flush
+
     # per-step device time distribution: events around each eager step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(64)]
     barrier()
@@ -449,10 +478,32 @@ def run_ours(args, rank, world):
     peak, peak_src = hbm_peak()
     roof = None
     if dom in alg:
-        ach = alg[dom] / (kernels[dom]["us_per_launch"] * 1e-6) / 1e9
+        # When every timed step is exactly one launch of the dominant kernel
+        # (no flush among them), its duration is the graph-replayed step time
+        # itself; otherwise the mean of the event-bracketed launches of the
+        # second capture (events add a little to each launch).
+        one_per_step = launches == args.steps and kernels[dom]["launches"] == args.steps
+        us_dom = 1e3 * ms / args.steps if one_per_step else kernels[dom]["us_per_launch"]
+        ach = alg[dom] / (us_dom * 1e-6) / 1e9
+        tr = traffic_record(dom, args)
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": traffic_record(dom, args),
+                "frac": round(ach / peak, 4), "peak_source": peak_src, "traffic": tr,
+                "traffic_source": "profiles/dram_traffic.txt (ncu capture of these kernel sources)" if tr else None,
+                "us_per_launch": us_dom,
+                "time_source": ("graph replay of the timed steps, one launch per step" if one_per_step else
+                                "CUDA events around each launch in a second captured replay"),
                 "algorithmic_bytes": alg[dom], "design_bytes": design[dom]}
+    # paris_retrieve alone (one decode-kernel launch per call, no attention):
+    # 16 B of ids per Retrieval key and (sequence, KV head), 128 B of codes
+    # and w per candidate and (sequence, query head), 8 B per top-k output
+    Nr = keys_retrieve / (b * hkv)
+    Cr = max((w["cand_bp"] * int(Nr) + 9999) // 10000, min(w["topk"], int(Nr)))
+    alg_r = b * hkv * 16 * Nr + b * hq * (Cr * 128 + min(w["topk"], Cr) * 8)
+    ach_r = alg_r / (ms_retrieve * 1e-3) / 1e9
+    roof_r = {"kernel": "decode (paris_retrieve: no attention)", "bound": "hbm", "achieved": round(ach_r, 1),
+              "peak": peak, "unit": "GB/s", "frac": round(ach_r / peak, 4), "peak_source": peak_src,
+              "us_per_launch": 1e3 * ms_retrieve, "time_source": "graph replay of K paris_retrieve calls",
+              "algorithmic_bytes": alg_r}
 
     # end to end through the public API with host buffers: each step's inputs
     # (q, k, v packed in one pinned buffer) go up in one copy, the step runs,
@@ -527,6 +578,9 @@ def run_ours(args, rank, world):
         "us_per_decode_step_eager_p10_p50_p90": [round(pct(0.1), 2), round(pct(0.5), 2), round(pct(0.9), 2)],
         "us_retrieve": 1e3 * ms_retrieve, "keys_per_s_retrieve": job_throughput(keys_retrieve, world, ms_retrieve),
         "us_sparse_attend": 1e3 * ms_attend, "us_append": 1e3 * ms_append,
+        # the step whose append flushes (once every update_buf steps per layer) and the mean step
+        "us_flush_step": 1e3 * ms_flush, "flush_step_launches": {k: v for k, v in flush_launches.items() if v},
+        "us_per_step_amortised": 1e3 * ((U - 1) * ms / args.steps + ms_flush) / U,
         # GQA-shared variant: the union of a KV head's query heads' top-k, each row read once per KV head
         "gqa_shared_attention": {
             "us_per_step": 1e3 * ms_gqa, "us_per_head_sparse_attention": 1e3 * ms_attend,
@@ -543,6 +597,7 @@ def run_ours(args, rank, world):
         "recall_at_k": recall,
         "kernels": kernels,
         "roofline": roof,
+        "roofline_retrieve": roof_r,
         "e2e": {"value": job_throughput(keys_e2e, world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
@@ -551,18 +606,181 @@ def run_ours(args, rank, world):
     return res
 
 
-def cpu_baseline(args):
-    """Time the oracle on the host cores in a fresh single-threaded process."""
+SWEEP_BP = (200, 500, 1000, 2000)
+SWEEP_RHO = (1, 2, 4, 8)
+SWEEP_K = (256, 512, 1024, 2048, 4096)
+
+
+def run_sweep(args):
+    """The 256K batch-5 sweep: candidate fraction x rho x k (80 points), one
+    JSON line per point with recall@k against the exact float64 top-k and the
+    decode-step and paris_retrieve times (graph replay over rotated layer
+    contexts, as the main benchmark).  Every point builds fresh contexts from
+    the same synthetic K/V."""
+    import torch
+
+    from long_context_kv_gb300 import build as B
+    from long_context_kv_gb300 import paris as P
+    from long_context_kv_gb300 import synth
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    B.build()
+    P.load()
+    w = dict(WORKLOADS["sweep-256k"])
+    nl = args.layers or 2
+    b, hkv, hq, d, S = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["sink"]
+    T = w["context"]
+    G = hq // hkv
+    steps = args.steps
+    per_layer = (args.warmup + 2 * steps + nl - 1) // nl + 2
+    gen = torch.Generator(device="cuda")
+    data = []
+    for li in range(nl):
+        seed = rank_seed(0, li)
+        scale = torch.from_numpy(synth.channel_scale(seed, hkv, d)).cuda()
+        gen.manual_seed(seed)
+        K = (torch.randn((b, hkv, T, d), generator=gen, device="cuda") * scale[None, :, None, :]).to(torch.bfloat16)
+        V = torch.randn((b, hkv, T, d), generator=gen, device="cuda").to(torch.bfloat16)
+        kn = (torch.randn((per_layer, b, hkv, d), generator=gen, device="cuda") * scale[None, None]).to(torch.bfloat16)
+        vn = torch.randn((per_layer, b, hkv, d), generator=gen, device="cuda").to(torch.bfloat16)
+        N0 = T - S - w["local"]
+        pos = torch.randint(S, S + N0, (per_layer + 4, b, hq), generator=gen, device="cuda")
+        kvh_of = torch.arange(hq, device="cuda") // G
+        picked = K[torch.arange(b, device="cuda")[None, :, None], kvh_of[None, None, :], pos].float()
+        qs = (picked + 0.5 * torch.randn(picked.shape, generator=gen, device="cuda")).to(torch.bfloat16).contiguous()
+        data.append(dict(K=K, V=V, kn=kn, vn=vn, qs=qs, seed=seed))
+        del picked
+    torch.cuda.synchronize()
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(torch.cuda.current_stream())
+        fn()
+        z.record(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return a.elapsed_time(z)
+
+    for bp in SWEEP_BP:
+        for rho in SWEEP_RHO:
+            for k in SWEEP_K:
+                layers = []
+                for li, dat in enumerate(data):
+                    cfg = P.make_config(batch=b, n_kv_heads=hkv, n_q_heads=hq, head_dim=d, n_sub=16, rho=rho, sink=S,
+                                        local=w["local"], update_buf=w["update_buf"], topk=k, cand_bp=bp,
+                                        max_ctx=T + per_layer + 8, retrieval_on_host=0)
+                    ctx = P.Context(cfg, synth.srht_signs(dat["seed"], d))
+                    ctx.paris_encode_prefill(dat["K"], dat["V"], T)
+                    layers.append(dict(ctx=ctx, dat=dat, step=0,
+                                       idx=torch.empty((b, hq, k), dtype=torch.int32, device="cuda"),
+                                       sc=torch.empty((b, hq, k), dtype=torch.float32, device="cuda"),
+                                       out=torch.empty((b, hq, d), dtype=torch.bfloat16, device="cuda")))
+
+                def one(i, retrieve_only=False):
+                    L = layers[i % nl]
+                    dat, j = L["dat"], L["step"]
+                    if retrieve_only:
+                        L["ctx"].paris_retrieve(dat["qs"][j], L["idx"], L["sc"])
+                        return
+                    L["step"] = j + 1
+                    L["ctx"].paris_decode_step(dat["kn"][j], dat["vn"][j], dat["qs"][j], L["idx"], L["sc"], L["out"])
+
+                for i in range(args.warmup):
+                    one(i)
+                res = {}
+                for name, ro in (("step", False), ("retrieve", True)):
+                    g = torch.cuda.CUDAGraph()
+                    cs = torch.cuda.Stream()
+                    with torch.cuda.graph(g, stream=cs):
+                        for i in range(steps):
+                            one(args.warmup + i, ro)
+                    g.replay()
+                    torch.cuda.synchronize()
+                    res[name] = 1e3 * timed(g.replay) / steps
+                    del g
+                # recall@k on layer 0 against the exact float64 top-k of <k, q>
+                L0 = layers[0]
+                st = L0["ctx"].paris_get_state()
+                N = int(st["N"])
+                rs = []
+                for t in range(2):
+                    q = L0["dat"]["qs"][per_layer + t]
+                    k_eff = L0["ctx"].paris_retrieve(q, L0["idx"], L0["sc"])
+                    for s_ in range(b):
+                        for kvh in range(hkv):
+                            Kz = L0["dat"]["K"][s_, kvh, S:S + N].double()
+                            ex_all = torch.topk(Kz @ q[s_, kvh * G:(kvh + 1) * G].double().T, k_eff, dim=0).indices
+                            for gi in range(G):
+                                got = L0["idx"][s_, kvh * G + gi, :k_eff].long()
+                                rs.append(torch.isin(got, ex_all[:, gi] + S).float().mean().item())
+                keys = b * hkv * N
+                print(json.dumps({"sweep_point": {"cand_pct": bp / 100, "rho": rho, "topk": k},
+                                  "recall_at_k": sum(rs) / len(rs), "us_per_decode_step": res["step"],
+                                  "us_retrieve": res["retrieve"], "keys_per_s_step": keys / (res["step"] * 1e-6),
+                                  "C": int(st["C"]), "k_eff": int(st["k_eff"]), "N": N,
+                                  "workload": DESCRIPTION["sweep-256k"], "layers_rotated": nl,
+                                  "timing": "graph replay, layers rotated"}), flush=True)
+                for L in layers:
+                    L["ctx"].close()
+                del layers
+                torch.cuda.synchronize()
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_process(args, procs: int):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", "--workload", args.workload,
            "--cand-bp", str(args.cand_bp), "--rho", str(args.rho), "--topk", str(args.topk),
-           "--steps", str(args.cpu_steps), "--warmup", str(args.warmup if args.impl == "reference" else 0)]
+           "--steps", str(args.cpu_steps), "--warmup", str(args.warmup if args.impl == "reference" else 0),
+           "--oracle-procs", str(procs)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         log(r.stderr[-2000:])
         return None
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(args):
+    """The oracle as it stands, timed on the host cores in fresh processes:
+    one process per core (each on its own KV head's decode steps, started
+    together), and once single-threaded.  No CUDA work in either."""
+    procs = max(1, min(host_cores(), args.oracle_procs_max))
+    many = _oracle_process(args, procs)
+    one = _oracle_process(args, 1) if procs > 1 else many
+    if many is None or one is None:
+        return None
+    res = dict(many)
+    res["cpu_model"] = cpu_model()
+    res["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1, "seconds": one["seconds"],
+                            "sample": one["sample"]}
+    return res
 
 
 def workload_of(args) -> dict:
@@ -575,9 +793,19 @@ def workload_of(args) -> dict:
     return w
 
 
-def oracle_sample(args):
-    """Decode steps of one KV head (its G query heads) of the workload, run
-    by the oracle as it stands; keys scanned = N per step."""
+def _bf16_values(x):
+    """float32 array -> the float32 values of its bf16 rounding (round to
+    nearest even; inputs are finite): what the library stores for K and V."""
+    import numpy as np
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def _oracle_setup(args, head: int, room: int):
+    """Prefill (untimed) of one KV head of the workload for the oracle: the
+    head's keys and values (bf16-valued where the workload is bf16) with
+    room for `room` decode tokens, its zones and its encoded Retrieval zone."""
     import numpy as np
 
     from long_context_kv_gb300 import synth
@@ -585,50 +813,106 @@ def oracle_sample(args):
 
     w = workload_of(args)
     d, S, L, U = w["head_dim"], w["sink"], w["local"], w["update_buf"]
-    G = w["n_q_heads"] // w["n_kv_heads"]
     T = w["context"]
     seed = 20260202 + 1
-    scale = synth.channel_scale(seed, 1, d)
-    K = synth.keys(seed, 1, 1, 0, T, d, scale)[0, 0]
-    V = synth.values(seed, 1, 1, 0, T, d)[0, 0]
+    scale = synth.channel_scale(seed, head + 1, d)  # row `head` is this head's scale
+    K = np.empty((T + room, d), dtype=np.float32)
+    V = np.empty((T + room, d), dtype=np.float32)
+    K[:T] = synth.key_rows(seed, 0, head, 0, T, d, scale)
+    V[:T] = synth.value_rows(seed, 0, head, 0, T, d)
     bf = args.workload != "tiny-4k"
     if bf:
-        import torch
-        K = torch.from_numpy(K).to(torch.bfloat16).float().numpy()
-        V = torch.from_numpy(V).to(torch.bfloat16).float().numpy()
+        K[:T] = _bf16_values(K[:T])
+        V[:T] = _bf16_values(V[:T])
     signs = synth.srht_signs(seed, d)
     lev, thr = o.rsq_levels_f32(8)
     z = o.Zones(S, L, U)
     z.prefill(T)
-    enc = o.encode_contract(K[S:], signs, 16, lev, thr)  # prefill (untimed)
-    rng = np.random.default_rng(seed)
-    steps = max(1, args.steps)
-    t0 = time.perf_counter()
+    enc = o.encode_contract(K[S:S + z.N], signs, 16, lev, thr)
+    return dict(w=w, K=K, V=V, z=z, enc=enc, signs=signs, lev=lev, thr=thr, scale=scale[head], bf=bf,
+                rng=np.random.default_rng(seed + 7919 * head))
+
+
+def _oracle_steps(st, n_steps: int) -> int:
+    """n_steps decode steps of one KV head (its G query heads): append the
+    step's token, then retrieval and sparse attention per query head.
+    Returns the Retrieval-zone keys scanned."""
+    import numpy as np
+
+    from oracle import pariskv as o
+
+    w, z, enc, rng, K, V = st["w"], st["z"], st["enc"], st["rng"], st["K"], st["V"]
+    d, S = w["head_dim"], w["sink"]
+    G = w["n_q_heads"] // w["n_kv_heads"]
     keys = 0
-    for s in range(args.warmup + steps):
-        if s == args.warmup:
-            t0 = time.perf_counter()
-            keys = 0
-        kn = (rng.standard_normal(d).astype(np.float32) * scale[0])
+    for _ in range(n_steps):
+        kn = rng.standard_normal(d).astype(np.float32) * st["scale"]
         vn = rng.standard_normal(d).astype(np.float32)
-        K = np.vstack([K, kn[None]])
-        V = np.vstack([V, vn[None]])
-        e1 = o.encode_contract(kn[None], signs, 16, lev, thr)
-        for key in enc:
-            enc[key] = np.concatenate([enc[key], e1[key]])
-        z.append()
+        t = z.T
+        K[t] = _bf16_values(kn) if st["bf"] else kn
+        V[t] = _bf16_values(vn) if st["bf"] else vn
+        lo, hi = z.append()
+        if hi > lo:  # a flush moved Local's oldest tokens into the Retrieval zone: encode them
+            e1 = o.encode_contract(K[lo:hi], st["signs"], 16, st["lev"], st["thr"])
+            for key in enc:
+                enc[key] = np.concatenate([enc[key], e1[key]])
         N = z.N
-        sub = {k: v[:N] for k, v in enc.items()}
-        for h in range(G):
+        for _h in range(G):
             q = K[S + rng.integers(0, N)] + 0.5 * rng.standard_normal(d).astype(np.float32)
-            r = o.retrieve_contract(sub, q.astype(np.float32), signs, 16, w["rho"], w["cand_bp"], w["topk"], lev)
+            r = o.retrieve_contract(enc, q.astype(np.float32), st["signs"], 16, w["rho"], w["cand_bp"], w["topk"],
+                                    st["lev"])
             rows = np.concatenate([z.sink(), z.local(), z.buffer(), S + r["top_idx"]])
             o.attention(q, K[rows], V[rows])
         keys += N
+    return keys
+
+
+def _oracle_worker(args, head, barrier, queue):
+    st = _oracle_setup(args, head, args.warmup + max(1, args.steps))
+    _oracle_steps(st, args.warmup)
+    barrier.wait()
+    t0 = time.perf_counter()
+    keys = _oracle_steps(st, max(1, args.steps))
+    queue.put((head, keys, time.perf_counter() - t0))
+
+
+def oracle_sample(args):
+    """Decode steps of the workload run by the oracle as it stands; keys
+    scanned = N per step and KV head.  With --oracle-procs P > 1, P processes
+    (spawned, one per core) each run their own KV head's steps, released
+    together by a barrier; the rate is all their keys over the wall time
+    from the barrier to the last one's end."""
+    steps = max(1, args.steps)
+    w = workload_of(args)
+    G = w["n_q_heads"] // w["n_kv_heads"]
+    P = max(1, args.oracle_procs)
+    if P == 1:
+        st = _oracle_setup(args, 0, args.warmup + steps)
+        _oracle_steps(st, args.warmup)
+        t0 = time.perf_counter()
+        keys = _oracle_steps(st, steps)
+        dt = time.perf_counter() - t0
+        print(json.dumps({"value": keys / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
+                          "sample": f"{steps} decode steps of 1 KV head ({G} query heads) of the "
+                                    f"{DESCRIPTION[args.workload]}, single thread"}))
+        return
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(P + 1)
+    queue = ctx.Queue()
+    ps = [ctx.Process(target=_oracle_worker, args=(args, h, barrier, queue)) for h in range(P)]
+    for p_ in ps:
+        p_.start()
+    barrier.wait(timeout=600)
+    t0 = time.perf_counter()
+    res = [queue.get(timeout=600) for _ in range(P)]
     dt = time.perf_counter() - t0
-    print(json.dumps({"value": keys / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "seconds": dt,
-                      "sample": f"{steps} decode steps of 1 KV head ({G} query heads) of the "
-                                f"{DESCRIPTION[args.workload]}, single thread"}))
+    for p_ in ps:
+        p_.join()
+    keys = sum(r[1] for r in res)
+    print(json.dumps({"value": keys / dt, "unit": UNIT, "cores": P, "kind": "oracle", "seconds": dt,
+                      "sample": f"{steps} decode steps of each of {P} KV heads ({G} query heads each) of the "
+                                f"{DESCRIPTION[args.workload]}, one process per core"}))
 
 
 def main():
@@ -647,11 +931,21 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=60)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-procs", dest="oracle_procs", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-procs-max", dest="oracle_procs_max", type=int, default=64,
+                    help="most processes of the multi-core oracle baseline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="with --workload sweep-256k: all 80 points (candidate fraction x rho x k), one JSON line each")
     ap.add_argument("--profile-case", action="store_true",
                     help="only set up the workload and run warmup + steps decode steps, untimed (for ncu)")
     args = ap.parse_args()
     if args.oracle_sample:
         oracle_sample(args)
+        return
+    if args.sweep:
+        if args.workload != "sweep-256k" or args.impl != "ours":
+            ap.error("--sweep runs the sweep-256k workload of our arm")
+        run_sweep(args)
         return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -669,7 +963,8 @@ def main():
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": run_config(args, world),
             "cpu_baseline": {"value": cb["value"], "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
-                             "sample": cb["sample"]},
+                             "sample": cb["sample"], "cpu_model": cb["cpu_model"],
+                             "single_thread": cb["single_thread"]},
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))
         return

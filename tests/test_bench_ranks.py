@@ -77,4 +77,6 @@ def test_reference_arm_line():
     assert line["impl"] == "reference"
     assert line["unit"] == "keys/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["cpu_model"]
+    assert line["cpu_baseline"]["single_thread"]["cores"] == 1 and line["cpu_baseline"]["single_thread"]["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0

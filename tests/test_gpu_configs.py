@@ -184,11 +184,15 @@ def test_one_million_tokens_retrieval_zone_in_host_memory():
     check(qs[1], idx, sc, out)
 
 
-SWEEP = [  # (candidates in basis points, rho, k)
+SWEEP = [  # (candidates in basis points, rho, k): the grid's corners and interior points
     (200, 1, 256),
+    (200, 8, 4096),
+    (2000, 1, 256),
+    (2000, 8, 4096),
     (500, 4, 1024),
     (1000, 2, 4096),
-    (2000, 8, 4096),
+    (500, 2, 512),
+    (1000, 4, 2048),
 ]
 
 

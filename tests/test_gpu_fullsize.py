@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 CFG = dict(batch=1, n_kv_heads=8, n_q_heads=32, sink=16, local=512, update_buf=128, topk=1024, cand_bp=500,
            rho=4)
 T0 = 131072
-SAMPLED = [(0, 0), (0, 13), (0, 31)]
+SAMPLED = [(0, 0), (0, 5), (0, 10), (0, 15), (0, 16), (0, 21), (0, 26), (0, 31)]  # one per KV head
 
 
 @pytest.fixture(scope="module", autouse=True)
