@@ -57,54 +57,65 @@ __global__ void __launch_bounds__(256) k_append(const void* __restrict__ k, cons
 // Inverted bucket index of one chunk of one (sequence, KV head): for every
 // subspace b, the chunk-local key numbers grouped by bucket id (a counting
 // sort; the order inside a bucket is not significant), with offsets
-// off[b][id] .. off[b][id + 1].  One block of 1024 threads per chunk.
-__global__ void __launch_bounds__(1024) k_build_index(int64_t N, int chunk0, Shape s, Tables t) {
-  __shared__ uint32_t cnt[kSub][kCentroids];
+// off[b][id] .. off[b][id + 1].  The subspaces are independent, so each
+// (chunk, sequence x KV head, subspace) is one block: it reads byte b of
+// every key's ids once (kept in registers), counts the buckets, scans the
+// counts and scatters the key numbers.
+constexpr int kIndexThreads = 512;
+constexpr int kIndexPer = kChunk / kIndexThreads;  // keys per thread
+static_assert(kIndexPer % 4 == 0, "ids packed four to a word");
+
+__global__ void __launch_bounds__(kIndexThreads) k_build_index(int64_t N, int chunk0, Shape s, Tables t) {
+  __shared__ uint32_t cnt[kCentroids];
   const int c = chunk0 + blockIdx.x;
   const int64_t sh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t base = (int64_t)c * kChunk;
   const int len = (int)min64(kChunk, N - base);
-  const uint4* ids = reinterpret_cast<const uint4*>(t.ids + (sh * t.rcap + base) * kSub);
-  uint32_t* off = t.off + ((sh * t.nchunk + c) * kSub) * kOffStride;
-  uint16_t* ent = t.ent + ((sh * t.nchunk + c) * kSub) * (int64_t)kChunk;
+  const uint8_t* ids = t.ids + (sh * t.rcap + base) * kSub + b;
+  uint32_t* off = t.off + ((sh * t.nchunk + c) * kSub + b) * kOffStride;
+  uint16_t* ent = t.ent + ((sh * t.nchunk + c) * kSub + b) * (int64_t)kChunk;
 
-  for (int i = threadIdx.x; i < kSub * kCentroids; i += blockDim.x) (&cnt[0][0])[i] = 0;
-  __syncthreads();
-  for (int key = threadIdx.x; key < len; key += blockDim.x) {
-    const uint4 r = ids[key];
-    const uint32_t wds[4] = {r.x, r.y, r.z, r.w};
+  for (int i = tid; i < kCentroids; i += kIndexThreads) cnt[i] = 0;
+  // key tid + kIndexThreads j; its id in byte j % 4 of word j / 4
+  uint32_t packed[kIndexPer / 4];
 #pragma unroll
-    for (int b = 0; b < kSub; ++b) atomicAdd(&cnt[b][(wds[b >> 2] >> (8 * (b & 3))) & 0xffu], 1u);
+  for (int j = 0; j < kIndexPer; ++j) {
+    const int key = tid + kIndexThreads * j;
+    const uint32_t id = key < len ? (uint32_t)__ldg(ids + (int64_t)key * kSub) : 0u;
+    if ((j & 3) == 0) packed[j >> 2] = 0;
+    packed[j >> 2] |= id << (8 * (j & 3));
   }
   __syncthreads();
-  // exclusive scan per subspace: warp b, 8 bins per lane
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp < kSub) {
-    const int b = warp;
+#pragma unroll
+  for (int j = 0; j < kIndexPer; ++j)
+    if (tid + kIndexThreads * j < len) atomicAdd(&cnt[(packed[j >> 2] >> (8 * (j & 3))) & 0xffu], 1u);
+  __syncthreads();
+  // exclusive scan of the 256 counts: warp 0, 8 bins per lane
+  if (warp == 0) {
     uint32_t vals[8], sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      vals[i] = cnt[b][8 * lane + i];
+      vals[i] = cnt[8 * lane + i];
       sum += vals[i];
     }
     uint32_t run = warp_incl_scan(sum, lane) - sum;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      off[b * kOffStride + 8 * lane + i] = run;
-      cnt[b][8 * lane + i] = run;
+      off[8 * lane + i] = run;
+      cnt[8 * lane + i] = run;
       run += vals[i];
     }
-    if (lane == 31) off[b * kOffStride + kCentroids] = run;
+    if (lane == 31) off[kCentroids] = run;
   }
   __syncthreads();
-  for (int key = threadIdx.x; key < len; key += blockDim.x) {
-    const uint4 r = ids[key];
-    const uint32_t wds[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int b = 0; b < kSub; ++b) {
-      const uint32_t id = (wds[b >> 2] >> (8 * (b & 3))) & 0xffu;
-      const uint32_t p = atomicAdd(&cnt[b][id], 1u);
-      ent[(int64_t)b * kChunk + p] = (uint16_t)key;
+  for (int j = 0; j < kIndexPer; ++j) {
+    const int key = tid + kIndexThreads * j;
+    if (key < len) {
+      const uint32_t p = atomicAdd(&cnt[(packed[j >> 2] >> (8 * (j & 3))) & 0xffu], 1u);
+      ent[p] = (uint16_t)key;
     }
   }
 }
@@ -138,8 +149,8 @@ cudaError_t launch_encode(const void* K, int dtype, int64_t T, int64_t pos0, int
 cudaError_t launch_build_index(int64_t N, int chunk0, int chunk1, const Shape& s, const Tables& t,
                                cudaStream_t st) {
   if (chunk1 <= chunk0) return cudaSuccess;
-  dim3 grid(chunk1 - chunk0, s.batch * s.hkv);
-  k_build_index<<<grid, 1024, 0, st>>>(N, chunk0, s, t);
+  dim3 grid(chunk1 - chunk0, s.batch * s.hkv, kSub);
+  k_build_index<<<grid, kIndexThreads, 0, st>>>(N, chunk0, s, t);
   return cudaGetLastError();
 }
 
