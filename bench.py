@@ -45,6 +45,10 @@ WORKLOADS = {
     # 1M-token context, Retrieval-zone K/V in pinned host memory read through UVA
     "1m-uva": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16, local=512,
                    update_buf=128, topk=2048, cand_bp=500, context=1048576, layers=2, retrieval_on_host=1),
+    # the 128K-token layer with its Retrieval-zone K/V in pinned host memory (UVA)
+    "llama8b-128k-uva": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16,
+                             local=512, update_buf=128, topk=1024, cand_bp=500, context=131072, layers=8,
+                             retrieval_on_host=1),
     # the same 1M-token context with the whole cache in HBM (it fits: ~4 GiB per layer of 280 GB)
     "1m-hbm": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16, local=512,
                    update_buf=128, topk=2048, cand_bp=500, context=1048576, layers=2, retrieval_on_host=0),
@@ -59,6 +63,7 @@ DESCRIPTION = {
     "qwen3-8b-drift": "Qwen3-8B-shaped long generation, batch 8, 32768-token prompt, drifting decode keys",
     "1m-uva": "1M-token context, Retrieval-zone K/V in pinned host memory (UVA)",
     "1m-hbm": "1M-token context, the whole cache in HBM",
+    "llama8b-128k-uva": "Llama-3.1-8B-shaped decode layer, 131072-token context, Retrieval-zone K/V in pinned host memory (UVA)",
     "sweep-256k": "256K-token context, batch 5 (one point of the candidate-fraction x rho x k sweep)",
 }
 
@@ -281,9 +286,13 @@ def run_ours(args, rank, world):
         step_layer(layers[i % nl])
 
     if args.profile_case:
-        # the decode steps, then as many dense-attention calls on the same caches
+        # the decode steps, then as many standalone sparse-attention calls
+        # (over each layer's last top-k) and dense-attention calls on the same caches
         for i in range(args.warmup + args.steps):
             step(i)
+        for i in range(args.warmup + args.steps):
+            L = layers[i % nl]
+            L["ctx"].paris_sparse_attend(L["qs"][0], L["idx"], L["out"])
         for i in range(args.warmup + args.steps):
             L = layers[i % nl]
             L["ctx"].paris_dense_attend(L["qs"][0], L["out"])

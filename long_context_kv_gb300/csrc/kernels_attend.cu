@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   __shared__ float fs[kMaxSplits];
   __shared__ float red[8];
   __shared__ int s_last;
+  __shared__ int64_t rsrc[kAttnSplit];  // element offset of each row (window rows flagged), -1: no row
   const int split = blockIdx.x;
   const int sq = blockIdx.y;
   const int seq = sq / a.s.hq, qh = sq - seq * a.s.hq, kvh = qh / a.s.g;
@@ -56,51 +57,51 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   trace_mark(tr, kTrAttend0);
   trace_block(a.trace, kTkAttend, 0);
 
-  // find row `row` of the split and copy half of its K and V.  Everything
-  // is read after the wait: the preceding kernel may be a decode step that
-  // writes its own token into a window slot, or the retrieval that writes
-  // the top-k.
+  // Everything is read after the wait: the preceding kernel may be a decode
+  // step that writes its own token into a window slot, or the retrieval that
+  // writes the top-k.  Thread r < kAttnSplit finds row r of the split; then
+  // 16 consecutive threads copy one row's 16-byte pieces, so every copy
+  // instruction covers whole rows (which keeps reads of host-resident rows
+  // in whole sectors).
   pdl_wait();
   pdl_trigger();
   trace_block(a.trace, kTkAttend, 1);
-  const int64_t r = (int64_t)split * kAttnSplit + row;
-  const __nv_bfloat16 *kp = nullptr, *vp = nullptr;
-  const int c0 = half * (kDim / 2);
-  if (r < nwin) {
-    int64_t slot = r;
-    if (r >= nsink) {
-      const int64_t pos = a.s.sink + a.N + (r - nsink);
-      slot = a.s.sink + (pos - a.s.sink) % ring;
+  constexpr int64_t kWin = int64_t(1) << 62;
+  if (tid < kAttnSplit) {
+    const int64_t r = (int64_t)split * kAttnSplit + tid;
+    int64_t src = -1;
+    if (r < nwin) {
+      int64_t slot = r;
+      if (r >= nsink) {
+        const int64_t pos = a.s.sink + a.N + (r - nsink);
+        slot = a.s.sink + (pos - a.s.sink) % ring;
+      }
+      src = kWin | ((sh * a.kv.win + slot) * kDim);
+    } else if (r < R) {
+      const int64_t pos = __ldcg(a.topk_idx + (int64_t)sq * a.k + (r - nwin));
+      if (pos >= a.s.sink && pos < a.s.sink + a.N) src = (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
+      else if (pos >= 0) atomicOr(a.status, kStatusBadIndex);
     }
-    kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
-    vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
-#pragma unroll
-    for (int j = 0; j < kDim / 16; ++j) {
-      cp_async16(ks + row * kKStride + c0 + 8 * j, kp + c0 + 8 * j);
-      cp_async16(vs + row * kDim + c0 + 8 * j, vp + c0 + 8 * j);
-    }
+    rsrc[tid] = src;
   }
   qf[tid] = load1(q, dtype, (int64_t)sq * kDim + tid) * qscale;
-  if (r >= nwin && r < R) {
-    const int64_t pos = __ldcg(a.topk_idx + (int64_t)sq * a.k + (r - nwin));
-    if (pos >= a.s.sink && pos < a.s.sink + a.N) {
-      kp = a.kv.st_k + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
-      vp = a.kv.st_v + (sh * a.kv.rcap + (pos - a.s.sink)) * kDim;
-#pragma unroll
-      for (int j = 0; j < kDim / 16; ++j) {
-        cp_async16(ks + row * kKStride + c0 + 8 * j, kp + c0 + 8 * j);
-        cp_async16(vs + row * kDim + c0 + 8 * j, vp + c0 + 8 * j);
-      }
-    } else if (pos >= 0 && half == 0) {
-      atomicOr(a.status, kStatusBadIndex);
+  __syncthreads();
+#pragma unroll 4
+  for (int i = tid; i < kAttnSplit * 16; i += kAttnThreads) {
+    const int rw = i >> 4, pc = i & 15;
+    const int64_t src = rsrc[rw];
+    if (src >= 0) {
+      const bool win = (src & kWin) != 0;
+      const int64_t e = (src & (kWin - 1)) + 8 * pc;
+      cp_async16(ks + rw * kKStride + 8 * pc, (win ? a.kv.win_k : a.kv.st_k) + e);
+      cp_async16(vs + rw * kDim + 8 * pc, (win ? a.kv.win_v : a.kv.st_v) + e);
+    } else {
+      // no row: zeros, so the weighted V sum below reads finite values
+      *reinterpret_cast<uint4*>(vs + rw * kDim + 8 * pc) = make_uint4(0, 0, 0, 0);
     }
   }
-  if (!kp) {
-    // no row: zeros, so the weighted V sum below reads finite values
-#pragma unroll
-    for (int j = 0; j < kDim / 16; ++j)
-      *reinterpret_cast<uint4*>(vs + row * kDim + c0 + 8 * j) = make_uint4(0, 0, 0, 0);
-  }
+  const bool has_row = rsrc[row] >= 0;
+  const int c0 = half * (kDim / 2);
   cp_async_wait_all();
   __syncthreads();
   trace_mark(tr, kTrAttend1);
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
       }
     }
     acc += __shfl_xor_sync(kFull, acc, 1);
-    if (kp) s = acc;
+    if (has_row) s = acc;
   }
   float mx = s;
 #pragma unroll
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   if (lane == 0) red[warp] = mx;
   __syncthreads();
   const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  const float pr = kp ? exp2f(s - M) : 0.f;
+  const float pr = has_row ? exp2f(s - M) : 0.f;
   if (half == 0) p[row] = pr;
   float l = half == 0 ? pr : 0.f;
 #pragma unroll
