@@ -76,9 +76,11 @@ def test_short_lists_and_a_null_score_array():
     assert torch.equal(idx, idx2)
 
 
-@pytest.mark.parametrize("k,T", [(5000, 30000), (16384, 20000)])
+@pytest.mark.parametrize("k,T", [(5000, 30000), (16384, 20000), (8000, 12000)])
 def test_long_lists(k, T):
     # every key a candidate (cand_bp = 10000): k_eff = min(k, N), sorted in one block
+    # (12000 tokens: every candidate's key fits the blocks' key tables, more than
+    # the counting sort takes)
     c = g.make_case(T, seed=84, batch=1, n_kv_heads=1, n_q_heads=2, sink=16, local=64, update_buf=32, topk=k,
                     cand_bp=10000)
     qd, idx, k_eff = g.check_retrieve(c, g.queries_from_zone(c), stages=False)
