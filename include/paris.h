@@ -204,9 +204,10 @@ paris_status paris_set_centroids(paris_ctx* ctx, const float* centroids, void* s
  * rows.  topk_idx: device int32 [batch][Hq][topk] as produced by
  * paris_retrieve (in either order; entries < 0 are skipped, entries
  * outside the Retrieval zone skipped and flagged).  q and out as in
- * paris_sparse_attend.  Same arithmetic as paris_dense_attend.  Limits: at
- * most 16 query heads per KV head and G x k_eff <= 32768, else PARIS_EINVAL.
- * Two launches (the union, then the attention); scratch from paris_create. */
+ * paris_sparse_attend.  Same arithmetic as paris_dense_attend.  Limit: at
+ * most 16 query heads per KV head, else PARIS_EINVAL.  One launch: each
+ * block builds the union over its own slice of the Retrieval zone and
+ * attends over it and its share of the window; scratch from paris_create. */
 paris_status paris_sparse_attend_gqa(paris_ctx* ctx, const void* q, paris_dtype dtype, const int32_t* topk_idx,
                                      void* out_bf16, void* stream);
 
@@ -293,7 +294,8 @@ typedef enum {
   PARIS_KERNEL_FILL = 6,        /* empty-result fill                                     */
   PARIS_KERNEL_DENSE = 7,       /* attention streaming rows once per KV head: the dense
                                    comparator, and the GQA-shared sparse attention      */
-  PARIS_KERNEL_UNION = 8,       /* union of a KV head's top-k lists (GQA-shared attention) */
+  PARIS_KERNEL_UNION = 8,       /* not launched: the GQA-shared attention builds its union
+                                   inside its PARIS_KERNEL_DENSE launch                 */
   PARIS_KERNEL_COUNT = 9
 } paris_kernel;
 

@@ -37,6 +37,7 @@ static_assert(kDTile * 16 == kDThreads * 8, "16-byte pieces: 8 per thread and ti
 constexpr int kDMaxSplits = 1024;  // splits per (sequence, KV head) the last block's merge tables hold
 
 constexpr size_t kDenseSmem = (size_t)2 * kDStages * kDTile * kDStride * sizeof(uint16_t);
+constexpr int kDUnionRows = 1792;  // union positions of a block kept in shared memory (the rest re-read)
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -96,24 +97,93 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   const int64_t sh = (int64_t)sh_i;
   const int G = a.s.g, qh0 = kvh * G;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t t0 = (int64_t)split * a.rows_per_split;
-  // rows of the (sequence, KV head): every token, or the window rows then the list
-  const int64_t total = a.list ? a.nwin + __ldcg(a.list_n + sh) : a.T;
-  const int64_t t1 = min64(total, t0 + a.rows_per_split);
+  const int ring = a.s.local + a.s.ubuf;
+  // Union mode: this block's share of the window rows, [w_lo, w_lo + nw),
+  // then the union of the G heads' top-k positions in its slice [z_lo, z_hi)
+  // of the Retrieval zone: every listed position sets its bit in a bitmap of
+  // the slice (in the stage area, before any tile), the set bits are read out
+  // in order (a block scan of the threads' bit counts places them) into
+  // ulist, nu of them, the first kDUnionRows also into shared memory.  Rows
+  // t < nw are window rows, the rest the union's positions.
+  __shared__ int32_t sul[kDUnionRows];
+  int64_t w_lo = 0, nw = 0, z_lo = 0;
+  int32_t* ul = nullptr;
+  int nu = 0;
+  if (a.topk != nullptr) {
+    const int J = gridDim.x;
+    w_lo = a.nwin * split / J;
+    nw = a.nwin * (split + 1) / J - w_lo;
+    z_lo = a.N * split / J;
+    const int64_t z_hi = a.N * (split + 1) / J;
+    const int nwords = (int)((z_hi - z_lo + 31) / 32);
+    uint32_t* bm = reinterpret_cast<uint32_t*>(dsm);
+    __shared__ uint32_t utmp[33];
+    for (int w = tid; w < nwords; w += kDThreads) bm[w] = 0u;
+    __syncthreads();
+    // the G lists' entries, eight loads in flight per thread
+    const int tot = G * (int)a.k_eff;
+    for (int e0 = tid; e0 < tot; e0 += 8 * kDThreads) {
+      int32_t pv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e = e0 + u * kDThreads;
+        pv[u] = -1;
+        if (e < tot) {
+          const int h = e / (int)a.k_eff, i = e - h * (int)a.k_eff;
+          pv[u] = __ldcg(a.topk + ((int64_t)seq * a.s.hq + qh0 + h) * a.k + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int32_t p = pv[u];
+        if (p >= a.s.sink && p < a.s.sink + a.N) {
+          const int64_t off = p - a.s.sink;
+          if (off >= z_lo && off < z_hi) atomicOr(&bm[(off - z_lo) >> 5], 1u << ((off - z_lo) & 31));
+        } else if (p >= 0) {
+          atomicOr(a.status, kStatusBadIndex);
+        }
+      }
+    }
+    __syncthreads();
+    const int per = (nwords + kDThreads - 1) / kDThreads;
+    const int w0 = min(nwords, tid * per), w1 = min(nwords, w0 + per);
+    uint32_t cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += (uint32_t)__popc(bm[w]);
+    uint32_t total;
+    uint32_t at = block_excl_scan(cnt, utmp, &total);
+    ul = a.ulist + sh * a.kv.rcap + z_lo;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t bits = bm[w];
+      while (bits) {
+        const int b = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int32_t p = (int32_t)(a.s.sink + z_lo + 32 * (int64_t)w + b);
+        if (at < (uint32_t)kDUnionRows) sul[at] = p;
+        else ul[at] = p;
+        ++at;
+      }
+    }
+    nu = (int)total;
+    __syncthreads();  // the bitmap's stage area is free, the list is written
+  }
+  // rows of the block: [t0, t1) of every token (a split of rows_per_split),
+  // or the block's window rows and union positions
+  const int64_t t0 = a.topk ? 0 : (int64_t)split * a.rows_per_split;
+  const int64_t t1 = a.topk ? nw + nu : min64(a.T, t0 + a.rows_per_split);
   const int nrows = (int)max64(0, t1 - t0);
   const int ntiles = (nrows + kDTile - 1) / kDTile;
-  const int ring = a.s.local + a.s.ubuf;
 
   // where row t's K/V is: the Sink slots and the Local/Buffer ring of the
   // window arrays, or the Retrieval-zone store.  Dense: row t is token t.
-  // List: rows below nwin are the window (Sink, then Local and Buffer in
-  // position order), the rest the listed Retrieval-zone tokens.
+  // Union mode: rows below nw are the window rows w_lo + t (Sink, then Local
+  // and Buffer in position order), the rest the union's positions.
   auto row_ptrs = [&](int64_t t, const __nv_bfloat16*& kp, const __nv_bfloat16*& vp) {
-    if (a.list) {
-      if (t < a.nwin) {
+    if (a.topk) {
+      if (t < nw) {
+        t += w_lo;
         t = t < a.nsink ? t : a.s.sink + a.N + (t - a.nsink);
       } else {
-        t = __ldcg(a.list + sh * a.list_stride + (t - a.nwin));
+        t = t - nw < kDUnionRows ? sul[t - nw] : __ldcg(ul + (t - nw));
       }
     }
     if (t < a.s.sink || t >= a.s.sink + a.N) {
@@ -354,98 +424,7 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   if (tid == 0) a.counter[blockIdx.y] = 0;
 }
 
-// The union of the G query heads' top-k lists of (sequence, KV head)
-// blockIdx.x, in ascending position, whatever order the lists are in.
-// While the Retrieval zone's bitmap fits shared memory (N <= 32 x
-// kUnionThreads x 32 tokens), every listed position sets its bit and the
-// set bits are read out in order (each thread owns a run of words; a block
-// scan of the runs' bit counts places them).  Otherwise the concatenated
-// lists are sorted (bitonic) and the first of each run of equal positions
-// kept.  Positions outside the Retrieval zone are dropped and flagged.
-constexpr int kUnionThreads = 1024;
-constexpr int64_t kUnionWords = 32 * kUnionThreads;  // shared-memory words: bitmap or sort keys
-__global__ void __launch_bounds__(kUnionThreads) k_union(const int32_t* __restrict__ topk_idx, int64_t k, int k_eff,
-                                                         Shape s, int64_t N, int32_t* list, int32_t* n,
-                                                         int64_t stride, uint32_t* status) {
-  extern __shared__ uint32_t ul[];  // the bitmap of the zone, or the G k_eff entries sorted
-  __shared__ uint32_t tmp[33];
-  const int sh = blockIdx.x, seq = sh / s.hkv, kvh = sh - seq * s.hkv;
-  const int G = s.g, tot = G * k_eff, tid = threadIdx.x;
-  const int64_t nwords = (N + 31) / 32;
-  auto entry = [&](int e) -> int32_t {
-    const int h = e / k_eff, i = e - h * k_eff;
-    const int32_t p = topk_idx[((int64_t)seq * s.hq + kvh * G + h) * k + i];
-    if (p >= s.sink && p < s.sink + N) return p;
-    if (p >= 0) atomicOr(status, kStatusBadIndex);
-    return -1;
-  };
-  pdl_wait();
-  if (nwords <= kUnionWords) {
-    for (int64_t w = tid; w < nwords; w += kUnionThreads) ul[w] = 0u;
-    __syncthreads();
-    for (int e = tid; e < tot; e += kUnionThreads) {
-      const int32_t p = entry(e);
-      if (p >= 0) atomicOr(&ul[(p - s.sink) >> 5], 1u << ((p - s.sink) & 31));
-    }
-    __syncthreads();
-    const int64_t per = (nwords + kUnionThreads - 1) / kUnionThreads;
-    const int64_t w0 = min64(nwords, tid * per), w1 = min64(nwords, w0 + per);
-    uint32_t cnt = 0;
-    for (int64_t w = w0; w < w1; ++w) cnt += (uint32_t)__popc(ul[w]);
-    uint32_t total;
-    uint32_t at = block_excl_scan(cnt, tmp, &total);
-    for (int64_t w = w0; w < w1; ++w) {
-      uint32_t bits = ul[w];
-      while (bits) {
-        const int b = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        list[(int64_t)sh * stride + at++] = (int32_t)(s.sink + w * 32 + b);
-      }
-    }
-    if (tid == 0) n[sh] = (int32_t)total;
-    return;
-  }
-  int n2 = 64;
-  while (n2 < tot) n2 <<= 1;
-  for (int e = tid; e < n2; e += kUnionThreads) {
-    uint32_t x = 0xffffffffu;  // skipped: padding and dropped entries
-    if (e < tot) {
-      const int32_t p = entry(e);
-      if (p >= 0) x = (uint32_t)p;
-    }
-    ul[e] = x;
-  }
-  block_sort_pow2(ul, n2);
-  // thread t owns entries [t per, t per + per): it keeps the first of each run
-  const int per = n2 / kUnionThreads > 0 ? n2 / kUnionThreads : 1;
-  const int e0 = min(n2, tid * per), e1 = min(n2, e0 + per);
-  uint32_t keep = 0;  // bit j: entry e0 + j is kept (per <= 32)
-  for (int e = e0; e < e1; ++e)
-    if (ul[e] != 0xffffffffu && (e == 0 || ul[e - 1] != ul[e])) keep |= 1u << (e - e0);
-  uint32_t total;
-  uint32_t at = block_excl_scan((uint32_t)__popc(keep), tmp, &total);
-  for (int e = e0; e < e1; ++e)
-    if ((keep >> (e - e0)) & 1u) list[(int64_t)sh * stride + at++] = (int32_t)ul[e];
-  if (tid == 0) n[sh] = (int32_t)total;
-}
-
 }  // namespace
-
-cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shape s, int64_t N, int32_t* list,
-                         int32_t* n, int64_t stride, uint32_t* status, cudaStream_t st) {
-  const int64_t tot = (int64_t)s.g * k_eff;
-  if (tot > 32 * kUnionThreads) return cudaErrorInvalidValue;
-  int64_t n2 = 64;
-  while (n2 < tot) n2 <<= 1;
-  const int64_t nwords = (N + 31) / 32;
-  const size_t smem = (size_t)std::max<int64_t>(1, nwords <= kUnionWords ? nwords : n2) * sizeof(uint32_t);
-  {
-    const cudaError_t e = set_smem_limit((const void*)k_union, (int)(kUnionWords * 4), kSmemUnion);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_pdl(k_union, dim3(s.batch * s.hkv), dim3(kUnionThreads), smem, st, topk_idx, k, (int)k_eff, s, N,
-                    list, n, stride, status);
-}
 
 int dense_splits(const DenseArgs& a, int sm_count) {
   // Splits per (sequence, KV head): the fewest that fill whole waves of one
@@ -468,6 +447,17 @@ int dense_splits(const DenseArgs& a, int sm_count) {
     if (eff > 0.999) break;
   }
   return (int)best;
+}
+
+int dense_union_splits(const DenseArgs& a, int sm_count) {
+  // rows per (sequence, KV head): the window and at most G k_eff positions;
+  // each slice's bitmap (zone bits / splits) must fit the stage area
+  DenseArgs r = a;
+  r.T = a.nwin + (int64_t)a.s.g * a.k_eff;
+  int n = dense_splits(r, sm_count);
+  const int64_t min_split = (a.N + (int64_t)kDenseSmem * 8 - 1) / ((int64_t)kDenseSmem * 8);
+  if (n < min_split) n = (int)min_split;
+  return n;
 }
 
 int64_t dense_rows_per_split(int64_t T, int nsplit) {

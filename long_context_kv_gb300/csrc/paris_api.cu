@@ -45,8 +45,7 @@ struct paris_ctx {
   uint32_t* counters;  // [2][batch*Hq]: rerank blocks, attention splits finished
   float* dense_part;   // dense comparator: [batch*Hq][dense_splits_max][kPartStride]
   uint32_t* dense_counter;  // [batch*Hkv]
-  int32_t* union_list;  // GQA-shared attention: [batch*Hkv][G*topk] union of the G top-k lists
-  int32_t* union_n;     // [batch*Hkv]
+  int32_t* gqa_list;    // GQA-shared attention: [batch*Hkv][rcap] the union of the G top-k lists, by zone slice
   float* cent_table;    // learned centroids [Hkv][16][256][8] (used when t.cent points to it)
   int32_t* ord_idx;     // top-k by score: the decode kernel's [batch*Hq][topk] positions, ascending
   float* ord_sc;        // and their estimates, before the order kernel lists them best first
@@ -159,7 +158,7 @@ void lloyd_max_levels(int m, double lev[8], double thr[7]) {
 void free_all(paris_ctx* c) {
   void* dev[] = {c->kv.win_k, c->kv.win_v, c->t.ids, c->t.rec, c->t.ent, c->t.off, c->qt, c->qnorm,
                  c->hot, c->votes, c->hist, c->cand_idx, c->cand_est, c->part, c->status,
-                 c->counters, c->trace, c->dense_part, c->dense_counter, c->union_list, c->union_n,
+                 c->counters, c->trace, c->dense_part, c->dense_counter, c->gqa_list,
                  c->cent_table, c->ord_idx, c->ord_sc};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -464,8 +463,7 @@ paris_status paris_create(const paris_config* cfg, const int8_t* srht_signs, par
   }
   TRY(dalloc(c, &c->dense_part, (size_t)bq * c->dense_splits_max * kPartStride * sizeof(float), "dense partials"));
   TRY(dalloc(c, &c->dense_counter, (size_t)bq * sizeof(uint32_t), "dense counters"));
-  TRY(dalloc(c, &c->union_list, (size_t)bq * f.topk * sizeof(int32_t), "top-k unions"));
-  TRY(dalloc(c, &c->union_n, (size_t)bh * sizeof(int32_t), "top-k union sizes"));
+  TRY(dalloc(c, &c->gqa_list, (size_t)bh * c->rcap * sizeof(int32_t), "top-k unions"));
   TRY(dalloc(c, &c->cent_table, (size_t)f.n_kv_heads * kTabPerHead * sizeof(float), "centroid table"));
   if (f.topk_order == PARIS_TOPK_BY_SCORE) {
     TRY(dalloc(c, &c->ord_idx, (size_t)bq * f.topk * sizeof(int32_t), "top-k positions before ordering"));
@@ -575,13 +573,7 @@ paris_status paris_sparse_attend_gqa(paris_ctx* c, const void* q, paris_dtype dt
   if (c->s.g > 16) return fail(c, PARIS_EINVAL, "paris_sparse_attend_gqa: at most 16 query heads per KV head");
   const int64_t k = c->cfg.topk;
   const int64_t k_eff = c->N > 0 ? std::min<int64_t>(k, candidate_count(c->N, c->cfg.cand_bp, k)) : 0;
-  if ((int64_t)c->s.g * k_eff > 32768)
-    return fail(c, PARIS_EINVAL, "paris_sparse_attend_gqa: query heads per KV head x k_eff must be at most 32768");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t stride = (int64_t)c->s.g * k;
-  PARIS_CUDA(c, launch(c, PARIS_KERNEL_UNION, s, [&] {
-    return launch_union(topk_idx, k, k_eff, c->s, c->N, c->union_list, c->union_n, stride, c->status, s);
-  }));
   DenseArgs a;
   a.s = c->s;
   a.kv = c->kv;
@@ -593,15 +585,18 @@ paris_status paris_sparse_attend_gqa(paris_ctx* c, const void* q, paris_dtype dt
   a.nsplit_max = c->dense_splits_max;
   a.counter = c->dense_counter;
   a.out = static_cast<__nv_bfloat16*>(out_bf16);
-  a.list = c->union_list;
-  a.list_n = c->union_n;
-  a.list_stride = stride;
+  a.topk = topk_idx;
+  a.k = k;
+  a.k_eff = k_eff;
+  a.ulist = c->gqa_list;
+  a.status = c->status;
   a.nsink = std::min<int64_t>(c->cfg.sink, c->T);
   a.nwin = a.nsink + c->n_local + c->n_buf;
-  a.T = a.nwin + (int64_t)c->s.g * k_eff;  // the most rows a (sequence, KV head) can have
-  int nsplit = dense_splits(a, c->sm_count);
-  a.rows_per_split = dense_rows_per_split(std::max<int64_t>(1, a.T), nsplit);
-  nsplit = (int)std::max<int64_t>(1, (a.T + a.rows_per_split - 1) / a.rows_per_split);
+  a.T = a.nwin + (int64_t)c->s.g * k_eff;
+  a.rows_per_split = 0;
+  const int nsplit = std::min(dense_union_splits(a, c->sm_count), c->dense_splits_max);
+  if ((a.N + nsplit - 1) / nsplit > (int64_t)8 * 200 * 1024)
+    return fail(c, PARIS_EINVAL, "paris_sparse_attend_gqa: Retrieval zone too long for %d splits", nsplit);
   PARIS_CUDA(c, launch(c, PARIS_KERNEL_DENSE, s, [&] { return launch_dense(a, nsplit, s); }));
   return PARIS_OK;
 }
@@ -638,9 +633,11 @@ paris_status paris_dense_attend(paris_ctx* c, const void* q, paris_dtype dtype, 
   a.nsplit_max = c->dense_splits_max;
   a.counter = c->dense_counter;
   a.out = static_cast<__nv_bfloat16*>(out_bf16);
-  a.list = nullptr;
-  a.list_n = nullptr;
-  a.list_stride = a.nsink = a.nwin = 0;
+  a.topk = nullptr;
+  a.k = a.k_eff = 0;
+  a.ulist = nullptr;
+  a.status = c->status;
+  a.nsink = a.nwin = 0;
   int nsplit = dense_splits(a, c->sm_count);
   a.rows_per_split = dense_rows_per_split(std::max<int64_t>(1, c->T), nsplit);
   nsplit = (int)std::max<int64_t>(1, (c->T + a.rows_per_split - 1) / a.rows_per_split);

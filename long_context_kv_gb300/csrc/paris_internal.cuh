@@ -142,7 +142,7 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device.  The attribute belongs to one device, so it is set once per
 // (device, kernel) pair; safe to call from several host threads.
-enum SmemKernel { kSmemDecode = 0, kSmemDecodeTable, kSmemAttend, kSmemDense, kSmemUnion, kSmemKernelCount };
+enum SmemKernel { kSmemDecode = 0, kSmemDecodeTable, kSmemAttend, kSmemDense, kSmemKernelCount };
 cudaError_t set_smem_limit(const void* func, int bytes, SmemKernel which);
 
 int decode_cluster_size(int nchunk_active);
@@ -179,17 +179,22 @@ struct DenseArgs {
   int nsplit_max;
   uint32_t* counter;          // [batch*Hkv] splits finished, reset by the last one
   __nv_bfloat16* out;
-  // list mode (GQA-shared sparse attention): the rows are the window (nsink
-  // Sink rows, then Local and Buffer) and then list[sh][0 .. list_n[sh]),
-  // Retrieval-zone positions; list == nullptr: every token
-  const int32_t* list;
-  const int32_t* list_n;
-  int64_t list_stride, nsink, nwin;
+  // union mode (GQA-shared sparse attention, topk != nullptr): block
+  // (split j of J, sequence x KV head) attends over its share of the window
+  // rows (nsink Sink rows, then Local and Buffer) and over the union of the
+  // G query heads' top-k positions (topk [batch][Hq][k], first k_eff of
+  // each) that fall in its slice of the Retrieval zone, which it builds
+  // itself and stores at ulist[sh][zone offset of the slice ...];
+  // topk == nullptr: every token
+  const int32_t* topk;
+  int64_t k, k_eff;
+  int32_t* ulist;      // [batch*Hkv][rcap]
+  uint32_t* status;
+  int64_t nsink, nwin;
 };
-// The union of the G query heads' top-k lists of every (sequence, KV head):
-// list[sh][0 .. n[sh]) in no particular order, each position once.
-cudaError_t launch_union(const int32_t* topk_idx, int64_t k, int64_t k_eff, Shape s, int64_t N, int32_t* list,
-                         int32_t* n, int64_t stride, uint32_t* status, cudaStream_t st);
+// Splits per (sequence, KV head) of the union mode: whole waves, and each
+// slice's bitmap of the Retrieval zone inside the stage area.
+int dense_union_splits(const DenseArgs& a, int sm_count);
 int dense_splits(const DenseArgs& a, int sm_count);  // splits per (sequence, KV head)
 
 // Top-k lists best first: at most kOrderMax entries per query head are
