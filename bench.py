@@ -35,6 +35,10 @@ WORKLOADS = {
     # through every layer (the whole model's decode-time retrieval and attention)
     "llama8b-128k-32l": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16,
                              local=512, update_buf=128, topk=1024, cand_bp=500, context=131072, layers=32),
+    # the 32 layers with each layer's Retrieval-zone K/V in pinned host memory (UVA, ~17 GB pinned in all)
+    "llama8b-128k-32l-uva": dict(batch=1, n_kv_heads=8, n_q_heads=32, head_dim=128, n_sub=16, rho=4, sink=16,
+                                 local=512, update_buf=128, topk=1024, cand_bp=500, context=131072, layers=32,
+                                 retrieval_on_host=1),
     # the small case the oracle finishes in seconds
     "tiny-4k": dict(batch=1, n_kv_heads=1, n_q_heads=1, head_dim=128, n_sub=16, rho=4, sink=0, local=0,
                     update_buf=128, topk=64, cand_bp=1000, context=4096, layers=64),
@@ -60,6 +64,8 @@ DESCRIPTION = {
     "llama8b-128k": "Llama-3.1-8B-shaped decode layer, 131072-token context",
     "tiny-4k": "one KV head, 4096 float32 keys",
     "llama8b-128k-32l": "Llama-3.1-8B-shaped decode, 32 layers of 131072-token context",
+    "llama8b-128k-32l-uva": "Llama-3.1-8B-shaped decode, 32 layers of 131072-token context, "
+                            "Retrieval-zone K/V in pinned host memory (UVA)",
     "qwen3-8b-drift": "Qwen3-8B-shaped long generation, batch 8, 32768-token prompt, drifting decode keys",
     "1m-uva": "1M-token context, Retrieval-zone K/V in pinned host memory (UVA)",
     "1m-hbm": "1M-token context, the whole cache in HBM",

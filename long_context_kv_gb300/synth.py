@@ -27,7 +27,7 @@ from __future__ import annotations
 import numpy as np
 
 # Stream ids keep the draws of one seed independent of each other.
-_S_SIGNS, _S_SCALE, _S_KEYS, _S_VALUES, _S_QPOS, _S_QNOISE, _S_DELTA, _S_DRIFT = range(8)
+_S_SIGNS, _S_SCALE, _S_KEYS, _S_VALUES, _S_QPOS, _S_QNOISE, _S_DELTA, _S_DRIFT, _S_QWALK = range(9)
 
 
 def _rng(seed: int, stream: int, *extra: int) -> np.random.Generator:
@@ -133,3 +133,12 @@ def queries_from_keys(seed: int, picked: np.ndarray, sigma: float = 0.5, step: i
     """q = picked key + N(0, sigma^2) noise.  picked: float32 [batch, Hq, d]."""
     noise = _rng(seed, _S_QNOISE, step).standard_normal(picked.shape, dtype=np.float32)
     return (picked + np.float32(sigma) * noise).astype(np.float32)
+
+
+def query_walk(seed: int, q: np.ndarray, corr: float, step: int) -> np.ndarray:
+    """The next decode step's queries as a correlated walk from q (float32
+    [..., d]): corr * q + sqrt(1 - corr^2) * n, with n Gaussian and each row of
+    n scaled to the norm of q's row, so that cos(q, q_next) is close to corr."""
+    n = _rng(seed, _S_QWALK, step).standard_normal(q.shape, dtype=np.float32)
+    n *= np.linalg.norm(q, axis=-1, keepdims=True) / np.linalg.norm(n, axis=-1, keepdims=True)
+    return (np.float32(corr) * q + np.float32(np.sqrt(1.0 - corr * corr)) * n).astype(np.float32)

@@ -36,3 +36,15 @@ def test_streams_are_distinct_and_seeded():
     m2 = synth.drift_offset(7, 2, 128, sc, 512)
     np.testing.assert_allclose(m2, 2 * m1, rtol=1e-6)
     np.testing.assert_allclose(np.abs(m1), 0.02 * sc, rtol=1e-6)
+
+
+def test_query_walk_keeps_the_norm_and_sets_the_cosine():
+    q = synth.queries_from_keys(3, synth.keys(3, 2, 4, 0, 1, 128, synth.channel_scale(3, 4, 128))[:, :, 0], 0.5, 0)
+    assert np.array_equal(synth.query_walk(3, q, 1.0, 5), q)
+    for corr in (0.0, 0.5, 0.9, 0.99):
+        nxt = synth.query_walk(3, q, corr, 5)
+        cos = np.sum(nxt * q, -1) / (np.linalg.norm(nxt, axis=-1) * np.linalg.norm(q, axis=-1))
+        # the noise has q's norm and is nearly orthogonal to it in 128 dimensions
+        assert np.all(np.abs(cos - corr) < 0.3 * np.sqrt(1 - corr * corr) + 1e-6)
+        np.testing.assert_allclose(np.linalg.norm(nxt, axis=-1), np.linalg.norm(q, axis=-1), rtol=0.3)
+    assert not np.array_equal(synth.query_walk(3, q, 0.5, 5), synth.query_walk(3, q, 0.5, 6))
