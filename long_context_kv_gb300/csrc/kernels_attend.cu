@@ -24,7 +24,13 @@ namespace paris {
 namespace {
 
 constexpr int kAttnThreads = 128;
-constexpr int kKStride = kDim + 8;  // bf16 elements per staged K row: 272 B keeps 16-byte reads conflict-free
+// A staged K row is 256 B with its 16-byte pieces permuted by row (piece c
+// of row r at c ^ (r & 7)): every 32-byte sector lands whole in an aligned
+// 32-byte slot, so each copy instruction is served as whole-sector requests
+// (a row stride padded to 272 B splits the sectors of every other row, which
+// doubles the requests and cut reads of host-resident rows to about 60 % of
+// the link's rate), and the 16-byte reads of the scores meet no bank conflict.
+__device__ __forceinline__ int kpiece(int row, int c) { return row * kDim + 8 * (c ^ (row & 7)); }
 static_assert(kAttnThreads == kDim && 2 * kAttnSplit == kAttnThreads, "one thread per output dimension, two per row");
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -36,9 +42,13 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict__ q, int dtype, AttendArgs a,
                                                         int64_t nsink, int64_t nwin, int nsplit, float qscale) {
-  extern __shared__ __align__(16) uint16_t smem[];
-  uint16_t* ks = smem;                          // [kAttnSplit][kKStride]
-  uint16_t* vs = smem + kAttnSplit * kKStride;  // [kAttnSplit][kDim]
+  // The dynamic region follows the static arrays below; 128-byte alignment
+  // keeps every staged row's 32-byte sectors on sector boundaries (at the
+  // default 16-byte alignment it started 16 bytes off one, and every row read
+  // from host memory cost twice its sectors).
+  extern __shared__ __align__(128) uint16_t smem[];
+  uint16_t* ks = smem;                      // [kAttnSplit][kDim], pieces permuted (kpiece)
+  uint16_t* vs = smem + kAttnSplit * kDim;  // [kAttnSplit][kDim]
   __shared__ float qf[kDim];
   __shared__ float p[kAttnSplit];
   __shared__ float fs[kMaxSplits];
@@ -93,7 +103,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
     if (src >= 0) {
       const bool win = (src & kWin) != 0;
       const int64_t e = (src & (kWin - 1)) + 8 * pc;
-      cp_async16(ks + rw * kKStride + 8 * pc, (win ? a.kv.win_k : a.kv.st_k) + e);
+      cp_async16(ks + kpiece(rw, pc), (win ? a.kv.win_k : a.kv.st_k) + e);
       cp_async16(vs + rw * kDim + 8 * pc, (win ? a.kv.win_v : a.kv.st_v) + e);
     } else {
       // no row: zeros, so the weighted V sum below reads finite values
@@ -106,18 +116,21 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   __syncthreads();
   trace_mark(tr, kTrAttend1);
 
-  // score of the row (log2 domain): each thread half the dot product
+  // score of the row (log2 domain): each thread half the dot product; the
+  // second half takes its pieces starting four pieces on, so the two
+  // threads of a row read different banks
   float s = -FLT_MAX;
   {
     float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < kDim / 16; ++j) {
-      const uint4 kv8 = *reinterpret_cast<const uint4*>(ks + row * kKStride + c0 + 8 * j);
+      const int c = c0 / 8 + (j ^ (4 * half));
+      const uint4 kv8 = *reinterpret_cast<const uint4*>(ks + kpiece(row, c));
       const uint32_t w[4] = {kv8.x, kv8.y, kv8.z, kv8.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        acc += qf[c0 + 8 * j + 2 * i] * bf16_bits_to_float(w[i] & 0xffffu);
-        acc += qf[c0 + 8 * j + 2 * i + 1] * bf16_bits_to_float(w[i] >> 16);
+        acc += qf[8 * c + 2 * i] * bf16_bits_to_float(w[i] & 0xffffu);
+        acc += qf[8 * c + 2 * i + 1] * bf16_bits_to_float(w[i] >> 16);
       }
     }
     acc += __shfl_xor_sync(kFull, acc, 1);
@@ -205,7 +218,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   trace_block(a.trace, kTkAttend, 3);
 }
 
-constexpr size_t kAttendSmem = (size_t)kAttnSplit * (kKStride + kDim) * sizeof(uint16_t);
+constexpr size_t kAttendSmem = (size_t)kAttnSplit * 2 * kDim * sizeof(uint16_t);
 
 }  // namespace
 

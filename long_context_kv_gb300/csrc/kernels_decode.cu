@@ -47,7 +47,6 @@ constexpr int kVoteSlots = 2;       // chunks per block whose votes stay in shar
 constexpr int kListCap = 4096;      // candidates of the block's slice kept in shared memory
 constexpr int kTile = 64;           // attention rows per pipeline stage
 constexpr int kStages = 4;
-constexpr int kKStride = kDim + 8;  // bf16 per staged row: 272 B keeps 16-byte reads conflict-free
 constexpr int kSelCap = 12288;      // candidates whose order keys every block of the cluster holds
 constexpr int kSelBins = 2048;      // 11-bit radix digits
 constexpr int kBinRank = 64;        // keys left in the k-th digit that are ranked directly
@@ -66,10 +65,10 @@ constexpr int kUWarpHist = kUOffs + kVoteSlots * kSub * kOffStride * 4;  // u32 
 constexpr int kUHot = kUWarpHist + kWarps * kWarpBins * 4;    // hot lists: hv[nhot], then per list
                                                               // (G x nhot) hbeg, hwt, hpre (+1), hsm
 constexpr int kURecSlots = 0;                                 // 128 B per thread: a candidate record being gathered
-constexpr int kUStageK = 0;                                   // bf16 [kStages][kTile][kKStride]
-constexpr int kUStageV = kStages * kTile * kKStride * 2;
-constexpr int kUAttnEnd = 2 * kStages * kTile * kKStride * 2;
-constexpr int kUSelHist = kUStageK + kStages / 2 * kTile * kKStride * 2;  // u32 [kSelBins], then u32 [kBinRank]:
+constexpr int kUStageK = 0;                                   // bf16 [kStages][kTile][kDim], pieces permuted (spiece)
+constexpr int kUStageV = kStages * kTile * kDim * 2;
+constexpr int kUAttnEnd = 2 * kStages * kTile * kDim * 2;
+constexpr int kUSelHist = kUStageK + kStages / 2 * kTile * kDim * 2;  // u32 [kSelBins], then u32 [kBinRank]:
                                                               // in the K rows of the second attention round
 constexpr int kUSelPos = kUSelHist + (kSelBins + kBinRank) * 4;  // i32 [kListCap]: positions the block's slice takes
 constexpr int kUKeys = kUAttnEnd;                             // u32 [kSelCap]: order keys of all C estimates,
@@ -124,6 +123,13 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
 }
+
+// A staged K or V row is 256 B with its 16-byte pieces permuted by row
+// (piece c of row r at c ^ (r & 7)): every 32-byte sector lands whole in an
+// aligned 32-byte slot, so a copy instruction is served as whole-sector
+// requests (a row stride padded to 272 B splits the sectors of every other
+// row and doubles the requests), and the reads below meet no bank conflict.
+__device__ __forceinline__ int spiece(int row, int c) { return row * kDim + 8 * (c ^ (row & 7)); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
@@ -547,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ float s_qn;
   __shared__ int s_T;
   __shared__ int64_t s_quota;
-  extern __shared__ __align__(16) uint8_t U[];
+  extern __shared__ __align__(128) uint8_t U[];  // 128-byte aligned: staged rows keep whole sectors
 
   const int nhot = kSub * a.rho;
   const int nlist = (nhot <= 1024 ? kVoteSlots : 1) * nhot;  // hot lists of a group of chunks
@@ -1300,8 +1306,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int rr = (tid >> 4) + 64 * u, ch = tid & 15;  // round row, 16-byte piece
-        uint16_t* kd = stK + (half * kRound + rr) * kKStride + 8 * ch;
-        uint16_t* vd = stV + (half * kRound + rr) * kKStride + 8 * ch;
+        const int so = (half * kRound + rr) * kDim + 8 * (ch ^ ((tid >> 4) & 7));  // spiece: rr & 7 = (tid >> 4) & 7
+        uint16_t* kd = stK + so;
+        uint16_t* vd = stV + so;
         const int rl = rd * kRound + rr;
         int64_t src = -1;
         if (rd < nrounds && rl < nrows) src = rl < kRowTab ? rsrc[rl] : row_source(rl);
@@ -1324,22 +1331,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     trace_mark(tr, kTrDecodeRound - 1);
     issue(0);
     issue(1);
-    const int hrow = 4 * warp + (lane >> 3), oct = lane & 7;  // scored row of the round, eighth of it
+    // scored row of the round; the lane takes pieces oct and oct + 8 of it
+    const int hrow = 4 * warp + (lane >> 3), oct = lane & 7;
+    const int kofs = spiece(hrow, oct);                                    // piece oct + 8 is 64 elements on
+    const int vofs = 8 * ((lane >> 1) ^ (4 * (warp & 1))) + 4 * (lane & 1);  // row 4 warp + i: vofs ^ 8 i
     float qv[16];  // the lane's 16 dimensions of the scaled q, loaded once
 #pragma unroll
-    for (int i = 0; i < 16; ++i) qv[i] = zs[16 * oct + i];
+    for (int i = 0; i < 16; ++i) qv[i] = zs[64 * (i >> 3) + 8 * oct + (i & 7)];
     float M = -FLT_MAX, l = 0.f, o4[4] = {0.f, 0.f, 0.f, 0.f};
     for (int rd = 0; rd < nrounds; ++rd) {
       const int half = rd & 1;
       cp_async_wait_group<1>();  // all but the newest group: round rd has landed
       __syncthreads();
       if (rd < 8) trace_mark(tr, kTrDecodeRound + 2 * rd);
-      const uint16_t* kh = stK + half * kRound * kKStride;
-      const uint16_t* vh = stV + half * kRound * kKStride;
+      const uint16_t* kh = stK + half * kRound * kDim;
+      const uint16_t* vh = stV + half * kRound * kDim;
       float s = 0.f;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const uint4 kv8 = *reinterpret_cast<const uint4*>(kh + hrow * kKStride + 16 * oct + 8 * u);
+        const uint4 kv8 = *reinterpret_cast<const uint4*>(kh + kofs + 64 * u);
         const float* q8 = qv + 8 * u;
         s += q8[0] * bf16_bits_to_float(kv8.x & 0xffffu) + q8[1] * __uint_as_float(kv8.x & 0xffff0000u);
         s += q8[2] * bf16_bits_to_float(kv8.y & 0xffffu) + q8[3] * __uint_as_float(kv8.y & 0xffff0000u);
@@ -1365,7 +1375,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float p = __shfl_sync(kFull, pm, 8 * i);
-        const uint2 v = *reinterpret_cast<const uint2*>(vh + (4 * warp + i) * kKStride + 4 * lane);
+        const uint2 v = *reinterpret_cast<const uint2*>(vh + (4 * warp + i) * kDim + (vofs ^ (8 * i)));
         o4[0] += p * bf16_bits_to_float(v.x & 0xffffu);
         o4[1] += p * __uint_as_float(v.x & 0xffff0000u);
         o4[2] += p * bf16_bits_to_float(v.y & 0xffffu);

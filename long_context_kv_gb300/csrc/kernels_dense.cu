@@ -31,18 +31,28 @@ constexpr int kDWarps = kDThreads / 32;
 constexpr int kDRowsW = 16;                // rows per warp and tile: one 16-deep k step of P V
 constexpr int kDTile = kDRowsW * kDWarps;  // 128 rows per tile
 constexpr int kDStages = 3;
-constexpr int kDStride = kDim + 8;         // bf16 per staged row: 272 B, conflict-free 8-row matrix loads
+constexpr int kDStride = kDim + 8;         // bf16 per row of the staged query: 272 B, conflict-free matrix loads
 constexpr int kDMaxHeads = 16;             // query heads per block: the rows of one mma tile
 static_assert(kDTile * 16 == kDThreads * 8, "16-byte pieces: 8 per thread and tile for K, 8 for V");
 constexpr int kDMaxSplits = 1024;  // splits per (sequence, KV head) the last block's merge tables hold
 
-constexpr size_t kDenseSmem = (size_t)2 * kDStages * kDTile * kDStride * sizeof(uint16_t);
+constexpr size_t kDStageBytes = (size_t)2 * kDStages * kDTile * kDim * sizeof(uint16_t);
+constexpr size_t kDMergeBytes = (size_t)(3 * kDMaxHeads * kDMaxSplits + kDMaxHeads) * sizeof(float);
+constexpr size_t kDenseSmem = kDStageBytes > kDMergeBytes ? kDStageBytes : kDMergeBytes;
 constexpr int kDUnionRows = 1792;  // union positions of a block kept in shared memory (the rest re-read)
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
 }
+
+// A staged K or V row is 256 B with its 16-byte pieces permuted by row
+// (piece c of row r at c ^ (r & 7)): every 32-byte sector lands whole in an
+// aligned 32-byte slot, so a copy instruction is served as whole-sector
+// requests (a row stride padded to 272 B splits the sectors of every other
+// row, doubling the requests: host-resident rows then stream at about 60 %
+// of the link's rate), and each 8-row matrix load touches all 32 banks once.
+__device__ __forceinline__ int dpiece(int row, int c) { return row * kDim + 8 * (c ^ (row & 7)); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
@@ -82,9 +92,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // dimensions).  Fragment layouts are those of mma.m16n8k16: lane l holds
 // rows l / 4 and l / 4 + 8 and columns 2 (l % 4), 2 (l % 4) + 1.
 __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
-  extern __shared__ __align__(16) uint16_t dsm[];
-  uint16_t* stK = dsm;                                // [kDStages][kDTile][kDStride]
-  uint16_t* stV = dsm + kDStages * kDTile * kDStride;
+  // The dynamic region follows the static arrays; 128-byte alignment keeps
+  // every staged row's 32-byte sectors on sector boundaries (at the default
+  // 16-byte alignment it started 16 bytes off one, behind 17.5 KB of static
+  // arrays, and every row read from host memory cost twice its sectors).
+  extern __shared__ __align__(128) uint16_t dsm[];
+  uint16_t* stK = dsm;                             // [kDStages][kDTile][kDim], pieces permuted (dpiece)
+  uint16_t* stV = dsm + kDStages * kDTile * kDim;
   __shared__ __align__(16) uint16_t qsh[2][kDMaxHeads][kDStride];  // the query as bf16 hi + lo
   __shared__ float wml[kDWarps][kDMaxHeads][2];
   __shared__ float fs[kDMaxHeads][kDWarps];
@@ -204,8 +218,8 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
       for (int j = 0; j < kDTile * 16 / kDThreads; ++j) {
         const int rr = (tid >> 4) + 16 * j;
         const int64_t t = t0 + (int64_t)i * kDTile + rr;
-        uint16_t* kd = stK + (st * kDTile + rr) * kDStride + 8 * ch;
-        uint16_t* vd = stV + (st * kDTile + rr) * kDStride + 8 * ch;
+        uint16_t* kd = stK + dpiece(st * kDTile + rr, ch);
+        uint16_t* vd = stV + dpiece(st * kDTile + rr, ch);
         if (t < t1) {
           const __nv_bfloat16 *kp, *vp;
           row_ptrs(t, kp, vp);
@@ -254,8 +268,8 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
     __syncthreads();                      // ... for every thread; stage (i - 1) % kDStages is free
     issue(i + kDStages - 1);
     const int st = i % kDStages;
-    const uint16_t* kt = stK + (st * kDTile + kDRowsW * warp) * kDStride;
-    const uint16_t* vt = stV + (st * kDTile + kDRowsW * warp) * kDStride;
+    const uint16_t* kt = stK + (st * kDTile + kDRowsW * warp) * kDim;  // 16 rows: the permutation restarts
+    const uint16_t* vt = stV + (st * kDTile + kDRowsW * warp) * kDim;
     // S = Q K^T for the warp's 16 rows: n-tile r holds rows 8 r .. 8 r + 7
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -264,7 +278,7 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
       for (int k2 = 0; k2 < kDim / 32; ++k2) {
         // matrices: rows 8 r .. 8 r + 7, dims 32 k2 + 8 m .. + 7
         uint32_t b[4];
-        ldsm_x4(b, kt + (8 * r + (lane & 7)) * kDStride + 32 * k2 + 8 * (lane >> 3));
+        ldsm_x4(b, kt + dpiece(8 * r + (lane & 7), 4 * k2 + (lane >> 3)));
         mma16816(s[r], qa[0][2 * k2], b[0], b[1]);
         mma16816(s[r], qa[1][2 * k2], b[0], b[1]);
         mma16816(s[r], qa[0][2 * k2 + 1], b[2], b[3]);
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
     for (int n2 = 0; n2 < kDim / 16; ++n2) {
       // matrices: rows 0-7 / 8-15 of the warp's rows, dims 16 n2 .. + 7 / + 8 .. + 15
       uint32_t b[4];
-      ldsm_x4_t(b, vt + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kDStride + 16 * n2 + 8 * (lane >> 4));
+      ldsm_x4_t(b, vt + dpiece((lane & 7) + 8 * ((lane >> 3) & 1), 2 * n2 + (lane >> 4)));
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         float* on = o[2 * n2 + h2];
