@@ -71,6 +71,7 @@ constexpr int kUAttnEnd = 2 * kStages * kTile * kDim * 2;
 constexpr int kUSelHist = kUStageK + kStages / 2 * kTile * kDim * 2;  // u32 [kSelBins], then u32 [kBinRank]:
                                                               // in the K rows of the second attention round
 constexpr int kUSelPos = kUSelHist + (kSelBins + kBinRank) * 4;  // i32 [kListCap]: positions the block's slice takes
+constexpr int kUBucket = kUSelPos + kListCap * 4;             // u16 [kSelCap]: every key's index, by bin
 constexpr int kUKeys = kUAttnEnd;                             // u32 [kSelCap]: order keys of all C estimates,
                                                               // then i64 [kRowTab]: attention row sources
 constexpr int kUListPos = kUKeys + kSelCap * 4;               // i32 [kListCap]: the block's rerank slice
@@ -79,6 +80,7 @@ static_assert(kUHot + (5 * kSub * kCentroids + 1) * 4 + 16 <= kUBytes, "hot list
 static_assert(kUWarpHist + kWarps * kWarpBins * 4 <= kUHot, "per-warp vote counts before the hot lists");
 static_assert(kUHot + (9 * 1024 + 1) * 4 + 16 <= kUBytes, "hot lists (G = 2) inside the region");
 static_assert(kUSelPos + kListCap * 4 <= kUStageV, "top-k tables inside the second round's K rows");
+static_assert(kUBucket + kSelCap * 2 <= kUKeys && kSelCap <= 65536, "key buckets below the order keys, u16 indexes");
 static_assert(kURecSlots + kThreads * kRecBytes <= kUKeys, "record slots below the order keys");
 
 struct DecodeArgs {
@@ -345,14 +347,17 @@ __device__ __forceinline__ uint32_t rank_in_bin(KeyOf key_of, int n, InBin in_bi
 // Otherwise (a crowded bin, or a range the linear map cannot represent):
 // 11-bit radix digits below the bits kmin and kmax share, with the same
 // direct ranking once a digit is small.  key_of(i) gives key i.  All threads
-// of the block call it and get the same results.
+// of the block call it and get the same results.  *linear_out is 1 when the
+// linear bins decided it (their counts are then left in hist), else 0.
 template <class KeyOf>
 __device__ __forceinline__ uint32_t select_kth(KeyOf key_of, const int64_t C, const int64_t k_eff, uint32_t kmin,
-                                               uint32_t kmax, uint8_t* U, uint32_t* tmp, uint32_t* remaining_out) {
+                                               uint32_t kmax, uint8_t* U, uint32_t* tmp, uint32_t* remaining_out,
+                                               uint32_t* linear_out) {
   uint32_t* hist = reinterpret_cast<uint32_t*>(U + kUSelHist);
   uint32_t* bin = hist + kSelBins;
   const int n = (int)C;
   uint32_t remaining = (uint32_t)k_eff;
+  *linear_out = 0u;
   if (kmin == kmax) {
     *remaining_out = remaining;
     return kmin;
@@ -366,6 +371,7 @@ __device__ __forceinline__ uint32_t select_kth(KeyOf key_of, const int64_t C, co
     if (held <= (uint32_t)kBinRank) {
       const uint32_t key = rank_in_bin(key_of, n, [&](uint32_t k) { return lin(k) == bsel; }, bin, remaining);
       *remaining_out = remaining;
+      *linear_out = 1u;  // hist holds the linear bins' counts
       return key;
     }
     remaining = (uint32_t)k_eff;
@@ -553,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ float s_qn;
   __shared__ int s_T;
   __shared__ int64_t s_quota;
+  __shared__ uint32_t s_rank;  // 1: the best-first list is placed directly (no sort)
   extern __shared__ __align__(128) uint8_t U[];  // 128-byte aligned: staged rows keep whole sectors
 
   const int nhot = kSub * a.rho;
@@ -1141,7 +1148,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   auto key_of = [&](int64_t i) -> uint32_t {
     return keys_staged ? keys[i] : order_key(__ldcg(a.cand_est + cq + i));
   };
-  uint32_t P = 0, remaining = 0;
+  uint32_t P = 0, remaining = 0, linear = 0;
   if (!select_all) {
     uint32_t x = 0xffffffffu, y = 0u;
 #pragma unroll
@@ -1150,7 +1157,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         x = min(x, skey_mm[q][0]);
         y = max(y, skey_mm[q][1]);
       }
-    P = select_kth(key_of, a.C, a.k_eff, x, y, U, tmp, &remaining);
+    P = select_kth(key_of, a.C, a.k_eff, x, y, U, tmp, &remaining, &linear);
   }
   trace_block(a.trace, kTkDecode3, 2);
   int64_t out_off = s_lo;  // place of the slice's first taken entry
@@ -1184,6 +1191,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     eq_take = remaining > eqb ? remaining - eqb : 0u;
     __syncthreads();  // red is reused below
   }
+  // The list best first, placed directly: every key of the query head goes
+  // into the shared bucket of its linear bin of the k-th key search (bins in
+  // key order), so a taken entry's place in the best-first list is the number
+  // of keys in the bins above its own plus those of its bin that precede it
+  // by (key desc, position asc).  It needs those bins, every key in shared
+  // memory and no bin over kOrdBinMax keys; all of that is the same in every
+  // block (each holds the same keys).  Otherwise the last block sorts.
+  bool rank_mode = false;  // the same in every thread
+  uint32_t* bhist = reinterpret_cast<uint32_t*>(U + kUSelHist);
+  uint16_t* bucket = reinterpret_cast<uint16_t*>(U + kUBucket);
+  float bmin = 0.f, bsc = 0.f;
+  if (a.ord_idx != nullptr && !select_all && keys_staged && linear != 0u) {
+    uint32_t x = 0xffffffffu, y = 0u;
+#pragma unroll
+    for (int q = 0; q < kClusterMax; ++q)
+      if (q < cs) {
+        x = min(x, skey_mm[q][0]);
+        y = max(y, skey_mm[q][1]);
+      }
+    bmin = key_to_float(x);  // the k-th key search's linear map
+    bsc = (float)kSelBins / (key_to_float(y) - bmin);
+    // thread t owns bins kSelBins-1-2t and kSelBins-2-2t; each becomes the
+    // number of keys in the bins above it
+    const uint32_t c0 = bhist[kSelBins - 1 - 2 * tid], c1 = bhist[kSelBins - 2 - 2 * tid];
+    const uint32_t mw = __reduce_max_sync(kFull, max(c0, c1));
+    if (lane == 0) red[warp] = mw;
+    uint32_t all;
+    const uint32_t above = block_excl_scan(c0 + c1, tmp, &all);  // its barriers publish red
+    bhist[kSelBins - 1 - 2 * tid] = above;
+    bhist[kSelBins - 2 - 2 * tid] = above + c0;
+    uint32_t mb = 0;
+    for (int w = 0; w < kWarps; ++w) mb = max(mb, red[w]);
+    rank_mode = mb <= kOrdBinMax;
+    if (rank_mode) {
+      __syncthreads();  // every bin's start is in place
+      for (int64_t i = tid; i < a.C; i += kThreads) {
+        const int b = min(kSelBins - 1, (int)((key_to_float(keys[i]) - bmin) * bsc));
+        bucket[atomicAdd(&bhist[b], 1u)] = (uint16_t)i;
+      }
+      // bin b's keys are now bucket[bhist[b + 1] .. bhist[b]) (from 0 for the top bin)
+    }
+    __syncthreads();
+  }
+  if (tid == 0) s_rank = rank_mode ? 1u : 0u;  // read after the barriers of the placement below
   // the slice in order: thread t owns entries [t per, t per + per) of it
   int32_t* selpos = reinterpret_cast<int32_t*>(U + kUSelPos);
   uint32_t nsel;  // entries the slice takes
@@ -1212,6 +1263,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
           a.topk_idx[(int64_t)sq * a.k + out_off + j] = pos;
           if (a.topk_score) a.topk_score[(int64_t)sq * a.k + out_off + j] = e;
         }
+        if (rank_mode) {
+          const int b = min(kSelBins - 1, (int)((key_to_float(k) - bmin) * bsc));
+          const uint32_t lo = b == kSelBins - 1 ? 0u : bhist[b + 1], hi = bhist[b], me = (uint32_t)(s_lo + i);
+          uint32_t rk = lo;
+          for (uint32_t f = lo; f < hi; ++f) {
+            const uint32_t o = bucket[f], ko = keys[o];
+            rk += ko > k || (ko == k && o < me) ? 1u : 0u;
+          }
+          if (rk < a.k_eff) {
+            a.ord_idx[(int64_t)sq * a.k + rk] = pos;
+            a.ord_sc[(int64_t)sq * a.k + rk] = e;
+          }
+        }
         if (j < kListCap) selpos[j] = pos;
         ++j;
       }
@@ -1220,6 +1284,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       for (int64_t i = a.k_eff + tid; i < a.k; i += kThreads) {
         a.topk_idx[(int64_t)sq * a.k + i] = -1;
         if (a.topk_score) a.topk_score[(int64_t)sq * a.k + i] = -INFINITY;
+        if (rank_mode) {
+          a.ord_idx[(int64_t)sq * a.k + i] = -1;
+          a.ord_sc[(int64_t)sq * a.k + i] = -INFINITY;
+        }
       }
     }
   }
@@ -1427,7 +1495,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     // block 0) lists the top-k best first (every slice's entries were in
     // global memory at the barrier before the attention; its row share is
     // the smaller one), then it is done.
-    if (a.ord_idx != nullptr && r == cs - 1 && r != 0) {
+    if (a.ord_idx != nullptr && s_rank == 0u && r == cs - 1 && r != 0) {
       cluster_arrive();
       trace_block(a.trace, kTkDecode2, 3);
       order_tail();
@@ -1467,7 +1535,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   // Without attention every slice's entries are in global memory after one
   // more barrier, and the last block sorts them; with attention a cluster
   // of one block sorts here (a larger one did inside its last barrier).
-  if (a.ord_idx != nullptr) {
+  if (a.ord_idx != nullptr && s_rank == 0u) {
     if (a.out == nullptr) cluster_sync();
     if (r == cs - 1 && (a.out == nullptr || cs == 1)) order_tail();
   }
@@ -1552,7 +1620,10 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   // about as long as two rounds), as far as the other blocks' larger shares
   // still fit the rounds an even share needs: the sort then overlaps the
   // other blocks' attention.
-  if (L.ord_idx != nullptr && L.out != nullptr && cs > 1) {
+  // (Not when every block can place its entries best first itself: keys
+  // staged, k_eff < C; a crowded bin then still falls back to the sort.)
+  const bool placed_directly = ra.C <= kSelCap && ra.k_eff < ra.C;
+  if (L.ord_idx != nullptr && L.out != nullptr && cs > 1 && !placed_directly) {
     constexpr int64_t kRoundRows = 128;  // rows per attention round
     const int64_t total = L.nwin + ra.k_eff;
     const int64_t rounds = ((total + cs - 1) / cs + kRoundRows - 1) / kRoundRows;
