@@ -71,7 +71,8 @@ constexpr int kUAttnEnd = 2 * kStages * kTile * kDim * 2;
 constexpr int kUSelHist = kUStageK + kStages / 2 * kTile * kDim * 2;  // u32 [kSelBins], then u32 [kBinRank]:
                                                               // in the K rows of the second attention round
 constexpr int kUSelPos = kUSelHist + (kSelBins + kBinRank) * 4;  // i32 [kListCap]: positions the block's slice takes
-constexpr int kUBucket = kUSelPos + kListCap * 4;             // u16 [kSelCap]: every key's index, by bin
+constexpr int kUBStart = 0;                                   // u32 [kSelBins]: keys above each linear bin
+constexpr int kUBucket = kUSelPos + kListCap * 4;             // u16 [kSelCap]: the taken keys' indexes, by bin
 constexpr int kUKeys = kUAttnEnd;                             // u32 [kSelCap]: order keys of all C estimates,
                                                               // then i64 [kRowTab]: attention row sources
 constexpr int kUListPos = kUKeys + kSelCap * 4;               // i32 [kListCap]: the block's rerank slice
@@ -81,6 +82,7 @@ static_assert(kUWarpHist + kWarps * kWarpBins * 4 <= kUHot, "per-warp vote count
 static_assert(kUHot + (9 * 1024 + 1) * 4 + 16 <= kUBytes, "hot lists (G = 2) inside the region");
 static_assert(kUSelPos + kListCap * 4 <= kUStageV, "top-k tables inside the second round's K rows");
 static_assert(kUBucket + kSelCap * 2 <= kUKeys && kSelCap <= 65536, "key buckets below the order keys, u16 indexes");
+static_assert(kUBStart + kSelBins * 4 <= kUSelHist, "bin starts below the k-th key search's bins");
 static_assert(kURecSlots + kThreads * kRecBytes <= kUKeys, "record slots below the order keys");
 
 struct DecodeArgs {
@@ -269,11 +271,12 @@ __device__ __forceinline__ float estimate(const uint4 (&x)[8], const float* tq, 
 // (a bin in 0 .. kSelBins-1, or -1 for a key not in play), and the bin
 // holding the `remaining`-th largest key in play is found by scanning from
 // the top bin (bin order must follow key order).  `remaining` loses the keys
-// of the bins above it; *held receives how many keys the bin holds.
+// of the bins above it; *held receives how many keys the bin holds; starts,
+// when given, receives every bin's number of keys in the bins above it.
 // key_of(i) gives the i-th of n keys.  All threads of the block call it.
 template <class KeyOf, class BinOf>
 __device__ __forceinline__ uint32_t count_pass(KeyOf key_of, int n, BinOf bin_of, uint32_t* hist, uint32_t* tmp,
-                                               uint32_t& remaining, uint32_t* held) {
+                                               uint32_t& remaining, uint32_t* held, uint32_t* starts = nullptr) {
   __shared__ uint32_t s_bin, s_skip;
   const int tid = threadIdx.x;
   for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
@@ -287,6 +290,10 @@ __device__ __forceinline__ uint32_t count_pass(KeyOf key_of, int n, BinOf bin_of
   const uint32_t c0 = hist[kSelBins - 1 - 2 * tid], c1 = hist[kSelBins - 2 - 2 * tid];
   uint32_t tot;
   const uint32_t exc = block_excl_scan(c0 + c1, tmp, &tot);
+  if (starts != nullptr) {  // every bin's number of keys in the bins above it
+    starts[kSelBins - 1 - 2 * tid] = exc;
+    starts[kSelBins - 2 - 2 * tid] = exc + c0;
+  }
   if (exc < remaining && exc + c0 >= remaining) {
     s_bin = (uint32_t)(kSelBins - 1 - 2 * tid);
     s_skip = exc;
@@ -348,7 +355,8 @@ __device__ __forceinline__ uint32_t rank_in_bin(KeyOf key_of, int n, InBin in_bi
 // 11-bit radix digits below the bits kmin and kmax share, with the same
 // direct ranking once a digit is small.  key_of(i) gives key i.  All threads
 // of the block call it and get the same results.  *linear_out is 1 when the
-// linear bins decided it (their counts are then left in hist), else 0.
+// linear bins decided it (the number of keys above each bin is then left at
+// U + kUBStart), else 0.
 template <class KeyOf>
 __device__ __forceinline__ uint32_t select_kth(KeyOf key_of, const int64_t C, const int64_t k_eff, uint32_t kmin,
                                                uint32_t kmax, uint8_t* U, uint32_t* tmp, uint32_t* remaining_out,
@@ -367,7 +375,8 @@ __device__ __forceinline__ uint32_t select_kth(KeyOf key_of, const int64_t C, co
   if (isfinite(sc) && sc > 0.f) {
     auto lin = [&](uint32_t k) -> int { return min(kSelBins - 1, (int)((key_to_float(k) - fmin) * sc)); };
     uint32_t held;
-    const int bsel = (int)count_pass(key_of, n, lin, hist, tmp, remaining, &held);
+    const int bsel = (int)count_pass(key_of, n, lin, hist, tmp, remaining, &held,
+                                     reinterpret_cast<uint32_t*>(U + kUBStart));
     if (held <= (uint32_t)kBinRank) {
       const uint32_t key = rank_in_bin(key_of, n, [&](uint32_t k) { return lin(k) == bsel; }, bin, remaining);
       *remaining_out = remaining;
@@ -1191,15 +1200,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     eq_take = remaining > eqb ? remaining - eqb : 0u;
     __syncthreads();  // red is reused below
   }
-  // The list best first, placed directly: every key of the query head goes
-  // into the shared bucket of its linear bin of the k-th key search (bins in
-  // key order), so a taken entry's place in the best-first list is the number
-  // of keys in the bins above its own plus those of its bin that precede it
-  // by (key desc, position asc).  It needs those bins, every key in shared
-  // memory and no bin over kOrdBinMax keys; all of that is the same in every
-  // block (each holds the same keys).  Otherwise the last block sorts.
+  // The list best first, placed directly: the linear count pass of the k-th
+  // key search left, for every bin (bins in key order), the number of keys
+  // in the bins above it; the keys at or above the k-th (every one the list
+  // takes, and all that can precede one of them) go into the shared bucket of
+  // their bin, so a taken entry's place in the best-first list is its bin's
+  // start plus the keys of its bucket that precede it by (key desc, position
+  // asc).  It needs the linear bins and every key in shared memory, the same
+  // in every block (each holds the same keys); otherwise the last block sorts.
   bool rank_mode = false;  // the same in every thread
-  uint32_t* bhist = reinterpret_cast<uint32_t*>(U + kUSelHist);
+  uint32_t* bstart = reinterpret_cast<uint32_t*>(U + kUBStart);
   uint16_t* bucket = reinterpret_cast<uint16_t*>(U + kUBucket);
   float bmin = 0.f, bsc = 0.f;
   if (a.ord_idx != nullptr && !select_all && keys_staged && linear != 0u) {
@@ -1212,27 +1222,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       }
     bmin = key_to_float(x);  // the k-th key search's linear map
     bsc = (float)kSelBins / (key_to_float(y) - bmin);
-    // thread t owns bins kSelBins-1-2t and kSelBins-2-2t; each becomes the
-    // number of keys in the bins above it
-    const uint32_t c0 = bhist[kSelBins - 1 - 2 * tid], c1 = bhist[kSelBins - 2 - 2 * tid];
-    const uint32_t mw = __reduce_max_sync(kFull, max(c0, c1));
-    if (lane == 0) red[warp] = mw;
-    uint32_t all;
-    const uint32_t above = block_excl_scan(c0 + c1, tmp, &all);  // its barriers publish red
-    bhist[kSelBins - 1 - 2 * tid] = above;
-    bhist[kSelBins - 2 - 2 * tid] = above + c0;
-    uint32_t mb = 0;
-    for (int w = 0; w < kWarps; ++w) mb = max(mb, red[w]);
-    rank_mode = mb <= kOrdBinMax;
-    if (rank_mode) {
-      __syncthreads();  // every bin's start is in place
-      for (int64_t i = tid; i < a.C; i += kThreads) {
-        const int b = min(kSelBins - 1, (int)((key_to_float(keys[i]) - bmin) * bsc));
-        bucket[atomicAdd(&bhist[b], 1u)] = (uint16_t)i;
-      }
-      // bin b's keys are now bucket[bhist[b + 1] .. bhist[b]) (from 0 for the top bin)
+    for (int64_t i = tid; i < a.C; i += kThreads) {
+      const uint32_t k = keys[i];
+      if (k >= P) bucket[atomicAdd(&bstart[min(kSelBins - 1, (int)((key_to_float(k) - bmin) * bsc))], 1u)] = (uint16_t)i;
     }
+    // every bin above P's is complete, so bin b's bucket is now
+    // bucket[bstart[b + 1] .. bstart[b]) (from 0 for the top bin)
     __syncthreads();
+    rank_mode = true;
   }
   if (tid == 0) s_rank = rank_mode ? 1u : 0u;  // read after the barriers of the placement below
   // the slice in order: thread t owns entries [t per, t per + per) of it
@@ -1265,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         }
         if (rank_mode) {
           const int b = min(kSelBins - 1, (int)((key_to_float(k) - bmin) * bsc));
-          const uint32_t lo = b == kSelBins - 1 ? 0u : bhist[b + 1], hi = bhist[b], me = (uint32_t)(s_lo + i);
+          const uint32_t lo = b == kSelBins - 1 ? 0u : bstart[b + 1], hi = bstart[b], me = (uint32_t)(s_lo + i);
           uint32_t rk = lo;
           for (uint32_t f = lo; f < hi; ++f) {
             const uint32_t o = bucket[f], ko = keys[o];
