@@ -35,6 +35,8 @@
 // the query is prepared (nothing in this launch reads the slots it writes).
 #include <float.h>
 
+#include <mutex>
+
 #include "paris_device.cuh"
 
 namespace paris {
@@ -1557,7 +1559,69 @@ cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_
   return cudaGetLastError();
 }
 
-int decode_cluster_size(int nchunk_active) { return nchunk_active < kClusterMax ? nchunk_active : kClusterMax; }
+// Clusters of `cs` decode blocks that fit on the device at once (per device,
+// queried once; the kernel's shared-memory limit must be set before).
+int active_clusters(const void* func, int cs) {
+  static std::mutex mu;
+  static int cache[64][kClusterMax + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev][cs] > 0) return cache[dev][cs];
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs, 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kUBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = cs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    int sms = 0;
+    if (dev < 0 || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = cs;
+    n = sms / cs > 0 ? sms / cs : 1;
+  }
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    cache[dev][cs] = n;
+  }
+  return n;
+}
+
+// Blocks per query head.  A head's cluster runs its phases one after
+// another: more blocks per head split the gathers and the passes over keys
+// but leave the phase latencies, and a grid of more clusters than fit at
+// once runs in waves that pay those latencies again.  The size (at most the
+// head's chunks and kClusterMax) minimises waves x per-wave time, the
+// per-wave time modelled as kWaveUs + (kHeadUs + kCandUs C) / size: constants
+// fitted to the kernel's times on GB300 (32 heads of a 131072-token layer
+// take 49 / 71 / 118 us per step at 4 / 2 / 1 blocks per head; 256 heads of
+// a 32768-token layer 175 us at 2 and 135 us at 1; 160 heads of a
+// 262144-token layer 409 / 366 / 402 us at 4 / 2 / 1).
+constexpr float kWaveUs = 27.f, kHeadUs = 20.f, kCandUs = 0.0104f;
+
+int decode_cluster_size(const void* func, int nchunk_active, int64_t heads, int64_t C) {
+  const int cmax = nchunk_active < kClusterMax ? nchunk_active : kClusterMax;
+  int best = cmax;
+  float best_t = 0.f;
+  for (int cs = cmax; cs >= 1; --cs) {
+    const int64_t slots = active_clusters(func, cs);
+    const int64_t waves = (heads + slots - 1) / slots;
+    const float t = (float)waves * (kWaveUs + (kHeadUs + kCandUs * (float)C) / (float)cs);
+    if (cs == cmax || t < best_t) {
+      best = cs;
+      best_t = t;
+    }
+  }
+  return best;
+}
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   const RetrieveArgs& ra = L.ra;
@@ -1571,8 +1635,13 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.flat = ra.flat;
   a.nbins = ra.nbins;
   a.nchunk_active = ra.nchunk_active;
-  const int cs = decode_cluster_size(ra.nchunk_active);
-  if (cs < 1) return cudaErrorInvalidValue;
+  const void* func = a.t.cent ? (const void*)k_decode<true> : (const void*)k_decode<false>;
+  {
+    cudaError_t e = set_smem_limit(func, kUBytes, a.t.cent ? kSmemDecodeTable : kSmemDecode);
+    if (e != cudaSuccess) return e;
+  }
+  if (ra.nchunk_active < 1) return cudaErrorInvalidValue;
+  const int cs = decode_cluster_size(func, ra.nchunk_active, (int64_t)ra.s.batch * ra.s.hq, ra.C);
   a.cpb = (ra.nchunk_active + cs - 1) / cs;
   a.N = ra.N;
   a.C = ra.C;
@@ -1634,11 +1703,6 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
     }
   }
   if (L.ord_idx != nullptr && (ra.k_eff > kOrderMax || ra.topk_score == nullptr)) return cudaErrorInvalidValue;
-  {
-    cudaError_t e = a.t.cent ? set_smem_limit((const void*)k_decode<true>, kUBytes, kSmemDecodeTable)
-                             : set_smem_limit((const void*)k_decode<false>, kUBytes, kSmemDecode);
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs, ra.s.batch * ra.s.hq);
   cfg.blockDim = dim3(kThreads);

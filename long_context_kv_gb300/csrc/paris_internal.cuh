@@ -145,7 +145,7 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 enum SmemKernel { kSmemDecode = 0, kSmemDecodeTable, kSmemAttend, kSmemDense, kSmemKernelCount };
 cudaError_t set_smem_limit(const void* func, int bytes, SmemKernel which);
 
-int decode_cluster_size(int nchunk_active);
+int decode_cluster_size(const void* func, int nchunk_active, int64_t heads, int64_t C);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st);
 cudaError_t launch_fill_empty(int32_t* idx, float* score, int64_t n, cudaStream_t st);
 
