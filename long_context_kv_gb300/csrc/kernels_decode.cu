@@ -1010,6 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   // ordered compaction: thread t owns keys [16 G t, 16 G (t + 1)) of each
   // group's span, compared four at a time (bytes of a word)
   const int64_t cq = (int64_t)sq * a.cmax;
+  __syncthreads();  // red is read above and scanned in below
   {
     uint32_t nsel = 0;
     const uint32_t T4 = (uint32_t)T * 0x01010101u;
@@ -1040,11 +1041,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         n_gt += __popc(gtm[w]);
         n_eq += __popc(eqm[w]);
       }
-      uint32_t eq_tot;
-      const uint32_t eq_rank0 = block_excl_scan(n_eq, tmp, &eq_tot);
+      // one scan of both counts: the keys equal to T are taken in position
+      // order, so those taken before this thread are min(equal before it, allowance)
+      uint32_t gt_rank0 = n_gt, eq_rank0 = n_eq, gt_tot, eq_tot;
+      block_excl_scan2(gt_rank0, eq_rank0, red, gt_tot, eq_tot);
       uint32_t eq_left = (uint32_t)max64(0, min64((int64_t)n_eq, eq_allow - (int64_t)eq_rank0));
-      uint32_t csel;
-      uint32_t pos = nsel + block_excl_scan(n_gt + eq_left, tmp, &csel);
+      const uint32_t csel = gt_tot + (uint32_t)min64((int64_t)eq_tot, eq_allow);
+      uint32_t pos = nsel + gt_rank0 + (uint32_t)min64((int64_t)eq_rank0, eq_allow);
       const int32_t pbase = (int32_t)(a.s.sink + gbase + k0);
 #pragma unroll
       for (int w = 0; w < 4 * kVoteSlots; ++w) {
