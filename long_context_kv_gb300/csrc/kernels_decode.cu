@@ -75,6 +75,13 @@ constexpr int kUSelHist = kUStageK + kStages / 2 * kTile * kDim * 2;  // u32 [kS
 constexpr int kUSelPos = kUSelHist + (kSelBins + kBinRank) * 4;  // i32 [kListCap]: positions the block's slice takes
 constexpr int kUBStart = 0;                                   // u32 [kSelBins]: keys above each linear bin
 constexpr int kUBucket = kUSelPos + kListCap * 4;             // u16 [kSelCap]: the taken keys' indexes, by bin
+// The k-th key search over keys that are not all in shared memory (C > kSelCap)
+// shares the work across the cluster: each block's own keys, every block's
+// histogram, and the keys of the k-th bin with their candidate numbers.
+constexpr int kUHall = 0;                                     // u32 [kClusterMax][kSelBins]
+constexpr int kUOwn = kUSelPos + kListCap * 4;                // u32 [kOwnCap]: the block's slice's order keys
+constexpr int kOwnCap = (kUAttnEnd - kUOwn) / 4;
+constexpr int kUBinEnt = kUAttnEnd;                           // u32 [kBinRank][2]: (key, candidate number)
 constexpr int kUKeys = kUAttnEnd;                             // u32 [kSelCap]: order keys of all C estimates,
                                                               // then i64 [kRowTab]: attention row sources
 constexpr int kUListPos = kUKeys + kSelCap * 4;               // i32 [kListCap]: the block's rerank slice
@@ -85,6 +92,8 @@ static_assert(kUHot + (9 * 1024 + 1) * 4 + 16 <= kUBytes, "hot lists (G = 2) ins
 static_assert(kUSelPos + kListCap * 4 <= kUStageV, "top-k tables inside the second round's K rows");
 static_assert(kUBucket + kSelCap * 2 <= kUKeys && kSelCap <= 65536, "key buckets below the order keys, u16 indexes");
 static_assert(kUBStart + kSelBins * 4 <= kUSelHist, "bin starts below the k-th key search's bins");
+static_assert(kUHall + kClusterMax * kSelBins * 4 <= kUSelHist, "pushed histograms below the search's bins");
+static_assert(kOwnCap >= 16384, "a slice of up to 16384 keys held by its block");
 static_assert(kURecSlots + kThreads * kRecBytes <= kUKeys, "record slots below the order keys");
 
 struct DecodeArgs {
@@ -551,7 +560,144 @@ __device__ __forceinline__ void order_topk(const int32_t* pos_in, const float* s
 
 // kTable: the query's centroid scores come from a learned-centroid table
 // (a separate instantiation, so the analytic path's code is untouched).
-template <bool kTable>
+// The k-th key search over keys that are not all in shared memory, shared
+// by the cluster (see the layout above): each block loads its own slice's
+// order keys (est: the slice's estimates), histograms them in the linear
+// bins of select_kth and pushes the histogram to every block; all find the
+// bin of the k_eff-th key the same way, each pushes its keys of that bin with
+// their candidate numbers, and all rank those few.  ok = false (the same in
+// every block) when the bin holds more than kBinRank keys or the range cannot
+// be mapped.  Every thread of every block of the cluster calls it.
+struct SharedSelect {
+  uint32_t P, remaining, eq_take;
+  int64_t out_off;
+  bool ok;
+};
+
+__device__ __noinline__ SharedSelect shared_select(const float* est, int64_t k_eff, int64_t s_lo, uint32_t nown, int r,
+                                                   int cs, const uint32_t* skey_mm, uint8_t* U, uint32_t* tmp,
+                                                   uint32_t* red, uint32_t* s_sel) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  SharedSelect res = {0u, 0u, 0u, s_lo, false};
+  uint32_t x = 0xffffffffu, y = 0u;
+  for (int q = 0; q < cs; ++q) {
+    x = min(x, skey_mm[2 * q]);
+    y = max(y, skey_mm[2 * q + 1]);
+  }
+  const float fmin = key_to_float(x), fmax = key_to_float(y);
+  const float sc = (float)kSelBins / (fmax - fmin);
+  if (x == y || !isfinite(sc) || !(sc > 0.f)) return res;
+  auto lin = [&](uint32_t k) -> int { return min(kSelBins - 1, (int)((key_to_float(k) - fmin) * sc)); };
+  uint32_t* hist = reinterpret_cast<uint32_t*>(U + kUSelHist);
+  uint32_t* hall2 = reinterpret_cast<uint32_t*>(U + kUHall);
+  uint32_t* ownw = reinterpret_cast<uint32_t*>(U + kUOwn);
+  uint32_t* ent = reinterpret_cast<uint32_t*>(U + kUBinEnt);
+  for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
+  for (uint32_t i = tid; i < nown; i += kThreads) ownw[i] = order_key(__ldcg(est + i));
+  __syncthreads();
+  // the slice's histogram
+  for (uint32_t i = tid; i < nown; i += kThreads) atomicAdd(&hist[lin(ownw[i])], 1u);
+  __syncthreads();
+  for (int i = tid; i < kSelBins; i += kThreads) {
+    const uint32_t v = hist[i];
+    for (int q = 0; q < cs; ++q) dsmem_st_u32(dsmem_addr(hall2 + r * kSelBins + i, q), v);
+  }
+  cluster_sync();
+  // thread t owns bins kSelBins-1-2t and kSelBins-2-2t, scanned from the top
+  const int hb0 = kSelBins - 1 - 2 * tid, hb1 = kSelBins - 2 - 2 * tid;
+  uint32_t c0 = 0, c1 = 0;
+  for (int q = 0; q < cs; ++q) {
+    c0 += hall2[q * kSelBins + hb0];
+    c1 += hall2[q * kSelBins + hb1];
+  }
+  uint32_t tot;
+  const uint32_t exc = block_excl_scan(c0 + c1, tmp, &tot);
+  const uint32_t want = (uint32_t)k_eff;
+  if (exc < want && exc + c0 >= want) {
+    s_sel[0] = (uint32_t)hb0;
+    s_sel[1] = exc;
+  } else if (exc + c0 < want && exc + c0 + c1 >= want) {
+    s_sel[0] = (uint32_t)hb1;
+    s_sel[1] = exc + c0;
+  }
+  __syncthreads();
+  const int bsel = (int)s_sel[0];
+  const uint32_t above_all = s_sel[1];
+  uint32_t held = 0, base_r = 0;
+  for (int q = 0; q < cs; ++q) {
+    const uint32_t c = hall2[q * kSelBins + bsel];
+    held += c;
+    base_r += q < r ? c : 0u;
+  }
+  if (held > (uint32_t)kBinRank) {  // the same in every block
+    __syncthreads();  // s_sel is read above
+    return res;
+  }
+  // keys in the bins above bsel in the blocks before this one
+  uint32_t gl = 0;
+  for (int q = 0; q < r; ++q) {
+    if (hb0 > bsel) gl += hall2[q * kSelBins + hb0];
+    if (hb1 > bsel) gl += hall2[q * kSelBins + hb1];
+  }
+  gl = __reduce_add_sync(kFull, gl);
+  __syncthreads();  // s_sel[0..1] are read above
+  if (tid == 0) s_sel[2] = 0u;
+  if (lane == 0) red[warp] = gl;
+  __syncthreads();
+  uint32_t gt_lower = 0;
+  for (int w = 0; w < kWarps; ++w) gt_lower += red[w];
+  // this block's keys of bin bsel, with their candidate numbers, to every block
+  for (uint32_t i = tid; i < nown; i += kThreads) {
+    const uint32_t k = ownw[i];
+    if (lin(k) == bsel) {
+      const uint32_t slot = base_r + atomicAdd(&s_sel[2], 1u);
+      for (int q = 0; q < cs; ++q) {
+        dsmem_st_u32(dsmem_addr(ent + 2 * slot, q), k);
+        dsmem_st_u32(dsmem_addr(ent + 2 * slot + 1, q), (uint32_t)(s_lo + i));
+      }
+    }
+  }
+  cluster_sync();
+  // the (k_eff - above_all)-th largest of the bin's keys, as in select_kth
+  const uint32_t rem = want - above_all;
+  if (tid < (int)held) {
+    const uint32_t mine = ent[2 * tid];
+    uint32_t ab = 0, at = 0;
+    for (uint32_t j = 0; j < held; ++j) {
+      const uint32_t o = ent[2 * j];
+      ab += o > mine ? 1u : 0u;
+      at += o >= mine ? 1u : 0u;
+    }
+    if (ab < rem && at >= rem) {  // every such thread holds the same key
+      s_sel[3] = mine;
+      s_sel[2] = rem - ab;
+    }
+  }
+  __syncthreads();
+  res.P = s_sel[3];
+  res.remaining = s_sel[2];
+  // keys above P and equal to P before the slice: the lower blocks' keys in
+  // higher bins, and the bin's keys with smaller candidate numbers
+  uint32_t gtb = gt_lower, eqb = 0;
+  for (uint32_t j = 0; j < held; ++j) {
+    const uint32_t o = ent[2 * j], ci = ent[2 * j + 1];
+    if ((int64_t)ci < s_lo) {
+      gtb += o > res.P ? 1u : 0u;
+      eqb += o == res.P ? 1u : 0u;
+    }
+  }
+  res.out_off = gtb + min(eqb, res.remaining);
+  res.eq_take = res.remaining > eqb ? res.remaining - eqb : 0u;
+  res.ok = true;
+  __syncthreads();  // s_sel, red and ent are read above
+  return res;
+}
+
+// kTable: learned centroids (a table) instead of the analytic sign patterns.
+// kShared: more candidates than kSelCap, whose k-th key search the cluster
+// shares (shared_select); a separate instantiation, so the other kernels keep
+// their registers.
+template <bool kTable, bool kShared>
 __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ __align__(16) float qs[kDim];
   __shared__ __align__(16) float zs[kDim];
@@ -570,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
   __shared__ float s_qn;
   __shared__ int s_T;
   __shared__ int64_t s_quota;
+  __shared__ uint32_t s_sel[4];  // the shared k-th key search: bin, keys above it, bin entries, lower blocks' part
   __shared__ uint32_t s_rank;  // 1: the best-first list is placed directly (no sort)
   extern __shared__ __align__(128) uint8_t U[];  // 128-byte aligned: staged rows keep whole sectors
 
@@ -1163,7 +1310,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     return keys_staged ? keys[i] : order_key(__ldcg(a.cand_est + cq + i));
   };
   uint32_t P = 0, remaining = 0, linear = 0;
-  if (!select_all) {
+  int64_t out_off = s_lo;  // place of the slice's first taken entry
+  uint32_t eq_take = 0;    // keys equal to P that the slice takes
+  // Keys not all in shared memory: each block holds its own slice's keys,
+  // histograms them (the linear bins of the search below) and pushes the
+  // histogram to every block; all find the bin of the k_eff-th key the same
+  // way, each pushes its keys of that bin, and all rank those few.  Falls back
+  // (the same in every block) to the search over every key in global memory
+  // when the bin holds more than kBinRank keys or the range cannot be mapped.
+  const uint32_t* own = reinterpret_cast<const uint32_t*>(U + kUOwn);
+  bool shared_search = false;
+  if (kShared && !select_all && !keys_staged && (a.C + cs - 1) / cs <= kOwnCap) {
+    const SharedSelect ss = shared_select(a.cand_est + cq + s_lo, a.k_eff, s_lo, nown, r, cs, &skey_mm[0][0], U, tmp,
+                                          red, s_sel);
+    if (ss.ok) {
+      P = ss.P;
+      remaining = ss.remaining;
+      out_off = ss.out_off;
+      eq_take = ss.eq_take;
+      shared_search = true;
+    }
+  }
+  if (!select_all && !shared_search) {
     uint32_t x = 0xffffffffu, y = 0u;
 #pragma unroll
     for (int q = 0; q < kClusterMax; ++q)
@@ -1174,9 +1342,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     P = select_kth(key_of, a.C, a.k_eff, x, y, U, tmp, &remaining, &linear);
   }
   trace_block(a.trace, kTkDecode3, 2);
-  int64_t out_off = s_lo;  // place of the slice's first taken entry
-  uint32_t eq_take = 0;    // keys equal to P that the slice takes
-  if (!select_all) {
+  if (!select_all && !shared_search) {
     uint32_t gtb = 0, eqb = 0;
     for (int64_t i = tid; i < s_lo; i += kThreads) {
       const uint32_t k = key_of(i);
@@ -1245,7 +1411,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     const uint32_t i0 = min(nown, tid * per), i1 = min(nown, i0 + per);
     uint32_t n_gt = 0, n_eq = 0;
     for (uint32_t i = i0; i < i1; ++i) {
-      const uint32_t k = key_of(s_lo + i);
+      const uint32_t k = kShared && shared_search ? own[i] : key_of(s_lo + i);
       n_gt += select_all || k > P ? 1u : 0u;
       n_eq += !select_all && k == P ? 1u : 0u;
     }
@@ -1254,7 +1420,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     nsel = gt_tot + min(eq_tot, eq_take);
     uint32_t j = gt_b + min(eq_b, eq_take), eq_seen = eq_b;
     for (uint32_t i = i0; i < i1; ++i) {
-      const uint32_t k = key_of(s_lo + i);
+      const uint32_t k = kShared && shared_search ? own[i] : key_of(s_lo + i);
       bool take = select_all || k > P;
       if (!select_all && k == P) take = eq_seen++ < eq_take;
       if (take) {
@@ -1638,9 +1804,18 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.flat = ra.flat;
   a.nbins = ra.nbins;
   a.nchunk_active = ra.nchunk_active;
-  const void* func = a.t.cent ? (const void*)k_decode<true> : (const void*)k_decode<false>;
+  // Many more candidates than every block can hold: the cluster shares the
+  // k-th key search.  Its two cluster barriers and pushes cost about as much as
+  // two passes over 2 kSelCap keys in global memory, so below that every block
+  // still searches all keys itself (measured: 1M-token layer, C = 52403:
+  // 36 -> 12 us; 256K-token layer, C = 13081 at 2 blocks per head: 9.1 -> 9.7 us).
+  const bool shared = ra.C > 2 * kSelCap;
+  const void* func = a.t.cent ? (shared ? (const void*)k_decode<true, true> : (const void*)k_decode<true, false>)
+                              : (shared ? (const void*)k_decode<false, true> : (const void*)k_decode<false, false>);
   {
-    cudaError_t e = set_smem_limit(func, kUBytes, a.t.cent ? kSmemDecodeTable : kSmemDecode);
+    const SmemKernel which = a.t.cent ? (shared ? kSmemDecodeTableShared : kSmemDecodeTable)
+                                      : (shared ? kSmemDecodeShared : kSmemDecode);
+    cudaError_t e = set_smem_limit(func, kUBytes, which);
     if (e != cudaSuccess) return e;
   }
   if (ra.nchunk_active < 1) return cudaErrorInvalidValue;
@@ -1720,7 +1895,8 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return a.t.cent ? cudaLaunchKernelEx(&cfg, k_decode<true>, a) : cudaLaunchKernelEx(&cfg, k_decode<false>, a);
+  if (a.t.cent) return shared ? cudaLaunchKernelEx(&cfg, k_decode<true, true>, a) : cudaLaunchKernelEx(&cfg, k_decode<true, false>, a);
+  return shared ? cudaLaunchKernelEx(&cfg, k_decode<false, true>, a) : cudaLaunchKernelEx(&cfg, k_decode<false, false>, a);
 }
 
 }  // namespace paris

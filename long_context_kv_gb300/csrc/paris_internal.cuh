@@ -142,7 +142,10 @@ cudaError_t launch_pdl(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, c
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current
 // device.  The attribute belongs to one device, so it is set once per
 // (device, kernel) pair; safe to call from several host threads.
-enum SmemKernel { kSmemDecode = 0, kSmemDecodeTable, kSmemAttend, kSmemDense, kSmemKernelCount };
+enum SmemKernel {
+  kSmemDecode = 0, kSmemDecodeTable, kSmemDecodeShared, kSmemDecodeTableShared, kSmemAttend, kSmemDense,
+  kSmemKernelCount
+};
 cudaError_t set_smem_limit(const void* func, int bytes, SmemKernel which);
 
 int decode_cluster_size(const void* func, int nchunk_active, int64_t heads, int64_t C);

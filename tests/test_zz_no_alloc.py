@@ -1,8 +1,9 @@
 """paris_sparse_attend_noalloc: the attention entry point for callers that
 must not allocate device memory (for instance while another component owns
 the device allocator, or under a fixed memory budget).  Its scratch is a fixed
-area inside the library; it must give what paris_sparse_attend gives, call
-after call, and refuse shapes its area cannot hold.
+area inside the library; it must give what paris_sparse_attend gives (and
+the oracle's attention), call after call, and refuse shapes its area cannot
+hold.
 
 This file is collected last on purpose, so a run that stops at the first
 failure has already run every other test."""
@@ -11,6 +12,7 @@ import pytest
 import torch
 
 from long_context_kv_gb300 import paris as P
+from oracle import pariskv as o
 from tests import gpu_cases as g
 
 pytestmark = pytest.mark.gpu
@@ -21,6 +23,22 @@ def _built():
     from long_context_kv_gb300 import build
     build.build()
     P.load()
+
+
+def _check_against_oracle(c, qd, idx, k_eff, got):
+    """Every (sequence, query head) of the no-alloc output within 2e-2 of the
+    float64 attention over Sink, Local, Update Buffer and its top-k rows."""
+    q_seen = qd.float().cpu().numpy()
+    idx_h = idx.cpu().numpy()
+    got_h = got.float().cpu().numpy()
+    Kb, Vb = g.as_seen(c.K, torch.bfloat16), g.as_seen(c.V, torch.bfloat16)
+    z = c.zones
+    for seq in range(c.cfg["batch"]):
+        for qh in range(c.cfg["n_q_heads"]):
+            kvh = qh // c.G
+            rows = np.concatenate([z.sink(), z.local(), z.buffer(), idx_h[seq, qh, :k_eff]]).astype(np.int64)
+            ref = o.attention(q_seen[seq, qh], Kb[seq, kvh, rows], Vb[seq, kvh, rows])
+            assert np.max(np.abs(got_h[seq, qh] - ref)) <= g.ATTN_ATOL, (seq, qh)
 
 
 def test_noalloc_attention_matches_the_context_scratch_version_twice():
@@ -37,6 +55,7 @@ def test_noalloc_attention_matches_the_context_scratch_version_twice():
         c.ctx.paris_check_device()
         np.testing.assert_allclose(got.float().cpu().numpy(), ref.float().cpu().numpy(), rtol=0, atol=g.ATTN_ATOL)
         assert k_eff == 256
+        _check_against_oracle(c, qd, idx, k_eff, got)
 
 
 def test_noalloc_attention_across_contexts_of_different_shapes():
@@ -60,6 +79,7 @@ def test_noalloc_attention_across_contexts_of_different_shapes():
         torch.cuda.synchronize()
         c.ctx.paris_check_device()
         np.testing.assert_allclose(got.float().cpu().numpy(), ref.float().cpu().numpy(), rtol=0, atol=g.ATTN_ATOL)
+        _check_against_oracle(c, qd, idx, k_eff, got)
         return k_eff
 
     assert compare(big, 0) == 4000  # (16 + 64 + 4000) rows -> 64 splits per head
