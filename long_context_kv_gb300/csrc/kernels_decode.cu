@@ -22,14 +22,19 @@
 //      the list and pushes the order keys of the
 //      estimates (and their range) to every block;
 //   4. barrier; every block finds the k-th best key over all C (a counting
-//      pass in shared memory), counts the entries taken before its slice and
-//      writes the ones its slice takes at their place in the top-k, and
-//      pushes their count to every block;
+//      pass in shared memory; with far more candidates than a block holds,
+//      a search the cluster shares, two more barriers), counts the entries
+//      taken before its slice and writes the ones its slice takes at their
+//      place in the top-k (and, for the list best first, at their rank in
+//      it), and pushes their count to every block;
 //   5. barrier; those rows, topped up with window rows to an even share of
 //      all rows, are the block's attention rows, staged in rounds of 128
 //      rows, two rounds in flight, every warp scoring 4 rows of a round with
 //      its own online softmax; the block's partial goes to block 0;
-//   6. barrier; block 0 merges the partials.
+//   6. barrier; block 0 merges the partials (where step 4 could not rank
+//      the entries, the last block sorts the list best first meanwhile).
+// The cluster size CS is chosen per launch from the waves of clusters the
+// grid needs (decode_cluster_size).
 // A decode token appended in the same step is read from the caller's k/v
 // where the attention needs it, and written to the cache by one warp while
 // the query is prepared (nothing in this launch reads the slots it writes).
