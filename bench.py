@@ -523,7 +523,11 @@ def run_ours(args, rank, world):
     # end to end through the public API with host buffers: each step's inputs
     # (q, k, v packed in one pinned buffer) go up in one copy, the step runs,
     # and its outputs (top-k positions and estimates, attention output, packed
-    # in one device buffer) come back in one copy
+    # in one device buffer) come back in one copy.  The copies run on a stream
+    # of their own with three device buffers each way: the next step's inputs
+    # go up while a step runs and its outputs come back during the next one,
+    # so no copy sits between two decode steps on the compute stream.  The
+    # timed region ends when the last outputs are in host memory.
     L0 = layers[0]
 
     def packed(parts, device, pinned=False):
@@ -537,25 +541,54 @@ def run_ours(args, rank, world):
     h_q.copy_(L0["qs"][0])
     h_k.copy_(L0["kn"][0])
     h_v.copy_(L0["vn"][0])
-    d_in, (d_q, d_k, d_v) = packed([L0["qs"][0], L0["kn"][0], L0["vn"][0]], "cuda")
-    d_res, (d_idx, d_sc, d_out) = packed([L0["idx"], L0["sc"], L0["out"]], "cuda")
-    h_res = torch.empty_like(d_res, device="cpu", pin_memory=True)
+    nbuf = 3
+    d_ins = [packed([L0["qs"][0], L0["kn"][0], L0["vn"][0]], "cuda") for _ in range(nbuf)]
+    d_ress = [packed([L0["idx"], L0["sc"], L0["out"]], "cuda") for _ in range(nbuf)]
+    h_ress = [torch.empty_like(d_ress[0][0], device="cpu", pin_memory=True) for _ in range(nbuf)]
+    copy_stream = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]   # inputs of buffer j are on the device
+    ev_run = [torch.cuda.Event() for _ in range(nbuf)]  # the step using buffer j is done
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]  # outputs of buffer j are in host memory
+    for j in range(nbuf):
+        ev_run[j].record(stream)
+        ev_out[j].record(stream)
+
+    def inputs_up(s_):
+        j = s_ % nbuf
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_run[j])  # the step that last read buffer j is done
+            d_ins[j][0].copy_(h_in, non_blocking=True)
+            ev_in[j].record(copy_stream)
+
     barrier()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     keys_e2e = 0
     e2.record(stream)
-    for _ in range(args.steps):
+    inputs_up(0)
+    for s_ in range(args.steps):
+        j = s_ % nbuf
+        if s_ + 1 < args.steps:
+            inputs_up(s_ + 1)
         L = layers[i % nl]
         keys_e2e += L["ctx"].paris_get_state()["N"] * b * hkv  # host bookkeeping, no device work
-        d_in.copy_(h_in, non_blocking=True)
+        _, (d_q, d_k, d_v) = d_ins[j]
+        d_res, (d_idx, d_sc, d_out) = d_ress[j]
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])  # buffer j's last outputs are in host memory
         L["ctx"].paris_decode_step(d_k, d_v, d_q, d_idx, d_sc, d_out)
-        h_res.copy_(d_res, non_blocking=True)
+        ev_run[j].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_run[j])
+            h_ress[j].copy_(d_res, non_blocking=True)
+            ev_out[j].record(copy_stream)
         i += 1
+    for j in range(nbuf):
+        stream.wait_event(ev_out[j])
     e3.record(stream)
     barrier()
     ms_e2e = max_over_ranks(e2.elapsed_time(e3))
     h2d = h_in.numel()
-    d2h = h_res.numel()
+    d2h = h_ress[0].numel()
 
     # recall@k on layer 0 against the exact float64 top-k of <k, q>
     recall = None
