@@ -988,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         if (lane == 0) hsm[e2] = (int32_t)(S + (hb & 7u)) - (int32_t)hpre[e2];
       }
       cp_async_wait_all();
-      __syncthreads();
+      __syncwarp();  // a warp walks exactly the lists it staged
     }
     // warp w walks lists w, w + 32, ...; lane l takes entries l, l + 32, ...
     uint32_t* votes32 = reinterpret_cast<uint32_t*>(span);
