@@ -61,8 +61,9 @@ typedef enum {
 
 typedef enum {
   PARIS_TOPK_BY_SCORE = 0,   /* best estimate first, equal estimates by ascending
-                                position (one block per list sorts it at the
-                                end of the retrieval kernel)                  */
+                                position (each block writes its entries at
+                                their rank; past 24576 candidates one block per
+                                list sorts it at the end of the kernel)       */
   PARIS_TOPK_BY_POSITION = 1 /* the same set in ascending position (no sort)   */
 } paris_topk_order;
 
@@ -145,8 +146,10 @@ paris_status paris_append_decode(paris_ctx* ctx, const void* k, const void* v, p
  * layout, the RSQ-IP estimates of <k, q> of those positions; entries past
  * k_eff are -1 and -inf.  topk_score may be NULL.  k_eff: host, receives
  * min(topk, C) (0 while the Retrieval zone is empty).  One launch (with
- * PARIS_TOPK_BY_SCORE its blocks first write position order to context
- * scratch, then one block per query head sorts it into topk_idx/score).    */
+ * PARIS_TOPK_BY_SCORE its blocks write position order to context scratch
+ * and, where every key of the query head is in their shared memory, each
+ * entry at its best-first rank in topk_idx/score; otherwise one block per
+ * query head sorts the scratch into them).                                */
 paris_status paris_retrieve(paris_ctx* ctx, const void* q, paris_dtype dtype, int32_t* topk_idx,
                             float* topk_score, int64_t* k_eff, void* stream);
 
