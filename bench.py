@@ -560,6 +560,13 @@ def run_ours(args, rank, world):
             d_ins[j][0].copy_(h_in, non_blocking=True)
             ev_in[j].record(copy_stream)
 
+    # the keys each step scans, from each layer's zone state: an append fills
+    # the Update Buffer, and the append that fills it moves update_buf tokens
+    # into the Retrieval zone before the step's retrieval (checked below
+    # against the library's own state)
+    zone = [L["ctx"].paris_get_state() for L in layers]
+    zN = [z_["N"] for z_ in zone]
+    zbuf = [z_["n_buf"] for z_ in zone]
     barrier()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     keys_e2e = 0
@@ -569,8 +576,13 @@ def run_ours(args, rank, world):
         j = s_ % nbuf
         if s_ + 1 < args.steps:
             inputs_up(s_ + 1)
-        L = layers[i % nl]
-        keys_e2e += L["ctx"].paris_get_state()["N"] * b * hkv  # host bookkeeping, no device work
+        li = i % nl
+        L = layers[li]
+        zbuf[li] += 1
+        if zbuf[li] == w["update_buf"]:
+            zN[li] += w["update_buf"]
+            zbuf[li] = 0
+        keys_e2e += zN[li] * b * hkv
         _, (d_q, d_k, d_v) = d_ins[j]
         d_res, (d_idx, d_sc, d_out) = d_ress[j]
         stream.wait_event(ev_in[j])
@@ -587,6 +599,9 @@ def run_ours(args, rank, world):
     e3.record(stream)
     barrier()
     ms_e2e = max_over_ranks(e2.elapsed_time(e3))
+    for li, L in enumerate(layers):
+        st_ = L["ctx"].paris_get_state()
+        assert (st_["N"], st_["n_buf"]) == (zN[li], zbuf[li]), "zone bookkeeping of the end-to-end loop"
     h2d = h_in.numel()
     d2h = h_ress[0].numel()
 
