@@ -293,7 +293,8 @@ def run_ours(args, rank, world):
 
     if args.profile_case:
         # the decode steps, then as many standalone sparse-attention calls
-        # (over each layer's last top-k) and dense-attention calls on the same caches
+        # (over each layer's last top-k), dense-attention calls and GQA-shared
+        # attention calls on the same caches
         for i in range(args.warmup + args.steps):
             step(i)
         for i in range(args.warmup + args.steps):
@@ -302,6 +303,9 @@ def run_ours(args, rank, world):
         for i in range(args.warmup + args.steps):
             L = layers[i % nl]
             L["ctx"].paris_dense_attend(L["qs"][0], L["out"])
+        for i in range(args.warmup + args.steps):
+            L = layers[i % nl]
+            L["ctx"].paris_sparse_attend_gqa(L["qs"][0], L["idx"], L["out"])
         torch.cuda.synchronize()
         return {"profile_case": DESCRIPTION[args.workload], "layers": nl, "steps": args.warmup + args.steps}
 
