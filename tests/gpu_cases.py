@@ -171,8 +171,12 @@ def check_retrieve(c: Case, q: np.ndarray, heads=None, stages=True):
             est = c.ctx.paris_debug_dump(P.DUMP_CAND_EST, seq, qh)
             np.testing.assert_allclose(est, r["est"], rtol=SCORE_RTOL, atol=1e-30)
             assert np.array_equal(est.view(np.uint32), r["est"].view(np.uint32)), "estimates not bit-identical"
-        np.testing.assert_array_equal(idx_h[seq, qh, :k_eff], S + r["top_idx"])
-        np.testing.assert_allclose(sc_h[seq, qh, :k_eff], r["top_est"], rtol=SCORE_RTOL, atol=1e-30)
+        top_idx, top_est = r["top_idx"], r["top_est"]
+        if c.cfg.get("topk_order") == P.PARIS_TOPK_BY_POSITION:  # the same set in ascending position
+            perm = np.argsort(top_idx, kind="stable")
+            top_idx, top_est = top_idx[perm], top_est[perm]
+        np.testing.assert_array_equal(idx_h[seq, qh, :k_eff], S + top_idx)
+        np.testing.assert_allclose(sc_h[seq, qh, :k_eff], top_est, rtol=SCORE_RTOL, atol=1e-30)
         assert np.all(idx_h[seq, qh, k_eff:] == -1)
         assert np.all(np.isneginf(sc_h[seq, qh, k_eff:]))
     return qd, idx, k_eff
