@@ -8,8 +8,9 @@ estimates and top-k bit for bit (against the oracle's encoding of every
 key, flushed ones included) and the attention within 2e-2.  The shapes
 reach the kernel's different regimes: one to five index chunks per head, one
 to four blocks per head, candidate lists held in shared memory or not, the
-cluster-shared k-th key search, and the best-first list placed directly or
-sorted."""
+cluster-shared k-th key search, the best-first list placed directly or
+sorted, and (every fourth case) learned centroids instead of the analytic
+ones."""
 import numpy as np
 import pytest
 import torch
@@ -45,8 +46,12 @@ def draw(i):
     k = int(rng.choice([1, 64, 300, 1024, 2048]))
     rho = int(rng.integers(1, 9))
     order = P.PARIS_TOPK_BY_SCORE if rng.random() < 0.8 else P.PARIS_TOPK_BY_POSITION
+    table = None
+    if i % 4 == 3:  # learned centroids: a random unit table per KV head
+        table = rng.standard_normal((hkv, 16, 256, 8)).astype(np.float32)
+        table /= np.linalg.norm(table, axis=-1, keepdims=True)
     return dict(T=S + N + L, batch=b, n_kv_heads=hkv, n_q_heads=hkv * G, sink=S, local=L, update_buf=U,
-                topk=k, cand_bp=cand_bp, rho=rho, topk_order=order, seed=2000 + i)
+                topk=k, cand_bp=cand_bp, rho=rho, topk_order=order, seed=2000 + i, table=table)
 
 
 @pytest.mark.parametrize("i", range(CASES))
