@@ -62,7 +62,7 @@ typedef enum {
 typedef enum {
   PARIS_TOPK_BY_SCORE = 0,   /* best estimate first, equal estimates by ascending
                                 position (each block writes its entries at
-                                their rank; past 12288 candidates one block per
+                                their rank; past 16384 candidates one block per
                                 list sorts it at the end of the kernel)       */
   PARIS_TOPK_BY_POSITION = 1 /* the same set in ascending position (no sort)   */
 } paris_topk_order;

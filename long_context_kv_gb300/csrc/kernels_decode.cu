@@ -51,12 +51,13 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kClusterMax = 4;
 constexpr int kVoteSlots = 2;       // chunks per block whose votes stay in shared memory
-constexpr int kListCap = 4096;      // candidates of the block's slice kept in shared memory
+constexpr int kListCap = 4032;      // candidates of the block's slice kept in shared memory
 constexpr int kTile = 64;           // attention rows per pipeline stage
 constexpr int kStages = 4;
-constexpr int kSelCap = 12288;      // candidates whose order keys every block of the cluster holds
+constexpr int kSelCap = 16384;      // candidates whose order keys every block of the cluster holds
 constexpr int kSelBins = 2048;      // 11-bit radix digits
 constexpr int kBinRank = 64;        // keys left in the k-th digit that are ranked directly
+constexpr int kSharedSelectMin = 24576;  // candidates past which the cluster shares the k-th key search
 constexpr int kRowTab = kSelCap / 2;  // attention rows whose sources are resolved into a table
 static_assert(kTile * 16 == kThreads, "16 threads per staged row");
 static_assert(2 * kWarps == kTile, "two rows of a tile per warp");
@@ -1811,10 +1812,10 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   a.nchunk_active = ra.nchunk_active;
   // Many more candidates than every block can hold: the cluster shares the
   // k-th key search.  Its two cluster barriers and pushes cost about as much as
-  // two passes over 2 kSelCap keys in global memory, so below that every block
+  // two passes over 24576 keys in global memory, so below that every block
   // still searches all keys itself (measured: 1M-token layer, C = 52403:
   // 36 -> 12 us; 256K-token layer, C = 13081 at 2 blocks per head: 9.1 -> 9.7 us).
-  const bool shared = ra.C > 2 * kSelCap;
+  const bool shared = ra.C > kSharedSelectMin;
   const void* func = a.t.cent ? (shared ? (const void*)k_decode<true, true> : (const void*)k_decode<true, false>)
                               : (shared ? (const void*)k_decode<false, true> : (const void*)k_decode<false, false>);
   {

@@ -34,7 +34,7 @@ def test_many_candidates_shared_search_matches_the_oracle(repeat):
     base = synth.keys(91, 1, 1, 0, -(-T // repeat), 128, scale)
     K = np.ascontiguousarray(np.repeat(base, repeat, axis=2)[:, :, :T])
     c = g.make_case(T, seed=91, K=K, **KW)
-    assert c.zones.N == 60000  # C = N: every key is a candidate, well past 2 x 12288
+    assert c.zones.N == 60000  # C = N: every key is a candidate, well past 24576
     qd, idx, k_eff = g.check_retrieve(c, g.queries_from_zone(c))
     assert k_eff == 700
     idx_h = idx.cpu().numpy()
