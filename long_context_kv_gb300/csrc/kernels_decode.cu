@@ -29,8 +29,9 @@
 //      it), and pushes their count to every block;
 //   5. barrier; those rows, topped up with window rows to an even share of
 //      all rows, are the block's attention rows, staged in rounds of 128
-//      rows, two rounds in flight, every warp scoring 4 rows of a round with
-//      its own online softmax; the block's partial goes to block 0;
+//      rows, two rounds in flight, every warp copying and scoring its own 4
+//      rows of a round (no block barrier between rounds) with its own online
+//      softmax; the block's partial goes to block 0;
 //   6. barrier; block 0 merges the partials (where step 4 could not rank
 //      the entries, the last block sorts the list best first meanwhile).
 // The cluster size CS is chosen per launch from the waves of clusters the
@@ -1536,10 +1537,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     trace_block(a.trace, kTkDecode1, 3);
     // Rounds of kRound rows through two halves of the stage area: round
     // rd + 2 loads into the half that round rd has just used, so two rounds
-    // are in flight.  A round's copies: 16 threads per row, one 16-byte piece
-    // each.  Warp w scores rows 4 w .. 4 w + 3 of a round (8 lanes per row,
-    // 16 dimensions each) with its own online softmax; lane l accumulates
-    // output dimensions 4 l .. 4 l + 3 over the warp's rows.
+    // are in flight.  Warp w copies and scores rows 4 w .. 4 w + 3 of every
+    // round, so it waits for its own copies only (no block barrier between
+    // rounds): 16 lanes per row copy one 16-byte piece each; 8 lanes per row
+    // score it (16 dimensions each) with the warp's own online softmax; lane l
+    // accumulates output dimensions 4 l .. 4 l + 3 over the warp's rows.
     constexpr int kRound = kStages * kTile / 2;
     static_assert(kRound == 4 * kWarps && 16 * kRound == 2 * kThreads, "4 rows per warp, 2 copied rows per thread");
     const int nrounds = (nrows + kRound - 1) / kRound;
@@ -1547,8 +1549,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       const int half = rd & 1;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int rr = (tid >> 4) + 64 * u, ch = tid & 15;  // round row, 16-byte piece
-        const int so = (half * kRound + rr) * kDim + 8 * (ch ^ ((tid >> 4) & 7));  // spiece: rr & 7 = (tid >> 4) & 7
+        const int rr = 4 * warp + 2 * u + (lane >> 4), ch = lane & 15;  // the warp's own round row, 16-byte piece
+        const int so = (half * kRound + rr) * kDim + 8 * (ch ^ (rr & 7));  // spiece
         uint16_t* kd = stK + so;
         uint16_t* vd = stV + so;
         const int rl = rd * kRound + rr;
@@ -1583,8 +1585,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     float M = -FLT_MAX, l = 0.f, o4[4] = {0.f, 0.f, 0.f, 0.f};
     for (int rd = 0; rd < nrounds; ++rd) {
       const int half = rd & 1;
-      cp_async_wait_group<1>();  // all but the newest group: round rd has landed
-      __syncthreads();
+      cp_async_wait_group<1>();  // all but the newest group: the warp's rows of round rd have landed
+      __syncwarp();
       if (rd < 8) trace_mark(tr, kTrDecodeRound + 2 * rd);
       const uint16_t* kh = stK + half * kRound * kDim;
       const uint16_t* vh = stV + half * kRound * kDim;
@@ -1624,7 +1626,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         o4[3] += p * __uint_as_float(v.y & 0xffff0000u);
       }
       M = Mn;
-      __syncthreads();  // this half is refilled next
+      __syncwarp();  // the warp's rows of this half are refilled next
       if (rd < 8) trace_mark(tr, kTrDecodeRound + 2 * rd + 1);
       issue(rd + 2);
     }
