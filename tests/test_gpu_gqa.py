@@ -97,3 +97,24 @@ def test_gqa_at_full_size_on_sampled_heads():
                     update_buf=128, topk=1024, cand_bp=500)
     qd, idx, _, k_eff = g.run_retrieve(c, g.queries_from_zone(c))
     check_gqa(c, qd, idx, k_eff, heads=[(0, 0), (0, 13), (0, 31)])
+
+
+@pytest.mark.parametrize("hq", [4, 16])
+def test_lists_crowded_into_a_few_slices(hq):
+    """Caller-made lists whose G heads cover one contiguous run of positions
+    (each head its own 1024, in shuffled order): the union piles up in the
+    first slices of the Retrieval zone, so those blocks hold more union rows
+    than they keep in shared memory (the rest go through the context's union
+    list) and stream many tiles while the others have none; with G = 16
+    every row of the kernel's head tiles is a real query head."""
+    S, L, U, N = 16, 64, 32, 100000
+    c = g.make_case(S + N + L, seed=66, batch=1, n_kv_heads=1, n_q_heads=hq, sink=S, local=L, update_buf=U,
+                    topk=1024, cand_bp=10000)
+    assert c.zones.N == N
+    rng = np.random.default_rng(hq)
+    lists = (S + np.arange(hq * 1024)).reshape(hq, 1024)
+    lists = np.stack([rng.permutation(r) for r in lists]).astype(np.int32)
+    idx = torch.from_numpy(lists[None]).cuda()
+    qd = g.to_dev(g.queries_from_zone(c), torch.bfloat16)
+    _, sizes = check_gqa(c, qd, idx, 1024)
+    assert sizes[(0, 0)] == hq * 1024
