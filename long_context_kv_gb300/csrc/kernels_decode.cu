@@ -1541,7 +1541,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     // round, so it waits for its own copies only (no block barrier between
     // rounds): 16 lanes per row copy one 16-byte piece each; 8 lanes per row
     // score it (16 dimensions each) with the warp's own online softmax; lane l
-    // accumulates output dimensions 4 l .. 4 l + 3 over the warp's rows.
+    // accumulates output dimensions 4 l .. 4 l + 3 over the warp's rows.  The
+    // instantiation with the cluster-shared k-th key search keeps the block
+    // barriers and copies rows (tid / 16) + 64 u (its registers spill less
+    // that way, and its many-round attention of large k ran faster).
     constexpr int kRound = kStages * kTile / 2;
     static_assert(kRound == 4 * kWarps && 16 * kRound == 2 * kThreads, "4 rows per warp, 2 copied rows per thread");
     const int nrounds = (nrows + kRound - 1) / kRound;
@@ -1549,7 +1552,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
       const int half = rd & 1;
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int rr = 4 * warp + 2 * u + (lane >> 4), ch = lane & 15;  // the warp's own round row, 16-byte piece
+        const int rr = kShared ? (tid >> 4) + 64 * u : 4 * warp + 2 * u + (lane >> 4), ch = lane & 15;  // round row, piece
         const int so = (half * kRound + rr) * kDim + 8 * (ch ^ (rr & 7));  // spiece
         uint16_t* kd = stK + so;
         uint16_t* vd = stV + so;
@@ -1586,7 +1589,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     for (int rd = 0; rd < nrounds; ++rd) {
       const int half = rd & 1;
       cp_async_wait_group<1>();  // all but the newest group: the warp's rows of round rd have landed
-      __syncwarp();
+      if constexpr (kShared) __syncthreads(); else __syncwarp();
       if (rd < 8) trace_mark(tr, kTrDecodeRound + 2 * rd);
       const uint16_t* kh = stK + half * kRound * kDim;
       const uint16_t* vh = stV + half * kRound * kDim;
@@ -1626,7 +1629,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
         o4[3] += p * __uint_as_float(v.y & 0xffff0000u);
       }
       M = Mn;
-      __syncwarp();  // the warp's rows of this half are refilled next
+      if constexpr (kShared) __syncthreads(); else __syncwarp();  // this half's rows are refilled next
       if (rd < 8) trace_mark(tr, kTrDecodeRound + 2 * rd + 1);
       issue(rd + 2);
     }
