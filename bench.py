@@ -145,7 +145,10 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-TRAFFIC_SOURCES = {"decode": ["kernels_decode.cu", "kernels_attend.cu"], "dense": ["kernels_dense.cu"]}
+TRAFFIC_SOURCES = {  # each kernel's source file and the headers it includes
+    "decode": ["kernels_decode.cu", "paris_device.cuh", "paris_internal.cuh"],
+    "dense": ["kernels_dense.cu", "paris_device.cuh", "paris_internal.cuh"],
+}
 
 
 TRAFFIC_WORKLOAD = "llama8b-128k"  # the workload the committed counters were taken on

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kAttnThreads) k_attend(const void* __restrict_
   const int d = tid;
   // every thread's first batch of o loads goes out together with warp 0's
   // loads of the splits' (max, sum)
-  constexpr int kBatch = 16;
+  constexpr int kBatch = 32;
   float oo[kBatch];
 #pragma unroll
   for (int u = 0; u < kBatch; ++u) oo[u] = u < nsplit ? __ldcg(part + (int64_t)u * kPartStride + 4 + d) : 0.f;

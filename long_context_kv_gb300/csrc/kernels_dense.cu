@@ -390,11 +390,22 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   __threadfence();
   // every split's (max, sum) of every head at once, then per head the
   // weights exp2(m_s - max) (0 for a split without rows), then each output
-  // element's weighted sum over the splits with its loads eight at a time
+  // element's weighted sum over the splits with its loads 32 at a time; a
+  // thread's first batch of its first element goes out before the weights
   const int nsplit = gridDim.x;
   float* ml = reinterpret_cast<float*>(dsm);  // [G][nsplit][2], then f [G][nsplit], then Lt [G]
   float* fw = ml + 2 * G * nsplit;
   float* lt = fw + G * nsplit;
+  constexpr int kMB = 32;
+  auto elem_at = [&](int e) {
+    return a.part + (((int64_t)seq * a.s.hq + qh0 + e / kDim) * a.nsplit_max) * kPartStride + 4 + e % kDim;
+  };
+  float oo[kMB];
+  if (tid < G * kDim) {
+    const float* ph = elem_at(tid);
+#pragma unroll
+    for (int u = 0; u < kMB; ++u) oo[u] = u < nsplit ? __ldcg(ph + (int64_t)u * kPartStride) : 0.f;
+  }
   for (int e = tid; e < G * nsplit; e += kDThreads) {
     const int h = e / nsplit, s0 = e - h * nsplit;
     const float* ph = a.part + (((int64_t)seq * a.s.hq + qh0 + h) * a.nsplit_max + s0) * kPartStride;
@@ -422,14 +433,15 @@ __global__ void __launch_bounds__(kDThreads, 1) k_dense(DenseArgs a) {
   __syncthreads();
   for (int e = tid; e < G * kDim; e += kDThreads) {
     const int h = e / kDim, d = e % kDim;
-    const float* ph = a.part + (((int64_t)seq * a.s.hq + qh0 + h) * a.nsplit_max) * kPartStride + 4 + d;
+    const float* ph = elem_at(e);
     float ot = 0.f;
-    for (int s0 = 0; s0 < nsplit; s0 += 8) {
-      float oo[8];
+    for (int s0 = 0; s0 < nsplit; s0 += kMB) {
+      if (s0 > 0 || e != tid) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) oo[u] = s0 + u < nsplit ? __ldcg(ph + (int64_t)(s0 + u) * kPartStride) : 0.f;
+        for (int u = 0; u < kMB; ++u) oo[u] = s0 + u < nsplit ? __ldcg(ph + (int64_t)(s0 + u) * kPartStride) : 0.f;
+      }
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < kMB; ++u)
         if (s0 + u < nsplit) ot += oo[u] * fw[h * nsplit + s0 + u];
     }
     const float L = lt[h];
