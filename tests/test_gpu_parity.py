@@ -194,13 +194,15 @@ def test_retrieval_zone_in_host_memory_matches_hbm():
     g.check_attention(b, qd, idx, k_eff)
 
 
-def test_decode_step_equals_the_three_calls():
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_step_equals_the_three_calls(dtype):
     """paris_decode_step (one fused kernel unless the append flushes) gives
     the top-k and estimates of append + retrieve + sparse_attend bit for bit,
     and their attention output up to float32 summation order, across
-    flushes."""
+    flushes; with float32 inputs the step's own token enters the attention
+    converted as the append stores it."""
     kw = dict(seed=24, batch=2, n_kv_heads=2, n_q_heads=4, sink=16, local=64, update_buf=16, topk=64,
-              cand_bp=500, rho=4)
+              cand_bp=500, rho=4, dtype=dtype)
     a = g.make_case(16 + 20000 + 64, **kw)
     b = g.make_case(16 + 20000 + 64, **kw)
     shp = (2, 4, 64)
@@ -208,7 +210,7 @@ def test_decode_step_equals_the_three_calls():
         k = synth.drift_keys(24, 2, 2, t, 128, a.scale, rate=0.3)
         v = synth.decode_values(24, 2, 2, t, 128)
         q = g.queries_from_zone(a, step=t)
-        kd, vd, qd = g.to_dev(k, torch.bfloat16), g.to_dev(v, torch.bfloat16), g.to_dev(q, torch.bfloat16)
+        kd, vd, qd = g.to_dev(k, dtype), g.to_dev(v, dtype), g.to_dev(q, dtype)
         ia = torch.empty(shp, dtype=torch.int32, device="cuda")
         sa = torch.empty(shp, dtype=torch.float32, device="cuda")
         oa = torch.empty((2, 4, 128), dtype=torch.bfloat16, device="cuda")
