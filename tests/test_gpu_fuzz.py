@@ -9,8 +9,8 @@ key, flushed ones included) and the attention within 2e-2.  The shapes
 reach the kernel's different regimes: one to five index chunks per head, one
 to four blocks per head, candidate lists held in shared memory or not, the
 cluster-shared k-th key search, the best-first list placed directly or
-sorted, and (every fourth case) learned centroids instead of the analytic
-ones."""
+sorted, (every fourth case) learned centroids instead of the analytic ones,
+and (every sixth) the Retrieval zone's K/V in mapped host memory."""
 import numpy as np
 import pytest
 import torch
@@ -50,8 +50,10 @@ def draw(i):
     if i % 4 == 3:  # learned centroids: a random unit table per KV head
         table = rng.standard_normal((hkv, 16, 256, 8)).astype(np.float32)
         table /= np.linalg.norm(table, axis=-1, keepdims=True)
+    host = 1 if i % 6 == 5 else 0  # every sixth case: Retrieval K/V in mapped host memory
     return dict(T=S + N + L, batch=b, n_kv_heads=hkv, n_q_heads=hkv * G, sink=S, local=L, update_buf=U,
-                topk=k, cand_bp=cand_bp, rho=rho, topk_order=order, seed=2000 + i, table=table)
+                topk=k, cand_bp=cand_bp, rho=rho, topk_order=order, seed=2000 + i, table=table,
+                retrieval_on_host=host)
 
 
 @pytest.mark.parametrize("i", range(CASES))
