@@ -118,3 +118,47 @@ def test_lists_crowded_into_a_few_slices(hq):
     qd = g.to_dev(g.queries_from_zone(c), torch.bfloat16)
     _, sizes = check_gqa(c, qd, idx, 1024)
     assert sizes[(0, 0)] == hq * 1024
+
+
+def test_gqa_and_dense_right_after_decode_steps_see_the_step_token():
+    """paris_sparse_attend_gqa and paris_dense_attend enqueued on the same
+    stream directly behind paris_decode_step (no host synchronisation) read
+    the window as the step left it, its own token included (through a flush
+    every 16 steps), and match the oracle over the window plus the union of
+    the group's top-k sets, and over every cached token."""
+    c = g.make_case(16 + 12000 + 64, seed=67, batch=1, n_kv_heads=2, n_q_heads=8, sink=16, local=64,
+                    update_buf=16, topk=128, cand_bp=500)
+    b, hq, d, k = 1, 8, 128, 128
+    for t in range(36):
+        kn = synth.decode_keys(67, b, 2, t, d, c.scale)
+        vn = synth.decode_values(67, b, 2, t, d)
+        q = g.queries_from_zone(c, step=t)
+        qd = g.to_dev(q, torch.bfloat16)
+        idx = torch.empty((b, hq, k), dtype=torch.int32, device="cuda")
+        sc = torch.empty((b, hq, k), dtype=torch.float32, device="cuda")
+        o_step = torch.empty((b, hq, d), dtype=torch.bfloat16, device="cuda")
+        o_gqa = torch.full((b, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        o_dense = torch.full((b, hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        k_eff = c.ctx.paris_decode_step(g.to_dev(kn, torch.bfloat16), g.to_dev(vn, torch.bfloat16), qd, idx, sc,
+                                        o_step)
+        c.ctx.paris_sparse_attend_gqa(qd, idx, o_gqa)
+        c.ctx.paris_dense_attend(qd, o_dense)
+        torch.cuda.synchronize()
+        c.ctx.paris_check_device()
+        g.append(c, kn, vn, device=False)
+        if t % 6 == 5:
+            q_seen = qd.float().cpu().numpy()
+            idx_h = idx.cpu().numpy()
+            got_g, got_d = o_gqa.float().cpu().numpy(), o_dense.float().cpu().numpy()
+            Kb, Vb = g.as_seen(c.K, torch.bfloat16), g.as_seen(c.V, torch.bfloat16)
+            z = c.zones
+            for qh in range(hq):
+                kvh = qh // c.G
+                group = idx_h[0, kvh * c.G:(kvh + 1) * c.G, :k_eff]
+                rows = np.concatenate([z.sink(), z.local(), z.buffer(), np.unique(group[group >= 0])])
+                rows = rows.astype(np.int64)
+                ref = o.attention(q_seen[0, qh], Kb[0, kvh, rows], Vb[0, kvh, rows])
+                assert np.max(np.abs(got_g[0, qh] - ref)) <= g.ATTN_ATOL, (t, qh)
+                ref = o.attention(q_seen[0, qh], Kb[0, kvh, :z.T], Vb[0, kvh, :z.T])
+                assert np.max(np.abs(got_d[0, qh] - ref)) <= g.ATTN_ATOL, (t, qh)
+    assert c.ctx.paris_get_state()["n_flushes"] >= 2
