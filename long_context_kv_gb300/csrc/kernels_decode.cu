@@ -112,10 +112,9 @@ struct DecodeArgs {
   int rho, flat, nbins, cpb, nchunk_active;
   int64_t N, C, k, k_eff, cmax;
   int64_t nsink, nwin;  // attention window rows
-  // cut points q = 0 .. kClusterMax (C q / CS and nwin q / CS, clamped at
-  // q = CS): the rerank slices of the candidate list and the blocks' shares
-  // of the window rows
-  int64_t ccut[kClusterMax + 1], wcut[kClusterMax + 1];
+  // cut points q = 0 .. kClusterMax (C q / CS, clamped at q = CS): the
+  // rerank slices of the candidate list
+  int64_t ccut[kClusterMax + 1];
   int64_t rcut[kClusterMax + 1];  // (nwin + k_eff) q / CS: the blocks' shares of the attention rows (the last one
                                   // smaller when it also sorts the top-k)
   uint32_t nmod;        // ring slot of the first Local token
@@ -825,27 +824,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     if (a.new_pos >= 0 && r == 0 && qh % a.s.g == 0)
       append_token_warp(a.k_new, a.v_new, a.kvdtype, a.new_pos, sh, lane, a.s, a.kv, a.t, a.sm, a.rp,
                         kTable ? a.t.cent : nullptr);
-  } else if (warp > kSub + 1) {
-    // warm L2 with the window rows this block's attention will read
-    if (a.out != nullptr) {
-      const int64_t w_lo = cut_at(a.wcut, r), w_hi = cut_at(a.wcut, r + 1);
-      const int ring = a.s.local + a.s.ubuf;
-      const uint32_t nmod = a.nmod;
-      for (int64_t row = w_lo + (tid - (kSub + 2) * 32); row < w_hi; row += kThreads - (kSub + 2) * 32) {
-        int64_t slot = row;
-        if (row >= a.nsink) {
-          uint32_t x = nmod + (uint32_t)(row - a.nsink);
-          if (x >= (uint32_t)ring) x -= (uint32_t)ring;
-          slot = a.s.sink + x;
-        }
-        const __nv_bfloat16* kp = a.kv.win_k + (sh * a.kv.win + slot) * kDim;
-        const __nv_bfloat16* vp = a.kv.win_v + (sh * a.kv.win + slot) * kDim;
-        prefetch_l2(kp);
-        prefetch_l2(kp + 64);
-        prefetch_l2(vp);
-        prefetch_l2(vp + 64);
-      }
-    }
   } else if (warp < kSub) {
     const int b = warp;
     // the lane's centroids are lane + 32 i: bits 0-4 of the id are the lane's,
@@ -1842,7 +1820,6 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t st) {
   for (int q = 0; q <= kClusterMax; ++q) {
     const int qq = q < cs ? q : cs;
     a.ccut[q] = ra.C * qq / cs;
-    a.wcut[q] = L.nwin * qq / cs;
     a.rcut[q] = (L.nwin + ra.k_eff) * qq / cs;
   }
   {
