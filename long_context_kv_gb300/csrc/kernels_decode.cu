@@ -157,7 +157,6 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 
 // Cluster barrier: every thread of every block of the cluster arrives; the
 // writes before it (shared and global) are visible to the cluster after it.
@@ -1224,9 +1223,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(DecodeArgs a) {
     for (uint32_t c0 = 32 * warp; c0 < nown; c0 += kThreads) {
       const uint32_t i = c0 + lane;
       const int32_t pm = i < nown ? cand_pos(i) : -1;
-      // the next round's records start on their way to L2 now
-      const uint32_t inx = i + kThreads;
-      if (inx < nown) prefetch_l2(rec + (int64_t)(cand_pos(inx) - a.s.sink) * kRecBytes);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int rc = 4 * u + (lane >> 3), piece = lane & 7;
